@@ -1,0 +1,436 @@
+"""Pins of the fp64 oracle to facts outside itself (CPU only).
+
+Each test checks the oracle against something it does not share code with:
+hand-derived golden values (tests/golden/, with their derivations), closed
+forms of softmax attention, invariants the definition fixes, and special
+cases that reduce to library routines (torch's binary32->bf16 rounding,
+torch complex multiplication, torch scaled_dot_product_attention in fp64).
+"""
+
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+import oracle
+from paged_kv_gqa_16_gb300 import workloads as wl
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# ----------------------------------------------------------------- bf16 ---
+def _golden_rows(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                yield line
+
+
+def test_bf16_rne_golden():
+    n = 0
+    for row in _golden_rows("bf16_rne.txt"):
+        x_hex, bits_hex = row.split()[:2]
+        x = float.fromhex(x_hex)
+        got = int(oracle.bf16_round(np.array([x]))[0])
+        assert got == int(bits_hex, 16), f"{x_hex}: got {got:#06x}, want {bits_hex}"
+        n += 1
+    assert n >= 15
+
+
+def test_bf16_rne_matches_torch_on_binary32_values():
+    # For inputs already in binary32 there is one rounding only, and torch's
+    # float -> bfloat16 conversion is round-to-nearest-even.
+    g = torch.Generator().manual_seed(1)
+    bits = torch.randint(0, 2**31 - 1, (200000,), generator=g, dtype=torch.int64)
+    bits = bits.to(torch.int32)
+    f = bits.view(torch.float32)
+    f = f[torch.isfinite(f)]
+    # plenty of exact ties: low 16 bits = 0x8000
+    ties = (torch.randint(0, 2**15, (5000,), generator=g, dtype=torch.int32) << 16) | 0x8000
+    f = torch.cat([f, ties.view(torch.float32), -f[:1000]])
+    f = f[torch.isfinite(f)]
+    want = f.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    got = oracle.bf16_round(f.to(torch.float64).numpy())
+    assert np.array_equal(got, want)
+
+
+def test_bf16_widening_is_exact_roundtrip():
+    allbits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    x = oracle.bf16_to_f64(allbits)
+    finite = np.isfinite(x)
+    back = oracle.bf16_round(x[finite])
+    assert np.array_equal(back, allbits[finite])
+    ref = torch.from_numpy(allbits.astype(np.int16)).view(torch.bfloat16).to(torch.float64)
+    assert np.array_equal(x[finite], ref.numpy()[finite])
+
+
+# ----------------------------------------------------------------- RoPE ---
+def _eval_expr(s):
+    return float(eval(s, {"cos": math.cos, "sin": math.sin, "__builtins__": {}}))
+
+
+def test_rope_golden():
+    n = 0
+    for row in _golden_rows("rope_cases.txt"):
+        D, base, pos, xs, ys = [c.strip() for c in row.split("|")]
+        x = np.array([float(v) for v in xs.split(",")])
+        want = np.array([_eval_expr(v) for v in ys.split(",")])
+        got = oracle.rope_rotate(x, int(pos), float(base))
+        assert x.size == int(D)
+        np.testing.assert_allclose(got, want, rtol=0, atol=1e-14)
+        n += 1
+    assert n >= 6
+
+
+def _torch_complex_rope(x, pos, base):
+    # The pages' training path: view pairs as complex numbers, multiply by
+    # a unit phasor built with torch.polar.
+    D = x.size
+    i = torch.arange(D // 2, dtype=torch.float64)
+    theta = base ** (-2.0 * i / D)
+    rot = torch.polar(torch.ones_like(theta), pos * theta)
+    xc = torch.view_as_complex(torch.from_numpy(x.copy()).view(D // 2, 2))
+    return torch.view_as_real(xc * rot).reshape(D).numpy()
+
+
+@pytest.mark.parametrize("D", [8, 64, 128])
+@pytest.mark.parametrize("pos", [0, 1, 17, 1023, 32767])
+def test_rope_matches_torch_complex_multiply(D, pos):
+    x = np.random.default_rng(D + pos).standard_normal(D)
+    got = oracle.rope_rotate(x, pos, 10000.0)
+    want = _torch_complex_rope(x, pos, 10000.0)
+    np.testing.assert_allclose(got, want, rtol=0, atol=1e-12)
+
+
+def test_rope_invariants():
+    rng = np.random.default_rng(3)
+    D = 64
+    q = rng.standard_normal(D)
+    k = rng.standard_normal(D)
+    # pair norms preserved
+    y = oracle.rope_rotate(q, 777, 10000.0)
+    np.testing.assert_allclose(np.hypot(y[0::2], y[1::2]), np.hypot(q[0::2], q[1::2]),
+                               rtol=1e-14)
+    # composition: R_a R_b = R_{a+b}
+    y2 = oracle.rope_rotate(oracle.rope_rotate(q, 300, 10000.0), 477, 10000.0)
+    np.testing.assert_allclose(y2, y, atol=1e-11)
+    # inner product depends only on the position difference
+    a = oracle.rope_rotate(q, 50, 10000.0) @ oracle.rope_rotate(k, 20, 10000.0)
+    b = oracle.rope_rotate(q, 1030, 10000.0) @ oracle.rope_rotate(k, 1000, 10000.0)
+    assert abs(a - b) < 1e-10
+
+
+# --------------------------------------------------------------- append ---
+def _bits(t):
+    return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def test_append_touches_exactly_the_new_slots():
+    w = wl.tiny()
+    kp, vp = w.full_pool_host()
+    q2, kp2, vp2 = oracle.append(w.host("q"), w.host("k_new"), w.host("v_new"), kp, vp,
+                                 w.host("kv_indices"), w.host("kv_indptr"),
+                                 w.host("seq_lens"), rope_base=10000.0, rope_q=False)
+    assert np.array_equal(q2, w.host("q"))
+    changed_k = np.argwhere(kp2 != kp)
+    changed_v = np.argwhere(vp2 != vp)
+    # every element of the new slot was NaN before and is finite after
+    assert len(changed_k) == w.B * w.Hkv * w.D
+    assert len(changed_v) == w.B * w.Hkv * w.D
+    idx = w.kv_indices.numpy()
+    ptr = w.kv_indptr.numpy()
+    for b in range(w.B):
+        pos = int(w.seq_lens[b]) - 1
+        page = idx[ptr[b] + pos // w.page_size]
+        slot = pos % w.page_size
+        # V is copied unchanged
+        assert np.array_equal(vp2[page, slot], w.host("v_new")[b])
+        # K is the rotated new key, rounded once
+        kf = oracle.bf16_to_f64(w.host("k_new")[b])
+        for g in range(w.Hkv):
+            want = _torch_complex_rope(kf[g], pos, 10000.0)
+            got = oracle.bf16_to_f64(kp2[page, slot, g])
+            # bf16 spacing near |want| bounds a single rounding
+            assert np.all(np.abs(got - want) <= np.abs(want) * 2.0**-8 + 1e-30)
+
+
+def test_append_position_zero_is_identity_and_rope_q():
+    w = wl.build("p0", B=3, Hq=4, Hkv=2, D=16, page_size=4, seq_lens=[1, 5, 9], seed=5)
+    kp, vp = w.full_pool_host()
+    q2, kp2, vp2 = oracle.append(w.host("q"), w.host("k_new"), w.host("v_new"), kp, vp,
+                                 w.host("kv_indices"), w.host("kv_indptr"),
+                                 w.host("seq_lens"), rope_base=10000.0, rope_q=True)
+    idx, ptr = w.kv_indices.numpy(), w.kv_indptr.numpy()
+    # row 0: position 0, cos = 1, sin = 0 -> bit-identical K and q
+    assert np.array_equal(kp2[idx[ptr[0]], 0], w.host("k_new")[0])
+    assert np.array_equal(q2[0], w.host("q")[0])
+    # rows 1, 2: q rotated by the same position as K
+    for b in (1, 2):
+        pos = int(w.seq_lens[b]) - 1
+        qf = oracle.bf16_to_f64(w.host("q")[b])
+        for h in range(w.Hq):
+            want = _torch_complex_rope(qf[h], pos, 10000.0)
+            got = oracle.bf16_to_f64(q2[b, h])
+            assert np.all(np.abs(got - want) <= np.abs(want) * 2.0**-8 + 1e-30)
+
+
+def test_append_without_rope_copies_k():
+    w = wl.build("norope", B=2, Hq=2, Hkv=1, D=8, page_size=2, seq_lens=[3, 6], seed=6)
+    kp, vp = w.full_pool_host()
+    _, kp2, _ = oracle.append(w.host("q"), w.host("k_new"), w.host("v_new"), kp, vp,
+                              w.host("kv_indices"), w.host("kv_indptr"), w.host("seq_lens"),
+                              rope_base=None, rope_q=False)
+    idx, ptr = w.kv_indices.numpy(), w.kv_indptr.numpy()
+    for b in range(2):
+        pos = int(w.seq_lens[b]) - 1
+        assert np.array_equal(kp2[idx[ptr[b] + pos // 2], pos % 2], w.host("k_new")[b])
+
+
+# --------------------------------------------------------------- decode ---
+def _torch_gather_sdpa(q_bits, kp_bits, vp_bits, kv_indices, kv_indptr, seq_lens, scale):
+    """Independent route: torch indexing gathers each row's pages, then
+    torch SDPA (fp64, enable_gqa) computes the attention."""
+    to64 = lambda a: torch.from_numpy(a.astype(np.int16)).view(torch.bfloat16).to(torch.float64)
+    q, kp, vp = to64(q_bits), to64(kp_bits), to64(vp_bits)
+    B, Hq, D = q.shape
+    P, ps, Hkv, _ = kp.shape
+    out = torch.zeros(B, Hq, D, dtype=torch.float64)
+    for b in range(B):
+        L = int(seq_lens[b])
+        if L == 0:
+            continue
+        pages = torch.from_numpy(kv_indices[kv_indptr[b]:kv_indptr[b + 1]].astype(np.int64))
+        K = kp[pages].reshape(-1, Hkv, D)[:L].permute(1, 0, 2)[None]
+        V = vp[pages].reshape(-1, Hkv, D)[:L].permute(1, 0, 2)[None]
+        o = F.scaled_dot_product_attention(q[b][None, :, None, :], K, V, scale=scale,
+                                           enable_gqa=True)
+        out[b] = o[0, :, 0, :]
+    return out.numpy()
+
+
+def _decode_case(w, full=True):
+    if full:
+        kp, vp = w.full_pool_host()
+        idx = w.host("kv_indices")
+    else:
+        kp, vp, idx = w.compact_host()
+    return (w.host("q"), kp, vp, idx, w.host("kv_indptr"), w.host("seq_lens"))
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(4, 4), (4, 2), (8, 2), (16, 2), (8, 1), (16, 16)])
+@pytest.mark.parametrize("ps", [1, 3, 16, 32])
+def test_decode_matches_torch_sdpa(Hq, Hkv, ps):
+    lens = [0, 1, 2, 15, 16, 17, 33, 70]
+    w = wl.build("sdpa", B=len(lens), Hq=Hq, Hkv=Hkv, D=64, page_size=ps, seq_lens=lens,
+                 seed=Hq * 100 + Hkv * 10 + ps, fill_new_slot=True)
+    args = _decode_case(w)
+    got = oracle.decode(*args, scale=w.scale)
+    want = _torch_gather_sdpa(*args, scale=w.scale)
+    assert np.all(np.isfinite(got))
+    np.testing.assert_allclose(got, want, rtol=0, atol=1e-12)
+    assert np.all(got[0] == 0.0)            # seq_len 0 row -> zeros
+
+
+def test_decode_tiny_after_append_is_finite_and_matches_sdpa():
+    w = wl.tiny()
+    kp, vp = w.full_pool_host()
+    _, kp2, vp2 = oracle.append(w.host("q"), w.host("k_new"), w.host("v_new"), kp, vp,
+                                w.host("kv_indices"), w.host("kv_indptr"),
+                                w.host("seq_lens"), rope_base=10000.0, rope_q=False)
+    args = (w.host("q"), kp2, vp2, w.host("kv_indices"), w.host("kv_indptr"),
+            w.host("seq_lens"))
+    got = oracle.decode(*args, scale=w.scale)
+    assert np.all(np.isfinite(got))         # NaN tails / unreferenced pages unread
+    np.testing.assert_allclose(got, _torch_gather_sdpa(*args, scale=w.scale), atol=1e-12)
+
+
+def _single_row(K, V, qv, ps=4):
+    """Pool holding one row (one kv head) with keys K [L,D] and values V."""
+    L, D = K.shape
+    n = -(-L // ps)
+    kp = np.full((n, ps, 1, D), wl.NAN_BF16_BITS, dtype=np.uint16)
+    vp = kp.copy()
+    for t in range(L):
+        kp[t // ps, t % ps, 0] = oracle.bf16_round(K[t])
+        vp[t // ps, t % ps, 0] = oracle.bf16_round(V[t])
+    q = oracle.bf16_round(qv)[None, None, :]
+    return q, kp, vp, np.arange(n, dtype=np.int32), np.array([0, n], np.int32), \
+        np.array([L], np.int32)
+
+
+def _exact_bf16(x):
+    return oracle.bf16_to_f64(oracle.bf16_round(x))
+
+
+def test_closed_form_single_token_returns_v0():
+    rng = np.random.default_rng(0)
+    K, V, qv = rng.standard_normal((1, 32)), rng.standard_normal((1, 32)), rng.standard_normal(32)
+    out = oracle.decode(*_single_row(K, V, qv), scale=0.3)
+    assert np.array_equal(out[0, 0], _exact_bf16(V[0]))
+
+
+def test_closed_form_identical_keys_give_mean_v():
+    rng = np.random.default_rng(1)
+    L, D = 37, 16
+    K = np.tile(rng.standard_normal(D), (L, 1))
+    V = rng.standard_normal((L, D))
+    out = oracle.decode(*_single_row(K, V, rng.standard_normal(D)), scale=1.0)
+    np.testing.assert_allclose(out[0, 0], _exact_bf16(V).mean(axis=0), atol=1e-14)
+
+
+def test_closed_form_zero_query_gives_mean_v():
+    rng = np.random.default_rng(2)
+    L, D = 21, 16
+    K, V = rng.standard_normal((L, D)), rng.standard_normal((L, D))
+    out = oracle.decode(*_single_row(K, V, np.zeros(D)), scale=1.0)
+    np.testing.assert_allclose(out[0, 0], _exact_bf16(V).mean(axis=0), atol=1e-14)
+
+
+def test_closed_form_dominant_key():
+    # one key aligned with a large query: its weight is 1 up to exp(-gap)
+    L, D = 10, 8
+    K = np.zeros((L, D))
+    K[6, 0] = 1.0
+    V = np.arange(L * D, dtype=np.float64).reshape(L, D) / 64.0
+    qv = np.zeros(D)
+    qv[0] = 64.0
+    out = oracle.decode(*_single_row(K, V, qv), scale=1.0)   # gap = 64
+    want = _exact_bf16(V[6])
+    bound = (L - 1) * math.exp(-64.0) * np.abs(_exact_bf16(V)).max() * 2
+    assert np.max(np.abs(out[0, 0] - want)) <= bound
+
+
+def test_two_token_closed_form():
+    # scores s0, s1: out = (v0 + e^(s1-s0) v1) / (1 + e^(s1-s0))
+    D = 8
+    K = np.zeros((2, D))
+    K[0, 0], K[1, 1] = 1.0, 1.0
+    qv = np.zeros(D)
+    qv[0], qv[1] = 0.5, 2.0                      # s = 0.5, 2.0 at scale 1
+    V = np.array([[1.0] * D, [-3.0] * D])
+    out = oracle.decode(*_single_row(K, V, qv), scale=1.0)
+    e = math.exp(1.5)
+    np.testing.assert_allclose(out[0, 0], (1.0 - 3.0 * e) / (1.0 + e), atol=1e-15)
+
+
+def test_gqa_head_mapping():
+    # V of kv head g is the constant g+1, so query head h must return
+    # h // n_rep + 1 whatever the scores are.
+    Hq, Hkv, D, ps = 8, 2, 16, 4
+    w = wl.build("map", B=2, Hq=Hq, Hkv=Hkv, D=D, page_size=ps, seq_lens=[5, 11], seed=9,
+                 fill_new_slot=True)
+    q, kp, vp, idx, ptr, sl = _decode_case(w, full=False)
+    vp = vp.copy()
+    for g in range(Hkv):
+        vp[:, :, g, :] = oracle.bf16_round(np.full(vp[:, :, g, :].shape, g + 1.0))
+    out = oracle.decode(q, kp, vp, idx, ptr, sl, scale=w.scale)
+    for h in range(Hq):
+        np.testing.assert_allclose(out[:, h, :], h // (Hq // Hkv) + 1.0, atol=1e-14)
+
+
+def test_page_permutation_invariance_is_bitwise():
+    w = wl.build("perm", B=3, Hq=8, Hkv=2, D=32, page_size=4, seq_lens=[9, 30, 4],
+                 seed=11, fill_new_slot=True)
+    q, kp, vp, idx, ptr, sl = _decode_case(w, full=False)
+    out = oracle.decode(q, kp, vp, idx, ptr, sl, scale=w.scale)
+    perm = np.random.default_rng(4).permutation(kp.shape[0])
+    inv = np.argsort(perm)
+    out2 = oracle.decode(q, kp[perm], vp[perm], inv[idx].astype(np.int32), ptr, sl,
+                         scale=w.scale)
+    assert np.array_equal(out, out2)
+
+
+def test_contiguous_equals_paged_bitwise():
+    w = wl.build("contig", B=2, Hq=4, Hkv=2, D=32, page_size=8, seq_lens=[40, 17],
+                 seed=12, fill_new_slot=True)
+    q, kp, vp, idx, ptr, sl = _decode_case(w, full=False)
+    out_paged = oracle.decode(q, kp, vp, idx, ptr, sl, scale=w.scale)
+    # one page per row, page_size = 40 (the longest row): a contiguous layout
+    Lmax = 40
+    kc = np.full((2, Lmax, 2, 32), wl.NAN_BF16_BITS, np.uint16)
+    vc = kc.copy()
+    for b in range(2):
+        K, V = oracle.gather(b, 0, kp, vp, idx, ptr, sl)
+        for g in range(2):
+            K, V = oracle.gather(b, g, kp, vp, idx, ptr, sl)
+            kc[b, :sl[b], g] = oracle.bf16_round(K)
+            vc[b, :sl[b], g] = oracle.bf16_round(V)
+    out_c = oracle.decode(q, kc, vc, np.array([0, 1], np.int32),
+                          np.array([0, 1, 2], np.int32), sl, scale=w.scale)
+    assert np.array_equal(out_paged, out_c)
+
+
+def test_decode_rejects_out_of_range_pages():
+    w = wl.build("bad", B=1, Hq=2, Hkv=1, D=8, page_size=4, seq_lens=[6], seed=13,
+                 fill_new_slot=True)
+    q, kp, vp, idx, ptr, sl = _decode_case(w, full=False)
+    with pytest.raises(ValueError):
+        oracle.decode(q, kp, vp, np.array([0, kp.shape[0]], np.int32), ptr, sl, scale=1.0)
+    with pytest.raises(ValueError):   # table shorter than the row
+        oracle.decode(q, kp, vp, idx, np.array([0, 1], np.int32), sl, scale=1.0)
+
+
+# ------------------------------------------------------ split + combine ---
+@pytest.mark.parametrize("chunk", [1, 5, 16, 48, 200])
+def test_split_then_combine_equals_direct(chunk):
+    lens = [0, 1, 16, 47, 100, 161]
+    w = wl.build("split", B=len(lens), Hq=8, Hkv=2, D=32, page_size=16, seq_lens=lens,
+                 seed=21, fill_new_slot=True)
+    args = _decode_case(w, full=False)
+    direct = oracle.decode(*args, scale=w.scale)
+    S = -(-max(lens) // chunk)
+    o, ml = oracle.decode_partials(*args, scale=w.scale, num_splits=S, chunk=chunk)
+    merged = oracle.combine(o, ml)
+    np.testing.assert_allclose(merged, direct, rtol=0, atol=1e-13)
+    # splits past the end of a row are empty
+    for b, L in enumerate(lens):
+        n_act = -(-L // chunk)
+        assert np.all(ml[b, :, n_act:, 0] == -np.inf)
+        assert np.all(ml[b, :, n_act:, 1] == 0.0)
+        assert np.all(ml[b, :, :n_act, 1] >= 1.0)     # l >= 1: the max term is e^0
+
+
+def test_single_split_statistics():
+    rng = np.random.default_rng(5)
+    L, D = 13, 8
+    K, V, qv = rng.standard_normal((L, D)), rng.standard_normal((L, D)), rng.standard_normal(D)
+    args = _single_row(K, V, qv)
+    o, ml = oracle.decode_partials(*args, scale=0.5, num_splits=1, chunk=64)
+    s = 0.5 * (_exact_bf16(K) @ _exact_bf16(qv))
+    assert ml[0, 0, 0, 0] == pytest.approx(s.max(), abs=1e-14)
+    assert ml[0, 0, 0, 1] == pytest.approx(np.exp(s - s.max()).sum(), rel=1e-14)
+    np.testing.assert_allclose(o[0, 0, 0], oracle.decode(*args, scale=0.5)[0, 0], atol=1e-15)
+
+
+def test_combine_rules():
+    rng = np.random.default_rng(6)
+    B, Hq, S, D = 2, 3, 5, 8
+    o = rng.standard_normal((B, Hq, S, D)).astype(np.float32)
+    ml = np.stack([rng.standard_normal((B, Hq, S)) * 3,
+                   rng.uniform(0.5, 20, (B, Hq, S))], axis=-1).astype(np.float32)
+    out = oracle.combine(o, ml)
+    # brute force in the plain weighted-average form
+    w = ml[..., 1].astype(np.float64) * np.exp(ml[..., 0].astype(np.float64))
+    want = (w[..., None] * o).sum(2) / w.sum(2)[..., None]
+    np.testing.assert_allclose(out, want, rtol=1e-12)
+    # order of splits does not matter
+    p = rng.permutation(S)
+    np.testing.assert_allclose(oracle.combine(o[:, :, p], ml[:, :, p]), out, rtol=1e-13)
+    # an empty split (l = 0, m = -inf, garbage o) contributes nothing
+    o2, ml2 = o.copy(), ml.copy()
+    o2[:, :, 2] = np.nan
+    ml2[:, :, 2] = (-np.inf, 0.0)
+    keep = [0, 1, 3, 4]
+    np.testing.assert_allclose(oracle.combine(o2, ml2), oracle.combine(o[:, :, keep],
+                                                                       ml[:, :, keep]),
+                               rtol=1e-13)
+    # every split empty -> zeros; one split -> its own output
+    ml3 = ml.copy()
+    ml3[..., 0], ml3[..., 1] = -np.inf, 0.0
+    assert np.all(oracle.combine(o, ml3) == 0.0)
+    np.testing.assert_array_equal(oracle.combine(o[:, :, :1], ml[:, :, :1]),
+                                  o[:, :, 0].astype(np.float64))
