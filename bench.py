@@ -1,0 +1,474 @@
+#!/usr/bin/env python3
+"""Benchmark of one decode step of paged GQA attention on GB300.
+
+A step is the whole hot path over one batch: fused RoPE + K/V append, the
+split-KV decode kernel and the combine (the split count comes from the
+library's planner).  The default workload is the batched ragged decode
+(B=32, Hq=32, Hkv=8, D=128, page_size=16, seq_lens uniform in [512, 4096],
+pages scattered over a 65536-page pool).
+
+Printed: one JSON line.  ``value`` is the KV-read throughput of the step:
+the bytes of K and V the attention must read (every token of every row,
+every kv head) divided by the step time, summed over ranks.  The L2 is
+flushed (a 2x-L2 write) between timed steps, outside the timed events.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                  [--splits S] [--pool-pages P] [--impl pkv|reference]
+
+``--impl reference`` times the fp64 CPU oracle on the host cores instead (a
+bounded sample of the same workload each step).  Under torchrun (N > 1)
+each rank runs an independent replica on its own GPU (replicas only: the
+path has no exchange step); timings are max-reduced over ranks.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "paged GQA decode attn: µs/call and KV-read GB/s (% of GB300 HBM peak)"
+FALLBACK_HBM_GBS = 6800.0
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "split_decode_traffic.json")
+DECODE_SRC = os.path.join(ROOT, "paged_kv_gqa_16_gb300", "csrc", "pkv_decode.cu")
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default="ragged_b32")
+    ap.add_argument("--splits", type=int, default=0, help="override the planner's split count")
+    ap.add_argument("--pool-pages", type=int, default=0,
+                    help="pool size override (smaller pools for profiling captures)")
+    ap.add_argument("--impl", choices=["pkv", "reference"], default="pkv")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-flush", action="store_true", help="skip the L2 flush (not for reporting)")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0,
+                    help="target CPU time of the oracle baseline sample")
+    return ap.parse_args(argv)
+
+
+# --------------------------------------------------------------------------
+def dist_info():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def init_dist(world: int, backend: str):
+    if world <= 1:
+        return None
+    import torch.distributed as dist
+    if not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return dist
+
+
+def reduce_max(value: float, world: int, device=None) -> float:
+    """Max of a float over ranks (identity for one rank)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int, device=None):
+    if world <= 1:
+        return
+    import torch.distributed as dist
+    if device is not None and dist.get_backend() == "nccl":
+        dist.barrier(device_ids=[device.index])
+    else:
+        dist.barrier()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            j = json.load(f)
+        return float(j["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def cached_traffic(workload: str, splits: int):
+    """DRAM bytes per split-decode launch from a committed ncu summary, valid
+    only while the kernel source is unchanged (else None)."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            j = json.load(f)
+        src_hash = hashlib.sha256(open(DECODE_SRC, "rb").read()).hexdigest()
+        if j.get("source_sha256") != src_hash:
+            return None
+        e = j.get("workloads", {}).get(workload)
+        if e is None or (e.get("splits") not in (None, splits)):
+            return None
+        return float(e["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, period_ms: int = 50):
+        self.gpu = gpu_index
+        self.period = period_ms
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", f"-lms={self.period}"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.perf_counter(), line.strip()))
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            if self.thread is not None:
+                self.thread.join(timeout=2)
+
+    def summary(self, t0=None, t1=None):
+        """Median SM clock and active throttle reasons over the samples read
+        inside [t0, t1] (host perf_counter times)."""
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ts, line in self.lines:
+            if t0 is not None and not (t0 <= ts <= t1):
+                continue
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def oracle_sample(w, target_s: float, max_reps: int = 50):
+    """Time the fp64 oracle's step (append + decode) on the host cores over a
+    bounded sample of the workload: whole rows, taken in order until their
+    estimated cost reaches the target, repeated while time remains."""
+    import numpy as np
+    import oracle
+    from paged_kv_gqa_16_gb300 import workloads as wl
+
+    cores = cpu_cores()
+    oracle.set_threads(cores)
+    kp, vp, idx = w.compact_host()
+    lens = w.seq_lens.numpy()
+    ptr = w.kv_indptr.numpy()
+
+    def run(rows):
+        b0, b1 = rows
+        sub_ptr = (ptr[b0:b1 + 1] - ptr[b0]).astype(np.int32)
+        p0, p1 = int(ptr[b0]), int(ptr[b1])
+        sl = lens[b0:b1].astype(np.int32)
+        q2, kp2, vp2 = oracle.append(w.host("q")[b0:b1], w.host("k_new")[b0:b1],
+                                     w.host("v_new")[b0:b1], kp[p0:p1], vp[p0:p1],
+                                     np.arange(p1 - p0, dtype=np.int32), sub_ptr, sl,
+                                     rope_base=w.rope_base, rope_q=True)
+        oracle.decode(q2, kp2, vp2, np.arange(p1 - p0, dtype=np.int32), sub_ptr, sl, w.scale)
+        return int(sl.sum())
+
+    # calibrate on the first row
+    t0 = time.perf_counter()
+    tok1 = run((0, 1))
+    dt1 = max(time.perf_counter() - t0, 1e-6)
+    per_tok = dt1 / max(tok1, 1)
+    budget_tok = target_s / per_tok
+    b1 = 1
+    while b1 < w.B and lens[:b1 + 1].sum() <= budget_tok:
+        b1 += 1
+    tokens = 0
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        tokens += run((0, b1))
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= target_s * 0.5 or reps >= max_reps:
+            break
+    el = time.perf_counter() - t0
+    bytes_kv = tokens * w.Hkv * w.D * 2 * 2
+    return {"seconds": el, "tokens": tokens, "rows": b1, "reps": reps, "cores": cores,
+            "gbs": bytes_kv / el / 1e9}
+
+
+# --------------------------------------------------------------------------
+def run_reference(args):
+    """The oracle, timed as the reference arm: each step is a bounded sample
+    of the workload on the host cores."""
+    rank, world, _ = dist_info()
+    if rank != 0:
+        return 0
+    from paged_kv_gqa_16_gb300 import workloads as wl
+    import oracle
+    oracle.build()
+    w = wl.make(args.workload)
+    steps, warm = max(1, args.steps), max(0, args.warmup)
+    # keep the whole run within a few minutes: per-step sample ~ budget/(steps+warm)
+    per_step = max(0.05, min(2.0, 120.0 / (steps + warm)))
+    for _ in range(min(warm, 3)):
+        oracle_sample(w, per_step, max_reps=1)
+    tot_s, tot_tok = 0.0, 0
+    res = None
+    for _ in range(steps):
+        res = oracle_sample(w, per_step, max_reps=1)
+        tot_s += res["seconds"]
+        tot_tok += res["tokens"]
+    gbs = tot_tok * w.Hkv * w.D * 4 / tot_s / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": steps, "warmup": warm,
+        "ms_per_step": round(1e3 * tot_s / steps, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D,
+                   "page_size": w.page_size, "num_pages": w.num_pages},
+        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": res["cores"],
+                         "kind": "oracle",
+                         "sample": f"fp64 oracle append+decode on rows 0..{res['rows'] - 1} of "
+                                   f"{w.name} per step"},
+        "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_pkv(args):
+    import torch
+    from paged_kv_gqa_16_gb300 import build as pkv_build
+    from paged_kv_gqa_16_gb300 import pkv
+    from paged_kv_gqa_16_gb300 import workloads as wl
+
+    rank, world, local = dist_info()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device (the library has no CPU path)")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    init_dist(world, "nccl")
+    if rank == 0:
+        pkv_build.build()
+    barrier(world, dev)
+    pkv.lib()
+
+    # each rank: an independent replica of the workload (own seed)
+    w = wl.make(args.workload, seed=rank)
+    t = w.to_device(dev, pool_pages=args.pool_pages or None)
+    P = t["k_pool"].shape[0]
+    d = pkv.dims(w.B, w.Hq, w.Hkv, w.D, w.page_size, P, int(w.kv_indices.numel()),
+                 w.max_seq_len, w.scale)
+    S = args.splits or pkv.plan(d)[0]
+    ws = pkv.alloc_workspace(d, S, dev)
+    o_part, ml_part = pkv.partial_views(d, S, ws)
+    rope_rows = max(w.max_seq_len, 1)
+    rope = torch.empty(rope_rows, w.D // 2, 2, dtype=torch.float32, device=dev)
+    pkv.rope_table(rope, rope_rows, w.D, w.rope_base or 10000.0)
+    out = torch.empty(w.B, w.Hq, w.D, dtype=torch.bfloat16, device=dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(q, k_new, v_new, kv_indices, kv_indptr, seq_lens, ev=None):
+        pkv.paged_kv_append(d, q, k_new, v_new, t["k_pool"], t["v_pool"], kv_indices,
+                            kv_indptr, seq_lens, rope_cos_sin=rope, rope_max_pos=rope_rows,
+                            rope_q=True, status=ws, stream=stream)
+        if S == 1:
+            if ev is not None:
+                ev[1].record(stream)
+            pkv.paged_decode_attn(d, q, t["k_pool"], t["v_pool"], kv_indices, kv_indptr,
+                                  seq_lens, 1, ws, out, stream=stream)
+            if ev is not None:
+                ev[2].record(stream)
+        else:
+            # the same two launches paged_decode_attn makes, bracketed apart
+            if ev is not None:
+                ev[1].record(stream)
+            pkv.paged_decode_partials(d, q, t["k_pool"], t["v_pool"], kv_indices, kv_indptr,
+                                      seq_lens, S, ws, stream=stream)
+            if ev is not None:
+                ev[2].record(stream)
+            pkv.decode_combine(d, o_part, ml_part, S, out, stream=stream)
+
+    launches_per_step = 2 if S == 1 else 3
+    dev_args = (t["q"], t["k_new"], t["v_new"], t["kv_indices"], t["kv_indptr"], t["seq_lens"])
+
+    for _ in range(max(3, args.warmup)):
+        step(*dev_args)
+    torch.cuda.synchronize(dev)
+    if pkv.status_word(ws) != 0:
+        raise SystemExit(f"device status {pkv.status_word(ws):#x} after warm-up")
+
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    barrier(world, dev)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(dev.index) as clk:
+        time.sleep(0.4)              # let the sampler start before the timed region
+        wall0 = time.perf_counter()
+        for k in range(K):
+            if not args.no_flush:
+                flush.zero_()
+            ev = evs[k]
+            ev[0].record(stream)
+            step(*dev_args, ev=ev)
+            ev[3].record(stream)
+        torch.cuda.synchronize(dev)
+        wall = time.perf_counter() - wall0
+    barrier(world, dev)
+    step_ms = [e[0].elapsed_time(e[3]) for e in evs]
+    dec_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    ms_step = statistics.mean(step_ms)
+    ms_dec = statistics.mean(dec_ms)
+    ms_step_max = reduce_max(ms_step, world, dev)
+    ms_dec_max = reduce_max(ms_dec, world, dev)
+
+    kv_bytes = w.kv_bytes()
+    total_bytes = kv_bytes * world
+    value = total_bytes / (ms_step_max * 1e-3) / 1e9
+
+    # e2e: host (pinned) inputs copied in, the step, the output copied back
+    e2e = None
+    if not args.no_e2e:
+        host = {k: v.cpu().pin_memory() for k, v in
+                zip(("q", "k_new", "v_new", "kv_indices", "kv_indptr", "seq_lens"),
+                    (w.q, w.k_new, w.v_new, w.kv_indices, w.kv_indptr, w.seq_lens))}
+        dev_in = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
+        out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        h2d = sum(v.numel() * v.element_size() for v in host.values())
+        d2h = out_host.numel() * out_host.element_size()
+        Ke = max(10, min(K, 500))
+        e_evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                 for _ in range(Ke)]
+        torch.cuda.synchronize(dev)
+        for k in range(Ke):
+            if not args.no_flush:
+                flush.zero_()
+            e_evs[k][0].record(stream)
+            for name in host:
+                dev_in[name].copy_(host[name], non_blocking=True)
+            step(dev_in["q"], dev_in["k_new"], dev_in["v_new"], dev_in["kv_indices"],
+                 dev_in["kv_indptr"], dev_in["seq_lens"])
+            out_host.copy_(out, non_blocking=True)
+            e_evs[k][1].record(stream)
+        torch.cuda.synchronize(dev)
+        e_ms = statistics.mean(a.elapsed_time(b) for a, b in e_evs)
+        e_ms = reduce_max(e_ms, world, dev)
+        e2e = {"value": round(total_bytes / (e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+               "ms_per_step": round(e_ms, 5), "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h}
+
+    status = pkv.status_word(ws)
+    if status != 0:
+        raise SystemExit(f"device status {status:#x} after the timed run")
+
+    # roofline of the dominant kernel (the split decode): algorithmic bytes =
+    # K and V of every token + q + page tables, per launch
+    alg_bytes = kv_bytes + w.B * w.Hq * w.D * 2 + 4 * int(w.kv_indices.numel()) + 8 * w.B
+    peak, peak_kind = load_peaks()
+    achieved = alg_bytes / (ms_dec * 1e-3) / 1e9
+    traffic = cached_traffic(w.name, S)
+    clocks = clk.summary(wall0, wall0 + wall)
+
+    if rank != 0:
+        return 0
+    cpu = None
+    if not args.no_cpu_baseline:
+        res = oracle_sample(w, args.cpu_seconds)
+        cpu = {"value": round(res["gbs"], 4), "unit": "GB/s", "cores": res["cores"],
+               "kind": "oracle",
+               "sample": f"fp64 oracle append+decode, rows 0..{res['rows'] - 1} of {w.name} "
+                         f"x{res['reps']} ({res['seconds']:.1f} s)"}
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": K, "warmup": max(3, args.warmup), "ms_per_step": round(ms_step_max, 5),
+        "us_per_call": round(1e3 * ms_step_max, 2),
+        "pct_hbm_peak": round(100.0 * value / world / peak, 1),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D,
+                   "page_size": w.page_size, "num_pages": P, "tokens": w.total_tokens,
+                   "kv_bytes": kv_bytes, "num_splits": S, "chunk": pkv.split_chunk(d, S),
+                   "l2": "flushed between steps" if not args.no_flush else "warm",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "kernel": "split_decode_kernel",
+                     "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "peak_source": f"{peak_kind} (copy bandwidth)",
+                     "us_per_launch": round(1e3 * ms_dec, 2),
+                     "alg_bytes_per_launch": alg_bytes},
+        "gpu_launches": K * launches_per_step,
+        "clocks": clocks,
+        "wall_s_timed": round(wall, 3),
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_pkv(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

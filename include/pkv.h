@@ -1,0 +1,188 @@
+/*
+ * pkv.h -- C ABI of libpkv: paged GQA decode attention for one NVIDIA GB300
+ * (sm_103a).
+ *
+ * The operation (AstrAI commit log, page "compare v1.3.12..6f09b1d",
+ * astrai/extension/attention_ops.py, docstring of attn_paged_decode, and
+ * astrai/extension/attention_backend.py, CudaBackend.fwd_decode): each of B
+ * query rows holds one new token.  The token's K/V are written into its slot
+ * of a paged pool; then each of its Hq query heads attends, with
+ * softmax(q K^T * scale) V, over all seq_lens[b] tokens of its row, reading
+ * kv head h / (Hq/Hkv) (grouped-query attention, repeat_kv on the same page).
+ * The attention is computed split-KV: each split of a row writes a partial
+ * (normalised output, max, sum) and a combine pass merges them (commits by
+ * author: "single combine kernel", "split partials", "compute_num_splits").
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Every tensor pointer is a DEVICE pointer owned by the caller; the library
+ *    allocates nothing, holds no per-call state, never synchronises and never
+ *    prints.  Kernels are launched asynchronously on `stream` (NULL = the
+ *    legacy default stream), so every call can be captured in a CUDA graph.
+ *  - bf16 means IEEE bfloat16; every bf16 array must be 16-byte aligned and
+ *    densely packed in the layout given.  Tables are int32.
+ *  - Layouts:
+ *      q, out          [B, Hq, D]                  bf16
+ *      k_new, v_new    [B, Hkv, D]                 bf16
+ *      k_pool, v_pool  [num_pages, page_size, Hkv, D] bf16
+ *      seq_lens        [B]    tokens of row b INCLUDING this step's new token
+ *      kv_indptr       [B+1]  row b's pages are kv_indices[kv_indptr[b] ..
+ *                             kv_indptr[b+1]), in logical order; it needs at
+ *                             least ceil(seq_lens[b] / page_size) of them
+ *      kv_indices      [num_indices] physical page ids in [0, num_pages)
+ *    Logical token t of row b lives in page kv_indices[kv_indptr[b] +
+ *    t / page_size], slot t % page_size (compare v1.3.12..6f09b1d,
+ *    astrai/inference/core/cache.py, PagePool._extend_slot).
+ *  - Host-side checks return a pkv_status before anything is launched.
+ *    Device-side checks never trap: a bad table entry or length is skipped
+ *    (reading page 0 instead, so nothing outside the pool is touched) and
+ *    recorded by OR-ing a PKV_FLAG_* bit into the 32-bit status word at
+ *    offset 0 of the workspace.  The word is sticky: clear it with
+ *    pkv_workspace_init and read it back with a device-to-host copy.
+ *  - Launch failures come back as PKV_ERR_LAUNCH (cudaGetLastError).
+ *  - Supported shapes: D in {64, 128}; Hq % Hkv == 0; 1 <= Hq/Hkv <= 16;
+ *    page_size >= 1 (powers of two take a shift, others a division);
+ *    1 <= B <= 65535; Hkv <= 65535.
+ */
+#ifndef PKV_H
+#define PKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st *pkv_stream_t;
+
+typedef enum {
+    PKV_OK = 0,
+    PKV_ERR_INVALID_ARG = -1,        /* null/misaligned pointer, bad shape  */
+    PKV_ERR_UNSUPPORTED = -2,        /* valid but not built (e.g. D = 96)   */
+    PKV_ERR_WORKSPACE_TOO_SMALL = -3,
+    PKV_ERR_LAUNCH = -4              /* a CUDA launch reported an error     */
+} pkv_status;
+
+/* Device status word bits (workspace offset 0). */
+#define PKV_FLAG_BAD_PAGE 0x1u  /* page id outside [0,num_pages), kv_indptr
+                                   outside [0,num_indices], or a row whose
+                                   table is shorter than its length         */
+#define PKV_FLAG_BAD_LEN  0x2u  /* seq_lens[b] < 0 or > max_seq_len         */
+#define PKV_FLAG_BAD_POS  0x4u  /* new-token position >= RoPE table rows    */
+#define PKV_FLAG_TIMEOUT  0x8u  /* an internal copy wait gave up (~2 s)     */
+
+typedef struct {
+    int B;            /* query rows in the batch                           */
+    int Hq;           /* query heads                                        */
+    int Hkv;          /* kv heads; query head h reads kv head h/(Hq/Hkv)    */
+    int D;            /* head dim, 64 or 128                                */
+    int page_size;    /* tokens per page                                    */
+    int num_pages;    /* pages in each pool (>= 1)                          */
+    int num_indices;  /* length of kv_indices                               */
+    int max_seq_len;  /* upper bound on every seq_lens[b]; with num_splits
+                         it fixes the split grid, so a captured graph stays
+                         valid while lengths change below it                */
+    float scale;      /* softmax scale; normally 1/sqrt(D)                  */
+} pkv_dims;
+
+/* ---- planning (host only, no CUDA calls) -------------------------------- */
+
+/* Tokens per split: ceil(ceil(max_seq_len / num_splits) / 16) * 16.  Split s
+ * of row b covers logical tokens [s*chunk, min((s+1)*chunk, seq_lens[b])).
+ * Returns 0 for invalid arguments. */
+int pkv_split_chunk(const pkv_dims *dims, int num_splits);
+
+/* Workspace bytes for num_splits: a 256-byte header (status word first),
+ * ml_part [B, Hq, S, 2] fp32 (max, sum) and o_part [B, Hq, S, D] fp32, each
+ * 256-byte aligned.  Returns 0 for invalid arguments. */
+size_t pkv_workspace_bytes(const pkv_dims *dims, int num_splits);
+
+/* Byte offsets of ml_part and o_part inside the workspace. */
+pkv_status pkv_workspace_layout(const pkv_dims *dims, int num_splits,
+                                size_t *ml_offset, size_t *o_offset);
+
+/* Split count for this shape on a GPU with num_sms SMs: enough (b, kv head,
+ * split) blocks to fill every SM, without splitting below 256 tokens
+ * (commits by author, "compute_num_splits ... undersplitting at large
+ * batch"; "bandwidth saturates near 256-512 total blocks").  Writes the
+ * count and the workspace size it needs. */
+pkv_status pkv_plan(const pkv_dims *dims, int num_sms, int *num_splits,
+                    size_t *ws_bytes);
+
+/* ---- set-up -------------------------------------------------------------- */
+
+/* Zero the workspace status word (stream-ordered memset; no allocation). */
+pkv_status pkv_workspace_init(void *workspace, size_t ws_bytes, pkv_stream_t stream);
+
+/* Fill the RoPE table cos_sin [max_pos, D/2, 2] fp32 with (cos, sin) of
+ * pos * base^(-2i/D), computed in double and rounded once to fp32 (commits
+ * by author: "cos/sin freqs_cis table"). */
+pkv_status pkv_rope_table(float *cos_sin, int max_pos, int D, double base,
+                          pkv_stream_t stream);
+
+/* ---- the hot path --------------------------------------------------------- */
+
+/* (1) Fused RoPE + K/V append.  For each row with L = seq_lens[b] > 0, the
+ * new token's position is p = L-1 (compare v1.3.12..6f09b1d,
+ * astrai/inference/core/task.py next_pos, and cache.py bind_tasks writing at
+ * seq_len - 1).  Each K head vector of k_new[b] is rotated by p on
+ * interleaved pairs (x[2i], x[2i+1]) -> (x[2i] c - x[2i+1] s,
+ * x[2i] s + x[2i+1] c), (c, s) = rope_cos_sin[p][i], in fp32, rounded to
+ * bf16 and stored at the token's slot; V is stored unchanged.  With rope_q,
+ * every query head of row b is rotated the same way, in place.
+ * rope_cos_sin == NULL skips rotation.  Rows with L = 0 are skipped.
+ * status (nullable) receives PKV_FLAG_* bits; an offending row writes
+ * nothing. */
+pkv_status paged_kv_append(const pkv_dims *dims, void *q, const void *k_new,
+                           const void *v_new, void *k_pool, void *v_pool,
+                           const int32_t *kv_indices, const int32_t *kv_indptr,
+                           const int32_t *seq_lens, const float *rope_cos_sin,
+                           int rope_max_pos, int rope_q, uint32_t *status,
+                           pkv_stream_t stream);
+
+/* (2)+(3) Split-KV decode attention.  out[b, h] = softmax(q[b,h] K^T * scale)
+ * V over the row's seq_lens[b] tokens (all of them: decode is causal and the
+ * query is the last token).  Rows with seq_lens[b] = 0 give zeros.  With
+ * num_splits == 1 one kernel writes out directly; otherwise the split
+ * kernel writes partials into the workspace and decode_combine merges
+ * them.  workspace must be 256-byte aligned and hold
+ * pkv_workspace_bytes(dims, num_splits) bytes. */
+pkv_status paged_decode_attn(const pkv_dims *dims, const void *q,
+                             const void *k_pool, const void *v_pool,
+                             const int32_t *kv_indices, const int32_t *kv_indptr,
+                             const int32_t *seq_lens, int num_splits,
+                             void *workspace, size_t ws_bytes, void *out,
+                             pkv_stream_t stream);
+
+/* The split kernel alone: always writes the partials (never out), for any
+ * num_splits >= 1.  Partial (b, h, s): o_part = the split's softmax-weighted
+ * V average (normalised), ml_part = (m, l) with m = max of scale * q.k over
+ * the split (natural-log units) and l = sum exp(scale * q.k - m); an empty
+ * split writes (m, l) = (-inf, 0) and leaves o_part unwritten. */
+pkv_status paged_decode_partials(const pkv_dims *dims, const void *q,
+                                 const void *k_pool, const void *v_pool,
+                                 const int32_t *kv_indices,
+                                 const int32_t *kv_indptr,
+                                 const int32_t *seq_lens, int num_splits,
+                                 void *workspace, size_t ws_bytes,
+                                 pkv_stream_t stream);
+
+/* (3) Combine: for each (b, h), M = max m_s over splits with l_s > 0,
+ * w_s = l_s exp(m_s - M), out = sum w_s o_s / sum w_s, rounded to bf16;
+ * all-empty -> 0.  o_part [B, Hq, S, D], ml_part [B, Hq, S, 2] fp32, as
+ * written by the split kernel (or by any producer of the same layout). */
+pkv_status decode_combine(const pkv_dims *dims, const float *o_part,
+                          const float *ml_part, int num_splits, void *out,
+                          pkv_stream_t stream);
+
+const char *pkv_status_str(pkv_status s);
+
+/* ABI version: (major << 16) | minor. */
+int pkv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PKV_H */

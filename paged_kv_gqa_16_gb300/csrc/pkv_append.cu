@@ -1,0 +1,137 @@
+// pkv_append.cu -- kernel (1): fused RoPE + K/V append into a paged pool,
+// and the set-up kernel that fills the RoPE cos/sin table.
+//
+// What it computes (AstrAI commit log): the decode step writes the new
+// token's K/V at its slot before attending (compare v1.3.12..6f09b1d,
+// astrai/extension/attention_backend.py, CudaBackend.fwd_decode writing
+// k_buffer[layer, out_cache_loc]); the slot of position pos is
+// page_table[pos / page_size] * page_size + pos % page_size (cache.py,
+// PagePool._extend_slot) and the position is seq_len - 1 (cache.py,
+// bind_tasks).  K is rotated first (commits by author: "extend CUDA rotary
+// embedding to packed 3d inputs", "cos/sin freqs_cis table"): each
+// interleaved pair is multiplied by the unit complex number (cos, sin) of
+// pos * theta_i.
+//
+// Layout of the work: one block per row; each thread moves 16-byte vectors
+// (8 bf16 = 4 rotation pairs) of the row's Hkv K/V head vectors and, when
+// asked, its Hq query heads.  The row's page lookup happens once per block.
+#include "pkv_device.cuh"
+#include "pkv_internal.h"
+
+namespace pkv {
+
+namespace {
+
+// Rotate the four interleaved pairs held in one 16-byte vector.  cs holds
+// (cos, sin) for those pairs: c0 s0 c1 s1 c2 s2 c3 s3.
+__device__ __forceinline__ uint4 rotate_vec8(uint4 x, float4 cs01, float4 cs23)
+{
+    auto rot = [](uint32_t w, float c, float s) -> uint32_t {
+        const float a = bf16_lo(w), b = bf16_hi(w);
+        return pack_bf16x2(fmaf(a, c, -b * s), fmaf(a, s, b * c));
+    };
+    uint4 y;
+    y.x = rot(x.x, cs01.x, cs01.y);
+    y.y = rot(x.y, cs01.z, cs01.w);
+    y.z = rot(x.z, cs23.x, cs23.y);
+    y.w = rot(x.w, cs23.z, cs23.w);
+    return y;
+}
+
+__global__ void __launch_bounds__(128) append_kernel(const AppendParams p)
+{
+    const int b = blockIdx.x;
+    const int L = p.seq_lens[b];
+    if (L <= 0) {
+        if (L < 0 && p.status != nullptr && threadIdx.x == 0)
+            atomicOr(p.status, kFlagBadLen);
+        return;
+    }
+    const int pos = L - 1;
+    const int pg0 = p.kv_indptr[b], pg1 = p.kv_indptr[b + 1];
+    unsigned bad = 0;
+    int page = 0;
+    const int pi = pos / p.page_size;
+    if (pg0 < 0 || pg1 < pg0 || pg1 > p.num_indices || pi >= pg1 - pg0) {
+        bad |= kFlagBadPage;
+    } else {
+        page = p.kv_indices[pg0 + pi];
+        if (page < 0 || page >= p.num_pages)
+            bad |= kFlagBadPage;
+    }
+    if (p.rope != nullptr && pos >= p.rope_max_pos)
+        bad |= kFlagBadPos;
+    if (bad) {
+        if (p.status != nullptr && threadIdx.x == 0)
+            atomicOr(p.status, bad);
+        return;
+    }
+    const int slot = pos - pi * p.page_size;
+    const int D = p.D;
+    const int vpr = D >> 3;  // 16-byte vectors per head vector
+    const size_t row_off = ((size_t)page * p.page_size + slot) * (size_t)p.Hkv * D;
+    const float *cs = p.rope != nullptr ? p.rope + (size_t)pos * D : nullptr;
+
+    const uint4 *kin = reinterpret_cast<const uint4 *>(p.k_new + (size_t)b * p.Hkv * D);
+    const uint4 *vin = reinterpret_cast<const uint4 *>(p.v_new + (size_t)b * p.Hkv * D);
+    uint4 *kout = reinterpret_cast<uint4 *>(p.k_pool + row_off);
+    uint4 *vout = reinterpret_cast<uint4 *>(p.v_pool + row_off);
+    for (int it = threadIdx.x; it < p.Hkv * vpr; it += blockDim.x) {
+        const int c = it % vpr;
+        uint4 k = kin[it];
+        if (cs != nullptr) {
+            const float4 *c4 = reinterpret_cast<const float4 *>(cs + 8 * c);
+            k = rotate_vec8(k, c4[0], c4[1]);
+        }
+        kout[it] = k;
+        vout[it] = vin[it];
+    }
+    if (cs != nullptr && p.rope_q) {
+        uint4 *qrow = reinterpret_cast<uint4 *>(p.q + (size_t)b * p.Hq * D);
+        for (int it = threadIdx.x; it < p.Hq * vpr; it += blockDim.x) {
+            const int c = it % vpr;
+            const float4 *c4 = reinterpret_cast<const float4 *>(cs + 8 * c);
+            qrow[it] = rotate_vec8(qrow[it], c4[0], c4[1]);
+        }
+    }
+}
+
+// (cos, sin) of pos * base^(-2i/D), in double, rounded once to fp32.
+__global__ void rope_table_kernel(float *cos_sin, int max_pos, int half, double base, int D)
+{
+    const long long n = (long long)max_pos * half;
+    for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < n;
+         idx += (long long)gridDim.x * blockDim.x) {
+        const int i = (int)(idx % half);
+        const long long pos = idx / half;
+        const double theta = pow(base, -2.0 * (double)i / (double)D);
+        double s, c;
+        sincos((double)pos * theta, &s, &c);
+        cos_sin[2 * idx] = (float)c;
+        cos_sin[2 * idx + 1] = (float)s;
+    }
+}
+
+} // namespace
+
+cudaError_t launch_append(const AppendParams &p, cudaStream_t stream)
+{
+    append_kernel<<<p.B, 128, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_rope_table(float *cos_sin, int max_pos, int D, double base,
+                              cudaStream_t stream)
+{
+    const long long n = (long long)max_pos * (D / 2);
+    const int threads = 256;
+    long long blocks = (n + threads - 1) / threads;
+    if (blocks > 4096)
+        blocks = 4096;
+    if (blocks < 1)
+        blocks = 1;
+    rope_table_kernel<<<(int)blocks, threads, 0, stream>>>(cos_sin, max_pos, D / 2, base, D);
+    return cudaGetLastError();
+}
+
+} // namespace pkv

@@ -1,0 +1,59 @@
+// pkv_internal.h -- parameter blocks and launchers shared by the .cu files of
+// libpkv (not part of the public ABI; see include/pkv.h for that).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+namespace pkv {
+
+struct AppendParams {
+    __nv_bfloat16 *q;
+    const __nv_bfloat16 *k_new;
+    const __nv_bfloat16 *v_new;
+    __nv_bfloat16 *k_pool;
+    __nv_bfloat16 *v_pool;
+    const int32_t *kv_indices;
+    const int32_t *kv_indptr;
+    const int32_t *seq_lens;
+    const float *rope;     // [rope_max_pos, D/2, 2] or nullptr
+    uint32_t *status;      // nullable
+    int B, Hq, Hkv, D, page_size, num_pages, num_indices, max_seq_len;
+    int rope_max_pos, rope_q;
+};
+
+struct DecodeParams {
+    const __nv_bfloat16 *q;
+    const __nv_bfloat16 *k_pool;
+    const __nv_bfloat16 *v_pool;
+    const int32_t *kv_indices;
+    const int32_t *kv_indptr;
+    const int32_t *seq_lens;
+    float *o_part;         // [B, Hq, S, D]
+    float *ml_part;        // [B, Hq, S, 2]
+    __nv_bfloat16 *out;    // [B, Hq, D], used when direct != 0
+    uint32_t *status;
+    int B, Hq, Hkv, n_rep, page_size, ps_shift, num_pages, num_indices;
+    int max_seq_len, num_splits, chunk, direct;
+    float scale_log2;      // scale * log2(e)
+};
+
+struct CombineParams {
+    const float *o_part;
+    const float *ml_part;
+    __nv_bfloat16 *out;
+    int B, Hq, D, num_splits;
+};
+
+cudaError_t launch_append(const AppendParams &p, cudaStream_t stream);
+cudaError_t launch_rope_table(float *cos_sin, int max_pos, int D, double base,
+                              cudaStream_t stream);
+cudaError_t launch_split_decode(const DecodeParams &p, int D, cudaStream_t stream);
+cudaError_t launch_combine(const CombineParams &p, cudaStream_t stream);
+
+// Resident split-decode blocks per SM for head dim D (shared-memory bound).
+int split_decode_blocks_per_sm(int D);
+
+} // namespace pkv

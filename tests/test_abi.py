@@ -1,0 +1,151 @@
+"""C-ABI tests that need no GPU: the library loads, exports every symbol the
+header declares, links no allocator, and its host-side planning and argument
+checks behave as documented.  No case here reaches a kernel launch: every
+negative case fails a host check first."""
+
+import os
+import re
+import subprocess
+
+import pytest
+
+from paged_kv_gqa_16_gb300 import build as pkv_build
+from paged_kv_gqa_16_gb300 import pkv
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pkv.h")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    pkv_build.build()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b((?:pkv|paged|decode)_\w+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol():
+    declared = _declared_functions()
+    assert set(declared) == set(pkv.EXPORTS)
+    L = pkv.lib()
+    for name in declared:
+        assert hasattr(L, name), name
+    out = subprocess.run(["nm", "-D", "--defined-only", pkv.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    for name in declared:
+        assert re.search(rf"\bT {name}$", out, re.M), f"{name} not exported"
+
+
+def test_links_no_device_allocator():
+    out = subprocess.run(["nm", "-D", "--undefined-only", pkv.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    bad = [l for l in out.splitlines() if re.search(r"cu(da)?Mem(Alloc|Free)|cudaMalloc|cudaFree", l)]
+    assert not bad, bad
+
+
+def test_version_and_strings():
+    assert pkv.version() >> 16 == 1
+    assert pkv.status_str(0) == "ok"
+    assert "workspace" in pkv.status_str(pkv.PKV_ERR_WORKSPACE_TOO_SMALL)
+
+
+def _d(**kw):
+    base = dict(B=32, Hq=32, Hkv=8, D=128, page_size=16, num_pages=65536, num_indices=5000,
+                max_seq_len=4096)
+    base.update(kw)
+    return pkv.dims(**base)
+
+
+@pytest.mark.parametrize("max_len,S", [(4096, 1), (4096, 3), (4096, 7), (100, 8), (1, 1),
+                                       (32768, 256), (0, 4)])
+def test_split_chunk(max_len, S):
+    d = _d(max_seq_len=max_len)
+    c = pkv.split_chunk(d, S)
+    assert c % 16 == 0 and c >= 16
+    assert c * S >= max_len                      # the splits cover every token
+    assert c - 16 < -(-max_len // S) or max_len == 0   # and are no coarser than needed
+
+
+def test_workspace_layout_and_bytes():
+    d = _d()
+    for S in (1, 5, 64):
+        ml, o = pkv.workspace_layout(d, S)
+        n = d.B * d.Hq * S
+        assert ml == 256 and ml % 256 == 0 and o % 256 == 0
+        assert o >= ml + n * 8
+        assert pkv.workspace_bytes(d, S) >= o + n * d.D * 4
+        assert pkv.workspace_bytes(d, S) % 256 == 0
+
+
+@pytest.mark.parametrize("B,Hkv,max_len", [(1, 8, 32768), (32, 8, 4096), (8, 8, 1025),
+                                            (128, 8, 8192), (1, 8, 16), (2, 2, 100)])
+def test_plan_invariants(B, Hkv, max_len):
+    d = _d(B=B, Hkv=Hkv, Hq=Hkv * 4, max_seq_len=max_len)
+    S, ws = pkv.plan(d, num_sms=152)
+    assert 1 <= S <= max(1, -(-max_len // 256))       # never below 256 tokens a split
+    assert ws == pkv.workspace_bytes(d, S)
+    # a long single row is split across the machine
+    if B == 1 and max_len >= 32768:
+        assert S >= 64
+
+
+def test_invalid_shapes_rejected():
+    ws = 1 << 20
+    fake = 1 << 32      # aligned, never dereferenced: every case fails a host check
+    cases = [
+        (_d(D=96), pkv.PKV_ERR_UNSUPPORTED),
+        (_d(Hq=30), pkv.PKV_ERR_INVALID_ARG),
+        (_d(Hq=8 * 17), pkv.PKV_ERR_UNSUPPORTED),
+        (_d(page_size=0), pkv.PKV_ERR_INVALID_ARG),
+        (_d(num_pages=0), pkv.PKV_ERR_INVALID_ARG),
+        (_d(B=70000), pkv.PKV_ERR_INVALID_ARG),
+        (_d(max_seq_len=-1), pkv.PKV_ERR_INVALID_ARG),
+    ]
+    for d, want in cases:
+        with pytest.raises(pkv.PkvError) as e:
+            pkv.lib()  # loaded
+            code = pkv.lib().paged_decode_attn(pkv.ctypes.byref(d), fake, fake, fake, fake,
+                                               fake, fake, 4, fake, ws, fake, None)
+            pkv._check("paged_decode_attn", code)
+        assert e.value.code == want, d
+
+
+def test_argument_checks_before_launch():
+    L = pkv.lib()
+    d = _d()
+    byref = pkv.ctypes.byref
+    fake = 1 << 32
+    # workspace too small
+    need = pkv.workspace_bytes(d, 4)
+    assert L.paged_decode_attn(byref(d), fake, fake, fake, fake, fake, fake, 4, fake, need - 1,
+                               fake, None) == pkv.PKV_ERR_WORKSPACE_TOO_SMALL
+    # misaligned pool / workspace / null out
+    assert L.paged_decode_attn(byref(d), fake, fake + 2, fake, fake, fake, fake, 4, fake, need,
+                               fake, None) == pkv.PKV_ERR_INVALID_ARG
+    assert L.paged_decode_attn(byref(d), fake, fake, fake, fake, fake, fake, 4, fake + 16, need,
+                               fake, None) == pkv.PKV_ERR_INVALID_ARG
+    assert L.paged_decode_attn(byref(d), fake, fake, fake, fake, fake, fake, 4, fake, need,
+                               None, None) == pkv.PKV_ERR_INVALID_ARG
+    # split count out of range
+    assert L.paged_decode_partials(byref(d), fake, fake, fake, fake, fake, fake, 0, fake, need,
+                                   None) == pkv.PKV_ERR_INVALID_ARG
+    # combine: null partials
+    assert L.decode_combine(byref(d), None, fake, 4, fake, None) == pkv.PKV_ERR_INVALID_ARG
+    # append: rope table given with no rows, misaligned k_new, rope_q without q
+    assert L.paged_kv_append(byref(d), fake, fake, fake, fake, fake, fake, fake, fake, fake, 0,
+                             0, None, None) == pkv.PKV_ERR_INVALID_ARG
+    assert L.paged_kv_append(byref(d), fake, fake + 8, fake, fake, fake, fake, fake, fake, None,
+                             0, 0, None, None) == pkv.PKV_ERR_INVALID_ARG
+    assert L.paged_kv_append(byref(d), None, fake, fake, fake, fake, fake, fake, fake, fake,
+                             16, 1, None, None) == pkv.PKV_ERR_INVALID_ARG
+    # rope table: odd D
+    assert L.pkv_rope_table(fake, 16, 63, 10000.0, None) == pkv.PKV_ERR_INVALID_ARG
+    # workspace init: misaligned
+    assert L.pkv_workspace_init(fake + 4, 4096, None) == pkv.PKV_ERR_INVALID_ARG
+    # B = 0 is a valid no-op that launches nothing
+    d0 = _d(B=0)
+    assert L.paged_decode_attn(byref(d0), None, None, None, None, None, None, 4, None, 0, None,
+                               None) == pkv.PKV_OK
