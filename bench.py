@@ -52,7 +52,7 @@ def parse_args(argv=None):
     ap.add_argument("--workload", default="ragged_b32")
     ap.add_argument("--splits", type=int, default=0, help="override the planner's split count")
     ap.add_argument("--pool-pages", type=int, default=0,
-                    help="pool size override (smaller pools for profiling captures)")
+                    help="pool size of the ragged workload (smaller pools for profiling)")
     ap.add_argument("--impl", choices=["pkv", "reference"], default="pkv")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -200,7 +200,7 @@ def cpu_cores():
         return os.cpu_count() or 1
 
 
-def oracle_sample(w, target_s: float, max_reps: int = 50):
+def oracle_sample(w, target_s: float, max_reps: int = 1000):
     """Time the fp64 oracle's step (append + decode) on the host cores over a
     bounded sample of the workload: whole rows, taken in order until their
     estimated cost reaches the target, repeated while time remains."""
@@ -242,7 +242,7 @@ def oracle_sample(w, target_s: float, max_reps: int = 50):
         tokens += run((0, b1))
         reps += 1
         el = time.perf_counter() - t0
-        if el >= target_s * 0.5 or reps >= max_reps:
+        if el >= target_s or reps >= max_reps:
             break
     el = time.perf_counter() - t0
     bytes_kv = tokens * w.Hkv * w.D * 2 * 2
@@ -309,44 +309,41 @@ def run_pkv(args):
     pkv.lib()
 
     # each rank: an independent replica of the workload (own seed)
-    w = wl.make(args.workload, seed=rank)
-    t = w.to_device(dev, pool_pages=args.pool_pages or None)
+    kw = {"num_pages": args.pool_pages} if args.pool_pages else {}
+    w = wl.make(args.workload, seed=rank, **kw)
+    t = w.to_device(dev)
     P = t["k_pool"].shape[0]
     d = pkv.dims(w.B, w.Hq, w.Hkv, w.D, w.page_size, P, int(w.kv_indices.numel()),
                  w.max_seq_len, w.scale)
     S = args.splits or pkv.plan(d)[0]
     ws = pkv.alloc_workspace(d, S, dev)
-    o_part, ml_part = pkv.partial_views(d, S, ws)
     rope_rows = max(w.max_seq_len, 1)
     rope = torch.empty(rope_rows, w.D // 2, 2, dtype=torch.float32, device=dev)
     pkv.rope_table(rope, rope_rows, w.D, w.rope_base or 10000.0)
     out = torch.empty(w.B, w.Hq, w.D, dtype=torch.bfloat16, device=dev)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
-    stream = torch.cuda.current_stream(dev)
+    flush_w = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+    flush_r = torch.zeros(max(2 * l2, 256 << 20) // 4, dtype=torch.int32, device=dev)
+    flush_sink = torch.empty((), dtype=torch.int64, device=dev)
 
-    def step(q, k_new, v_new, kv_indices, kv_indptr, seq_lens, ev=None):
-        pkv.paged_kv_append(d, q, k_new, v_new, t["k_pool"], t["v_pool"], kv_indices,
-                            kv_indptr, seq_lens, rope_cos_sin=rope, rope_max_pos=rope_rows,
-                            rope_q=True, status=ws, stream=stream)
-        if S == 1:
-            if ev is not None:
-                ev[1].record(stream)
-            pkv.paged_decode_attn(d, q, t["k_pool"], t["v_pool"], kv_indices, kv_indptr,
-                                  seq_lens, 1, ws, out, stream=stream)
-            if ev is not None:
-                ev[2].record(stream)
-        else:
-            # the same two launches paged_decode_attn makes, bracketed apart
-            if ev is not None:
-                ev[1].record(stream)
-            pkv.paged_decode_partials(d, q, t["k_pool"], t["v_pool"], kv_indices, kv_indptr,
-                                      seq_lens, S, ws, stream=stream)
-            if ev is not None:
-                ev[2].record(stream)
-            pkv.decode_combine(d, o_part, ml_part, S, out, stream=stream)
+    def flush_l2():
+        """Evict the L2: write a buffer of twice its size, then read another
+        of the same size so the lines left behind are clean (a dirty L2 would
+        charge its write-back to the next timed kernel)."""
+        flush_w.zero_()
+        torch.sum(flush_r, dim=0, out=flush_sink)
 
-    launches_per_step = 2 if S == 1 else 3
+    def step(q, k_new, v_new, kv_indices, kv_indptr, seq_lens):
+        """One pass of the hot path on the current stream: the new token's
+        RoPE + append, the split decode and the combine (paged_decode_step)."""
+        pkv.paged_decode_step(d, q, k_new, v_new, t["k_pool"], t["v_pool"], kv_indices,
+                              kv_indptr, seq_lens, rope, rope_rows, S, ws, out)
+
+    def decode(q, kv_indices, kv_indptr, seq_lens):
+        pkv.paged_decode_attn(d, q, t["k_pool"], t["v_pool"], kv_indices, kv_indptr,
+                              seq_lens, S, ws, out)
+
+    launches_per_step = 1 if S == 1 else 2
     dev_args = (t["q"], t["k_new"], t["v_new"], t["kv_indices"], t["kv_indptr"], t["seq_lens"])
 
     for _ in range(max(3, args.warmup)):
@@ -355,25 +352,40 @@ def run_pkv(args):
     if pkv.status_word(ws) != 0:
         raise SystemExit(f"device status {pkv.status_word(ws):#x} after warm-up")
 
+    # the step and the decode call alone, each captured once in a CUDA graph
+    # (the calls allocate nothing and take fixed addresses), then replayed
+    g_step, g_dec = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_step):
+        step(*dev_args)
+    with torch.cuda.graph(g_dec):
+        decode(t["q"], t["kv_indices"], t["kv_indptr"], t["seq_lens"])
+    for _ in range(3):
+        g_step.replay()
+        g_dec.replay()
+    stream = torch.cuda.current_stream(dev)
+
+    def timed(graph, K):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(K)]
+        for k in range(K):
+            if not args.no_flush:
+                flush_l2()
+            evs[k][0].record(stream)
+            graph.replay()
+            evs[k][1].record(stream)
+        torch.cuda.synchronize(dev)
+        return [a.elapsed_time(b) for a, b in evs]
+
     K = args.steps
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
     barrier(world, dev)
     torch.cuda.synchronize(dev)
     with ClockSampler(dev.index) as clk:
         time.sleep(0.4)              # let the sampler start before the timed region
         wall0 = time.perf_counter()
-        for k in range(K):
-            if not args.no_flush:
-                flush.zero_()
-            ev = evs[k]
-            ev[0].record(stream)
-            step(*dev_args, ev=ev)
-            ev[3].record(stream)
-        torch.cuda.synchronize(dev)
+        step_ms = timed(g_step, K)
         wall = time.perf_counter() - wall0
     barrier(world, dev)
-    step_ms = [e[0].elapsed_time(e[3]) for e in evs]
-    dec_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    dec_ms = timed(g_dec, max(50, min(K, 2000)))
     ms_step = statistics.mean(step_ms)
     ms_dec = statistics.mean(dec_ms)
     ms_step_max = reduce_max(ms_step, world, dev)
@@ -386,10 +398,8 @@ def run_pkv(args):
     # e2e: host (pinned) inputs copied in, the step, the output copied back
     e2e = None
     if not args.no_e2e:
-        host = {k: v.cpu().pin_memory() for k, v in
-                zip(("q", "k_new", "v_new", "kv_indices", "kv_indptr", "seq_lens"),
-                    (w.q, w.k_new, w.v_new, w.kv_indices, w.kv_indptr, w.seq_lens))}
-        dev_in = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
+        names = ("q", "k_new", "v_new", "kv_indices", "kv_indptr", "seq_lens")
+        host = {k: getattr(w, k).contiguous().pin_memory() for k in names}
         out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
         h2d = sum(v.numel() * v.element_size() for v in host.values())
         d2h = out_host.numel() * out_host.element_size()
@@ -399,12 +409,11 @@ def run_pkv(args):
         torch.cuda.synchronize(dev)
         for k in range(Ke):
             if not args.no_flush:
-                flush.zero_()
+                flush_l2()
             e_evs[k][0].record(stream)
-            for name in host:
-                dev_in[name].copy_(host[name], non_blocking=True)
-            step(dev_in["q"], dev_in["k_new"], dev_in["v_new"], dev_in["kv_indices"],
-                 dev_in["kv_indptr"], dev_in["seq_lens"])
+            for name in names:       # host inputs into the graph's fixed buffers
+                t[name].copy_(host[name], non_blocking=True)
+            g_step.replay()
             out_host.copy_(out, non_blocking=True)
             e_evs[k][1].record(stream)
         torch.cuda.synchronize(dev)
@@ -412,17 +421,24 @@ def run_pkv(args):
         e_ms = reduce_max(e_ms, world, dev)
         e2e = {"value": round(total_bytes / (e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                "ms_per_step": round(e_ms, 5), "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h}
+               "d2h_bytes_per_step": d2h, "path": "pinned host inputs -> step graph -> host"}
 
     status = pkv.status_word(ws)
     if status != 0:
         raise SystemExit(f"device status {status:#x} after the timed run")
 
-    # roofline of the dominant kernel (the split decode): algorithmic bytes =
-    # K and V of every token + q + page tables, per launch
-    alg_bytes = kv_bytes + w.B * w.Hq * w.D * 2 + 4 * int(w.kv_indices.numel()) + 8 * w.B
+    # roofline of the dominant kernel, the fused step kernel (its launch is
+    # timed as the step call, so the small piece combine is included).
+    # Algorithmic bytes per call: K and V of every token, q, the new token's
+    # K/V read and written to its slot, the output, and the page tables.
+    n_idx = int(w.kv_indices.numel())
+    io_bytes = (w.B * w.Hq * w.D * 2 * 2            # q in, out
+                + w.B * w.Hkv * w.D * 2 * 2 * 2     # k_new/v_new in, slot writes
+                + 4 * n_idx + 8 * w.B)              # kv_indices, kv_indptr, seq_lens
+    alg_bytes = kv_bytes + io_bytes
+    dec_bytes = kv_bytes + w.B * w.Hq * w.D * 2 * 2 + 4 * n_idx + 8 * w.B
     peak, peak_kind = load_peaks()
-    achieved = alg_bytes / (ms_dec * 1e-3) / 1e9
+    achieved = alg_bytes / (ms_step * 1e-3) / 1e9
     traffic = cached_traffic(w.name, S)
     clocks = clk.summary(wall0, wall0 + wall)
 
@@ -438,6 +454,7 @@ def run_pkv(args):
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": K, "warmup": max(3, args.warmup), "ms_per_step": round(ms_step_max, 5),
+        "timing": "CUDA graph replay of the step; events on the replay stream",
         "us_per_call": round(1e3 * ms_step_max, 2),
         "pct_hbm_peak": round(100.0 * value / world / peak, 1),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
@@ -445,14 +462,20 @@ def run_pkv(args):
         "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D,
                    "page_size": w.page_size, "num_pages": P, "tokens": w.total_tokens,
                    "kv_bytes": kv_bytes, "num_splits": S, "chunk": pkv.split_chunk(d, S),
-                   "l2": "flushed between steps" if not args.no_flush else "warm",
+                   "l2": ("flushed between steps (2x L2 written, then 2x L2 read), outside the "
+                         "timed events") if not args.no_flush else "warm",
                    "parallelism": f"replicas x{world}"},
-        "roofline": {"bound": "hbm", "kernel": "split_decode_kernel",
+        "roofline": {"bound": "hbm",
+                     "kernel": "fused_decode_kernel (paged_decode_step; its piece combine "
+                               "is inside the timed call)",
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
                      "peak_source": f"{peak_kind} (copy bandwidth)",
-                     "us_per_launch": round(1e3 * ms_dec, 2),
+                     "us_per_launch": round(1e3 * ms_step, 2),
                      "alg_bytes_per_launch": alg_bytes},
+        "decode_only": {"call": "paged_decode_attn", "us": round(1e3 * ms_dec_max, 2),
+                        "kv_read_gbs": round(kv_bytes / (ms_dec_max * 1e-3) / 1e9, 1),
+                        "alg_gbs": round(dec_bytes / (ms_dec_max * 1e-3) / 1e9, 1)},
         "gpu_launches": K * launches_per_step,
         "clocks": clocks,
         "wall_s_timed": round(wall, 3),

@@ -89,25 +89,38 @@ typedef struct {
 
 /* ---- planning (host only, no CUDA calls) -------------------------------- */
 
-/* Tokens per split: ceil(ceil(max_seq_len / num_splits) / 16) * 16.  Split s
- * of row b covers logical tokens [s*chunk, min((s+1)*chunk, seq_lens[b])).
- * Returns 0 for invalid arguments. */
+/* num_splits, two readings.  paged_decode_attn / paged_decode_step on the
+ * persistent path (at most 4096 rows x kv-head groups, the usual case): the
+ * number of persistent blocks; all rows' tokens laid end to end are cut into
+ * num_splits equal ranges (never below 64 tokens each), so a row is split
+ * into as many pieces as ranges it touches -- a single row into up to
+ * num_splits.  paged_decode_partials, and paged_decode_attn on other shapes:
+ * the per-row split count, each split covering `chunk` tokens (below). */
+
+/* Tokens per split of the per-row layout:
+ * ceil(ceil(max_seq_len / num_splits) / 16) * 16.  Split s of row b covers
+ * logical tokens [s*chunk, min((s+1)*chunk, seq_lens[b])).  Returns 0 for
+ * invalid arguments. */
 int pkv_split_chunk(const pkv_dims *dims, int num_splits);
 
 /* Workspace bytes for num_splits: a 256-byte header (status word first),
- * ml_part [B, Hq, S, 2] fp32 (max, sum) and o_part [B, Hq, S, D] fp32, each
- * 256-byte aligned.  Returns 0 for invalid arguments. */
+ * per-row bookkeeping, a [B, Hq, D] bf16 scratch, and room for either
+ * partial layout (the per-row one [B, Hq, S, 2] + [B, Hq, S, D] fp32, or the
+ * persistent path's pieces), each region 256-byte aligned.  Returns 0 for
+ * invalid arguments. */
 size_t pkv_workspace_bytes(const pkv_dims *dims, int num_splits);
 
-/* Byte offsets of ml_part and o_part inside the workspace. */
+/* Byte offsets of the per-row layout's ml_part and o_part (as written by
+ * paged_decode_partials) inside the workspace. */
 pkv_status pkv_workspace_layout(const pkv_dims *dims, int num_splits,
                                 size_t *ml_offset, size_t *o_offset);
 
-/* Split count for this shape on a GPU with num_sms SMs: enough (b, kv head,
- * split) blocks to fill every SM, without splitting below 256 tokens
- * (commits by author, "compute_num_splits ... undersplitting at large
- * batch"; "bandwidth saturates near 256-512 total blocks").  Writes the
- * count and the workspace size it needs. */
+/* Split count for this shape on a GPU with num_sms SMs.  Persistent path:
+ * one block per SM, fewer when max_seq_len x rows gives under 64 tokens a
+ * block.  Per-row path: enough (split, kv head, row) blocks for a few waves,
+ * never splitting below 256 tokens (commits by author, "compute_num_splits
+ * ... undersplitting at large batch"; "bandwidth saturates near 256-512
+ * total blocks").  Writes the count and the workspace size it needs. */
 pkv_status pkv_plan(const pkv_dims *dims, int num_sms, int *num_splits,
                     size_t *ws_bytes);
 
@@ -144,17 +157,37 @@ pkv_status paged_kv_append(const pkv_dims *dims, void *q, const void *k_new,
 
 /* (2)+(3) Split-KV decode attention.  out[b, h] = softmax(q[b,h] K^T * scale)
  * V over the row's seq_lens[b] tokens (all of them: decode is causal and the
- * query is the last token).  Rows with seq_lens[b] = 0 give zeros.  With
- * num_splits == 1 one kernel writes out directly; otherwise the split
- * kernel writes partials into the workspace and decode_combine merges
- * them.  workspace must be 256-byte aligned and hold
- * pkv_workspace_bytes(dims, num_splits) bytes. */
+ * query is the last token).  Rows with seq_lens[b] = 0 give zeros.
+ * Persistent path: one token-balanced kernel (a piece that is a whole row
+ * writes out directly) plus, when num_splits > 1, the piece combine.  Other
+ * shapes: the per-(split, kv head, row) kernel, plus decode_combine when
+ * num_splits > 1.  workspace must be 256-byte aligned and hold
+ * pkv_workspace_bytes(dims, num_splits) bytes; its status word must have
+ * been zeroed once (pkv_workspace_init). */
 pkv_status paged_decode_attn(const pkv_dims *dims, const void *q,
                              const void *k_pool, const void *v_pool,
                              const int32_t *kv_indices, const int32_t *kv_indptr,
                              const int32_t *seq_lens, int num_splits,
                              void *workspace, size_t ws_bytes, void *out,
                              pkv_stream_t stream);
+
+/* (1)+(2)+(3) in one pass: the whole decode step.  Appends each row's new
+ * token exactly as paged_kv_append does (K rotated by position seq_len - 1
+ * and rounded to bf16, V copied, both into the token's slot of the pools)
+ * and computes out exactly as paged_decode_attn does, with q rotated by the
+ * same position.  q itself is NOT modified (its rotation stays internal).
+ * For shapes the persistent kernel serves (at most 4096 rows x kv-head
+ * groups) it is one launch plus the combine: the new token is rotated in
+ * the decode kernel and attended from shared memory, and q is rotated in
+ * registers.  Otherwise it runs a rotated copy of q (in the workspace), the
+ * append and the split decode.  rope_cos_sin == NULL: no rotation.
+ * Device-side errors set the PKV_FLAG_* bits of the workspace status word. */
+pkv_status paged_decode_step(const pkv_dims *dims, const void *q, const void *k_new,
+                             const void *v_new, void *k_pool, void *v_pool,
+                             const int32_t *kv_indices, const int32_t *kv_indptr,
+                             const int32_t *seq_lens, const float *rope_cos_sin,
+                             int rope_max_pos, int num_splits, void *workspace,
+                             size_t ws_bytes, void *out, pkv_stream_t stream);
 
 /* The split kernel alone: always writes the partials (never out), for any
  * num_splits >= 1.  Partial (b, h, s): o_part = the split's softmax-weighted

@@ -11,7 +11,7 @@ namespace {
 
 constexpr size_t kHeaderBytes = 256;
 constexpr int kMaxSplits = 65536;
-constexpr int kMinChunkTokens = 256;   // the planner does not split finer than this
+constexpr int kMinChunkTokens = 256;   // per-split path: never split finer than this
 
 size_t round_up(size_t x, size_t a)
 {
@@ -21,6 +21,11 @@ size_t round_up(size_t x, size_t a)
 bool aligned(const void *p, uintptr_t a)
 {
     return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0;
+}
+
+pkv_status launch_status(cudaError_t e)
+{
+    return e == cudaSuccess ? PKV_OK : PKV_ERR_LAUNCH;
 }
 
 // Shape checks common to every entry point.
@@ -63,16 +68,49 @@ int log2_exact(int x)
     return s;
 }
 
-pkv_status launch_status(cudaError_t e)
+// Workspace: [header 256 B | row info, persistent path: Bv x 2 int32 |
+//             rotated-q scratch [B, Hq, D] bf16 | partials].
+// The partial region holds either layout: the per-split one [B,Hq,S,(2|D)]
+// of paged_decode_partials, or the piece one [(S+Bv)*HQV, (2|D)] of the
+// persistent path.  Every region starts on a 256-byte boundary.
+struct Layout {
+    int hpc, Bv, HQV;
+    size_t rowinfo_off, qscratch_off, split_ml_off, split_o_off, piece_ml_off, piece_o_off,
+        total;
+};
+
+Layout layout_for(const pkv_dims *d, int num_splits)
 {
-    return e == cudaSuccess ? PKV_OK : PKV_ERR_LAUNCH;
+    Layout L{};
+    L.hpc = pkv::fused_heads_per_block(d->Hkv);
+    L.Bv = d->B * (d->Hkv / L.hpc);
+    L.HQV = L.hpc * (d->Hq / d->Hkv);
+    L.rowinfo_off = kHeaderBytes;
+    L.qscratch_off = L.rowinfo_off + round_up((size_t)L.Bv * 2 * sizeof(int32_t), 256);
+    const size_t part = L.qscratch_off + round_up((size_t)d->B * d->Hq * d->D * 2, 256);
+    const size_t rows = (size_t)d->B * d->Hq * num_splits;
+    L.split_ml_off = part;
+    L.split_o_off = part + round_up(rows * 2 * sizeof(float), 256);
+    const size_t split_end = L.split_o_off + round_up(rows * d->D * sizeof(float), 256);
+    const size_t pieces = ((size_t)num_splits + L.Bv) * L.HQV;
+    L.piece_ml_off = part;
+    L.piece_o_off = part + round_up(pieces * 2 * sizeof(float), 256);
+    const size_t piece_end = L.piece_o_off + round_up(pieces * d->D * sizeof(float), 256);
+    L.total = split_end > piece_end ? split_end : piece_end;
+    return L;
 }
 
-pkv_status decode_common(const pkv_dims *dims, const void *q, const void *k_pool,
-                         const void *v_pool, const int32_t *kv_indices,
-                         const int32_t *kv_indptr, const int32_t *seq_lens, int num_splits,
-                         void *workspace, size_t ws_bytes, void *out, bool direct,
-                         pkv_stream_t stream)
+// The persistent path keeps every virtual row's prefix sum in shared memory.
+bool fused_path_ok(const pkv_dims *d)
+{
+    const Layout L = layout_for(d, 1);
+    return L.Bv <= pkv::kFusedMaxRows && (long long)L.Bv * d->max_seq_len < (1ll << 31);
+}
+
+pkv_status check_decode_args(const pkv_dims *dims, const void *q, const void *k_pool,
+                             const void *v_pool, const int32_t *kv_indices,
+                             const int32_t *kv_indptr, const int32_t *seq_lens, int num_splits,
+                             void *workspace, size_t ws_bytes, void *out, bool need_out)
 {
     pkv_status st = check_dims(dims);
     if (st != PKV_OK)
@@ -82,12 +120,12 @@ pkv_status decode_common(const pkv_dims *dims, const void *q, const void *k_pool
     if (dims->B == 0)
         return PKV_OK;
     if (q == nullptr || k_pool == nullptr || v_pool == nullptr || kv_indptr == nullptr ||
-        seq_lens == nullptr || workspace == nullptr || (direct && out == nullptr))
+        seq_lens == nullptr || workspace == nullptr || (need_out && out == nullptr))
         return PKV_ERR_INVALID_ARG;
     if (dims->num_indices > 0 && kv_indices == nullptr)
         return PKV_ERR_INVALID_ARG;
     if (!aligned(q, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16) ||
-        !aligned(workspace, 256) || (direct && !aligned(out, 16)) ||
+        !aligned(workspace, 256) || (need_out && !aligned(out, 16)) ||
         !aligned(kv_indptr, 4) || !aligned(seq_lens, 4) ||
         (kv_indices != nullptr && !aligned(kv_indices, 4)))
         return PKV_ERR_INVALID_ARG;
@@ -96,9 +134,18 @@ pkv_status decode_common(const pkv_dims *dims, const void *q, const void *k_pool
         return PKV_ERR_INVALID_ARG;
     if (ws_bytes < need)
         return PKV_ERR_WORKSPACE_TOO_SMALL;
-    size_t ml_off = 0, o_off = 0;
-    pkv_workspace_layout(dims, num_splits, &ml_off, &o_off);
+    return PKV_OK;
+}
 
+// Per-(split, kv head, row) blocks: writes split partials, or the output
+// directly when `direct` (one split).  Arguments already checked.
+pkv_status launch_split(const pkv_dims *dims, const void *q, const void *k_pool,
+                        const void *v_pool, const int32_t *kv_indices, const int32_t *kv_indptr,
+                        const int32_t *seq_lens, int num_splits, void *workspace, void *out,
+                        bool direct, pkv_stream_t stream)
+{
+    const Layout L = layout_for(dims, num_splits);
+    char *ws = static_cast<char *>(workspace);
     pkv::DecodeParams p{};
     p.q = static_cast<const __nv_bfloat16 *>(q);
     p.k_pool = static_cast<const __nv_bfloat16 *>(k_pool);
@@ -106,10 +153,10 @@ pkv_status decode_common(const pkv_dims *dims, const void *q, const void *k_pool
     p.kv_indices = kv_indices;
     p.kv_indptr = kv_indptr;
     p.seq_lens = seq_lens;
-    p.ml_part = reinterpret_cast<float *>(static_cast<char *>(workspace) + ml_off);
-    p.o_part = reinterpret_cast<float *>(static_cast<char *>(workspace) + o_off);
+    p.ml_part = reinterpret_cast<float *>(ws + L.split_ml_off);
+    p.o_part = reinterpret_cast<float *>(ws + L.split_o_off);
     p.out = static_cast<__nv_bfloat16 *>(out);
-    p.status = static_cast<uint32_t *>(workspace);
+    p.status = reinterpret_cast<uint32_t *>(ws);
     p.B = dims->B;
     p.Hq = dims->Hq;
     p.Hkv = dims->Hkv;
@@ -126,13 +173,140 @@ pkv_status decode_common(const pkv_dims *dims, const void *q, const void *k_pool
     return launch_status(pkv::launch_split_decode(p, dims->D, (cudaStream_t)stream));
 }
 
+pkv_status launch_combine_split(const pkv_dims *dims, int num_splits, void *workspace,
+                                void *out, pkv_stream_t stream)
+{
+    const Layout L = layout_for(dims, num_splits);
+    char *ws = static_cast<char *>(workspace);
+    pkv::CombineParams p{};
+    p.o_part = reinterpret_cast<const float *>(ws + L.split_o_off);
+    p.ml_part = reinterpret_cast<const float *>(ws + L.split_ml_off);
+    p.out = static_cast<__nv_bfloat16 *>(out);
+    p.B = dims->B;
+    p.Hq = dims->Hq;
+    p.D = dims->D;
+    p.num_splits = num_splits;
+    return launch_status(pkv::launch_combine(p, (cudaStream_t)stream));
+}
+
+// Persistent path: the token-balanced kernel, then the piece combine.  With
+// k_new != nullptr the kernel also appends the step's new token (fused step).
+pkv_status launch_persistent(const pkv_dims *dims, const void *q, const void *k_pool,
+                             const void *v_pool, const int32_t *kv_indices,
+                             const int32_t *kv_indptr, const int32_t *seq_lens,
+                             int num_splits, void *workspace, void *out, const void *k_new,
+                             const void *v_new, const float *rope, int rope_max_pos,
+                             pkv_stream_t stream)
+{
+    const Layout L = layout_for(dims, num_splits);
+    char *ws = static_cast<char *>(workspace);
+    pkv::FusedParams p{};
+    p.q = static_cast<const __nv_bfloat16 *>(q);
+    p.k_pool = static_cast<const __nv_bfloat16 *>(k_pool);
+    p.v_pool = static_cast<const __nv_bfloat16 *>(v_pool);
+    p.kv_indices = kv_indices;
+    p.kv_indptr = kv_indptr;
+    p.seq_lens = seq_lens;
+    p.out = static_cast<__nv_bfloat16 *>(out);
+    p.o_part = reinterpret_cast<float *>(ws + L.piece_o_off);
+    p.ml_part = reinterpret_cast<float *>(ws + L.piece_ml_off);
+    p.row_info = reinterpret_cast<int32_t *>(ws + L.rowinfo_off);
+    p.status = reinterpret_cast<uint32_t *>(ws);
+    p.B = dims->B;
+    p.Hq = dims->Hq;
+    p.Hkv = dims->Hkv;
+    p.n_rep = dims->Hq / dims->Hkv;
+    p.page_size = dims->page_size;
+    p.ps_shift = log2_exact(dims->page_size);
+    p.num_pages = dims->num_pages;
+    p.num_indices = dims->num_indices;
+    p.max_seq_len = dims->max_seq_len;
+    p.Bv = L.Bv;
+    p.hpc = L.hpc;
+    p.scale_log2 = (float)((double)dims->scale * 1.4426950408889634);
+    p.step = k_new != nullptr ? 1 : 0;
+    p.k_pool_w = const_cast<__nv_bfloat16 *>(p.k_pool);
+    p.v_pool_w = const_cast<__nv_bfloat16 *>(p.v_pool);
+    p.k_new = static_cast<const __nv_bfloat16 *>(k_new);
+    p.v_new = static_cast<const __nv_bfloat16 *>(v_new);
+    p.rope = rope;
+    p.rope_max_pos = rope_max_pos;
+    pkv_status st =
+        launch_status(pkv::launch_fused_decode(p, dims->D, num_splits, (cudaStream_t)stream));
+    if (st != PKV_OK || num_splits == 1)
+        return st;
+    pkv::PieceCombineParams c{};
+    c.o_part = p.o_part;
+    c.ml_part = p.ml_part;
+    c.row_info = p.row_info;
+    c.out = p.out;
+    c.B = dims->B;
+    c.Bv = L.Bv;
+    c.Hq = dims->Hq;
+    c.HQV = L.HQV;
+    return launch_status(
+        pkv::launch_piece_combine(c, dims->D, num_splits, (cudaStream_t)stream));
+}
+
+pkv_status check_append_args(const pkv_dims *dims, const void *q, const void *k_new,
+                             const void *v_new, const void *k_pool, const void *v_pool,
+                             const int32_t *kv_indices, const int32_t *kv_indptr,
+                             const int32_t *seq_lens, const float *rope_cos_sin,
+                             int rope_max_pos, int rope_q, const uint32_t *status)
+{
+    if (k_new == nullptr || v_new == nullptr || k_pool == nullptr || v_pool == nullptr ||
+        kv_indptr == nullptr || seq_lens == nullptr ||
+        (dims->num_indices > 0 && kv_indices == nullptr))
+        return PKV_ERR_INVALID_ARG;
+    if (rope_cos_sin != nullptr && rope_q && q == nullptr)
+        return PKV_ERR_INVALID_ARG;
+    if (rope_cos_sin != nullptr && (rope_max_pos <= 0 || !aligned(rope_cos_sin, 16)))
+        return PKV_ERR_INVALID_ARG;
+    if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(k_pool, 16) ||
+        !aligned(v_pool, 16) || (q != nullptr && !aligned(q, 16)) || !aligned(kv_indptr, 4) ||
+        !aligned(seq_lens, 4) || (kv_indices != nullptr && !aligned(kv_indices, 4)) ||
+        (status != nullptr && !aligned(status, 4)))
+        return PKV_ERR_INVALID_ARG;
+    return PKV_OK;
+}
+
+pkv_status launch_append(const pkv_dims *dims, void *q, const void *k_new, const void *v_new,
+                         void *k_pool, void *v_pool, const int32_t *kv_indices,
+                         const int32_t *kv_indptr, const int32_t *seq_lens,
+                         const float *rope_cos_sin, int rope_max_pos, int rope_q,
+                         uint32_t *status, pkv_stream_t stream)
+{
+    pkv::AppendParams p{};
+    p.q = static_cast<__nv_bfloat16 *>(q);
+    p.k_new = static_cast<const __nv_bfloat16 *>(k_new);
+    p.v_new = static_cast<const __nv_bfloat16 *>(v_new);
+    p.k_pool = static_cast<__nv_bfloat16 *>(k_pool);
+    p.v_pool = static_cast<__nv_bfloat16 *>(v_pool);
+    p.kv_indices = kv_indices;
+    p.kv_indptr = kv_indptr;
+    p.seq_lens = seq_lens;
+    p.rope = rope_cos_sin;
+    p.status = status;
+    p.B = dims->B;
+    p.Hq = dims->Hq;
+    p.Hkv = dims->Hkv;
+    p.D = dims->D;
+    p.page_size = dims->page_size;
+    p.num_pages = dims->num_pages;
+    p.num_indices = dims->num_indices;
+    p.max_seq_len = dims->max_seq_len;
+    p.rope_max_pos = rope_max_pos;
+    p.rope_q = rope_q ? 1 : 0;
+    return launch_status(pkv::launch_append(p, (cudaStream_t)stream));
+}
+
 } // namespace
 
 extern "C" {
 
 int pkv_version(void)
 {
-    return (1 << 16) | 0;
+    return (1 << 16) | 1;
 }
 
 const char *pkv_status_str(pkv_status s)
@@ -168,19 +342,17 @@ pkv_status pkv_workspace_layout(const pkv_dims *dims, int num_splits, size_t *ml
     if (num_splits < 1 || num_splits > kMaxSplits || ml_offset == nullptr ||
         o_offset == nullptr)
         return PKV_ERR_INVALID_ARG;
-    const size_t rows = (size_t)dims->B * dims->Hq * num_splits;
-    *ml_offset = kHeaderBytes;
-    *o_offset = kHeaderBytes + round_up(rows * 2 * sizeof(float), 256);
+    const Layout L = layout_for(dims, num_splits);
+    *ml_offset = L.split_ml_off;
+    *o_offset = L.split_o_off;
     return PKV_OK;
 }
 
 size_t pkv_workspace_bytes(const pkv_dims *dims, int num_splits)
 {
-    size_t ml = 0, o = 0;
-    if (pkv_workspace_layout(dims, num_splits, &ml, &o) != PKV_OK)
+    if (check_dims(dims) != PKV_OK || num_splits < 1 || num_splits > kMaxSplits)
         return 0;
-    const size_t rows = (size_t)dims->B * dims->Hq * num_splits;
-    return o + round_up(rows * dims->D * sizeof(float), 256);
+    return layout_for(dims, num_splits).total;
 }
 
 pkv_status pkv_plan(const pkv_dims *dims, int num_sms, int *num_splits, size_t *ws_bytes)
@@ -190,15 +362,23 @@ pkv_status pkv_plan(const pkv_dims *dims, int num_sms, int *num_splits, size_t *
         return st;
     if (num_sms <= 0 || num_splits == nullptr)
         return PKV_ERR_INVALID_ARG;
-    const long long units = (long long)(dims->B > 0 ? dims->B : 1) * dims->Hkv;
-    const long long slots = (long long)num_sms * pkv::split_decode_blocks_per_sm(dims->D);
-    const long long target = 4 * slots;             // a few waves of blocks
-    long long s = (target + units - 1) / units;
-    long long s_max = ((long long)dims->max_seq_len + kMinChunkTokens - 1) / kMinChunkTokens;
-    if (s_max < 1)
-        s_max = 1;
-    if (s > s_max)
-        s = s_max;
+    long long s;
+    if (fused_path_ok(dims)) {
+        // one persistent block per SM, each with at least kFusedMinTokens
+        const Layout L = layout_for(dims, 1);
+        const long long work = (long long)(L.Bv > 0 ? L.Bv : 1) * dims->max_seq_len;
+        s = (work + pkv::kFusedMinTokens - 1) / pkv::kFusedMinTokens;
+        if (s > num_sms)
+            s = num_sms;
+    } else {
+        const long long units = (long long)(dims->B > 0 ? dims->B : 1) * dims->Hkv;
+        const long long slots = (long long)num_sms * pkv::split_decode_blocks_per_sm(dims->D);
+        const long long target = 4 * slots;             // a few waves of blocks
+        s = (target + units - 1) / units;
+        long long s_max = ((long long)dims->max_seq_len + kMinChunkTokens - 1) / kMinChunkTokens;
+        if (s > s_max)
+            s = s_max;
+    }
     if (s < 1)
         s = 1;
     *num_splits = (int)s;
@@ -234,41 +414,12 @@ pkv_status paged_kv_append(const pkv_dims *dims, void *q, const void *k_new, con
         return st;
     if (dims->B == 0)
         return PKV_OK;
-    if (k_new == nullptr || v_new == nullptr || k_pool == nullptr || v_pool == nullptr ||
-        kv_indptr == nullptr || seq_lens == nullptr ||
-        (dims->num_indices > 0 && kv_indices == nullptr))
-        return PKV_ERR_INVALID_ARG;
-    if (rope_cos_sin != nullptr && rope_q && q == nullptr)
-        return PKV_ERR_INVALID_ARG;
-    if (rope_cos_sin != nullptr && (rope_max_pos <= 0 || !aligned(rope_cos_sin, 16)))
-        return PKV_ERR_INVALID_ARG;
-    if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(k_pool, 16) ||
-        !aligned(v_pool, 16) || (q != nullptr && !aligned(q, 16)) || !aligned(kv_indptr, 4) ||
-        !aligned(seq_lens, 4) || (kv_indices != nullptr && !aligned(kv_indices, 4)) ||
-        (status != nullptr && !aligned(status, 4)))
-        return PKV_ERR_INVALID_ARG;
-    pkv::AppendParams p{};
-    p.q = static_cast<__nv_bfloat16 *>(q);
-    p.k_new = static_cast<const __nv_bfloat16 *>(k_new);
-    p.v_new = static_cast<const __nv_bfloat16 *>(v_new);
-    p.k_pool = static_cast<__nv_bfloat16 *>(k_pool);
-    p.v_pool = static_cast<__nv_bfloat16 *>(v_pool);
-    p.kv_indices = kv_indices;
-    p.kv_indptr = kv_indptr;
-    p.seq_lens = seq_lens;
-    p.rope = rope_cos_sin;
-    p.status = status;
-    p.B = dims->B;
-    p.Hq = dims->Hq;
-    p.Hkv = dims->Hkv;
-    p.D = dims->D;
-    p.page_size = dims->page_size;
-    p.num_pages = dims->num_pages;
-    p.num_indices = dims->num_indices;
-    p.max_seq_len = dims->max_seq_len;
-    p.rope_max_pos = rope_max_pos;
-    p.rope_q = rope_q ? 1 : 0;
-    return launch_status(pkv::launch_append(p, (cudaStream_t)stream));
+    st = check_append_args(dims, q, k_new, v_new, k_pool, v_pool, kv_indices, kv_indptr,
+                           seq_lens, rope_cos_sin, rope_max_pos, rope_q, status);
+    if (st != PKV_OK)
+        return st;
+    return launch_append(dims, q, k_new, v_new, k_pool, v_pool, kv_indices, kv_indptr,
+                         seq_lens, rope_cos_sin, rope_max_pos, rope_q, status, stream);
 }
 
 pkv_status paged_decode_attn(const pkv_dims *dims, const void *q, const void *k_pool,
@@ -276,19 +427,60 @@ pkv_status paged_decode_attn(const pkv_dims *dims, const void *q, const void *k_
                              const int32_t *kv_indptr, const int32_t *seq_lens, int num_splits,
                              void *workspace, size_t ws_bytes, void *out, pkv_stream_t stream)
 {
-    if (out == nullptr && dims != nullptr && dims->B > 0)
-        return PKV_ERR_INVALID_ARG;
-    const bool direct = num_splits == 1;
-    pkv_status st = decode_common(dims, q, k_pool, v_pool, kv_indices, kv_indptr, seq_lens,
-                                  num_splits, workspace, ws_bytes, out, direct, stream);
-    if (st != PKV_OK || direct || dims->B == 0)
+    pkv_status st = check_decode_args(dims, q, k_pool, v_pool, kv_indices, kv_indptr,
+                                      seq_lens, num_splits, workspace, ws_bytes, out, true);
+    if (st != PKV_OK || dims->B == 0)
         return st;
-    size_t ml_off = 0, o_off = 0;
-    pkv_workspace_layout(dims, num_splits, &ml_off, &o_off);
-    return decode_combine(dims,
-                          reinterpret_cast<const float *>(static_cast<char *>(workspace) + o_off),
-                          reinterpret_cast<const float *>(static_cast<char *>(workspace) + ml_off),
-                          num_splits, out, stream);
+    if (fused_path_ok(dims))
+        return launch_persistent(dims, q, k_pool, v_pool, kv_indices, kv_indptr, seq_lens,
+                                 num_splits, workspace, out, nullptr, nullptr, nullptr, 0,
+                                 stream);
+    const bool direct = num_splits == 1;
+    st = launch_split(dims, q, k_pool, v_pool, kv_indices, kv_indptr, seq_lens, num_splits,
+                      workspace, out, direct, stream);
+    if (st != PKV_OK || direct)
+        return st;
+    return launch_combine_split(dims, num_splits, workspace, out, stream);
+}
+
+pkv_status paged_decode_step(const pkv_dims *dims, const void *q, const void *k_new,
+                             const void *v_new, void *k_pool, void *v_pool,
+                             const int32_t *kv_indices, const int32_t *kv_indptr,
+                             const int32_t *seq_lens, const float *rope_cos_sin,
+                             int rope_max_pos, int num_splits, void *workspace,
+                             size_t ws_bytes, void *out, pkv_stream_t stream)
+{
+    pkv_status st = check_decode_args(dims, q, k_pool, v_pool, kv_indices, kv_indptr,
+                                      seq_lens, num_splits, workspace, ws_bytes, out, true);
+    if (st != PKV_OK || dims->B == 0)
+        return st;
+    uint32_t *status = static_cast<uint32_t *>(workspace);
+    st = check_append_args(dims, q, k_new, v_new, k_pool, v_pool, kv_indices, kv_indptr,
+                           seq_lens, rope_cos_sin, rope_max_pos, 0, status);
+    if (st != PKV_OK)
+        return st;
+    if (fused_path_ok(dims))
+        return launch_persistent(dims, q, k_pool, v_pool, kv_indices, kv_indptr, seq_lens,
+                                 num_splits, workspace, out, k_new, v_new, rope_cos_sin,
+                                 rope_max_pos, stream);
+    // other shapes: rotate a copy of q in the workspace, append, then decode
+    const Layout L = layout_for(dims, num_splits);
+    void *qs = static_cast<char *>(workspace) + L.qscratch_off;
+    const size_t qbytes = (size_t)dims->B * dims->Hq * dims->D * 2;
+    st = launch_status(
+        cudaMemcpyAsync(qs, q, qbytes, cudaMemcpyDeviceToDevice, (cudaStream_t)stream));
+    if (st != PKV_OK)
+        return st;
+    st = launch_append(dims, qs, k_new, v_new, k_pool, v_pool, kv_indices, kv_indptr, seq_lens,
+                       rope_cos_sin, rope_max_pos, rope_cos_sin != nullptr, status, stream);
+    if (st != PKV_OK)
+        return st;
+    const bool direct = num_splits == 1;
+    st = launch_split(dims, qs, k_pool, v_pool, kv_indices, kv_indptr, seq_lens, num_splits,
+                      workspace, out, direct, stream);
+    if (st != PKV_OK || direct)
+        return st;
+    return launch_combine_split(dims, num_splits, workspace, out, stream);
 }
 
 pkv_status paged_decode_partials(const pkv_dims *dims, const void *q, const void *k_pool,
@@ -297,8 +489,12 @@ pkv_status paged_decode_partials(const pkv_dims *dims, const void *q, const void
                                  int num_splits, void *workspace, size_t ws_bytes,
                                  pkv_stream_t stream)
 {
-    return decode_common(dims, q, k_pool, v_pool, kv_indices, kv_indptr, seq_lens, num_splits,
-                         workspace, ws_bytes, nullptr, false, stream);
+    pkv_status st = check_decode_args(dims, q, k_pool, v_pool, kv_indices, kv_indptr,
+                                      seq_lens, num_splits, workspace, ws_bytes, nullptr, false);
+    if (st != PKV_OK || dims->B == 0)
+        return st;
+    return launch_split(dims, q, k_pool, v_pool, kv_indices, kv_indptr, seq_lens, num_splits,
+                        workspace, nullptr, false, stream);
 }
 
 pkv_status decode_combine(const pkv_dims *dims, const float *o_part, const float *ml_part,

@@ -22,24 +22,11 @@ namespace pkv {
 
 namespace {
 
-// Rotate the four interleaved pairs held in one 16-byte vector.  cs holds
-// (cos, sin) for those pairs: c0 s0 c1 s1 c2 s2 c3 s3.
-__device__ __forceinline__ uint4 rotate_vec8(uint4 x, float4 cs01, float4 cs23)
-{
-    auto rot = [](uint32_t w, float c, float s) -> uint32_t {
-        const float a = bf16_lo(w), b = bf16_hi(w);
-        return pack_bf16x2(fmaf(a, c, -b * s), fmaf(a, s, b * c));
-    };
-    uint4 y;
-    y.x = rot(x.x, cs01.x, cs01.y);
-    y.y = rot(x.y, cs01.z, cs01.w);
-    y.z = rot(x.z, cs23.x, cs23.y);
-    y.w = rot(x.w, cs23.z, cs23.w);
-    return y;
-}
-
 __global__ void __launch_bounds__(128) append_kernel(const AppendParams p)
 {
+    // the decode launched next may start its prologue; it waits for this
+    // grid's completion before it reads q or the pools
+    grid_launch_dependents();
     const int b = blockIdx.x;
     const int L = p.seq_lens[b];
     if (L <= 0) {
@@ -81,7 +68,7 @@ __global__ void __launch_bounds__(128) append_kernel(const AppendParams p)
         uint4 k = kin[it];
         if (cs != nullptr) {
             const float4 *c4 = reinterpret_cast<const float4 *>(cs + 8 * c);
-            k = rotate_vec8(k, c4[0], c4[1]);
+            k = rotate_pairs8(k, c4[0], c4[1]);
         }
         kout[it] = k;
         vout[it] = vin[it];
@@ -91,7 +78,7 @@ __global__ void __launch_bounds__(128) append_kernel(const AppendParams p)
         for (int it = threadIdx.x; it < p.Hq * vpr; it += blockDim.x) {
             const int c = it % vpr;
             const float4 *c4 = reinterpret_cast<const float4 *>(cs + 8 * c);
-            qrow[it] = rotate_vec8(qrow[it], c4[0], c4[1]);
+            qrow[it] = rotate_pairs8(qrow[it], c4[0], c4[1]);
         }
     }
 }

@@ -161,3 +161,52 @@ __device__ __forceinline__ float bf16_hi(uint32_t v)
 }
 
 } // namespace pkv
+
+namespace pkv {
+
+// Plain arrive (release, CTA scope) on an mbarrier.
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
+{
+    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar))
+                 : "memory");
+}
+
+// Barrier over a subset of the block's warps (ids 1..15; 0 is __syncthreads).
+__device__ __forceinline__ void named_bar_sync(int id, int threads)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// Programmatic dependent launch: wait for the preceding grid's completion and
+// memory flush (a no-op when the launch carried no such dependency) ...
+__device__ __forceinline__ void grid_dependency_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// ... and let the next grid in the stream start its prologue early.
+__device__ __forceinline__ void grid_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// RoPE on one interleaved pair held as packed bf16x2 (x = low half):
+// (x, y) -> (x c - y s, x s + y c) in fp32, rounded to bf16.
+__device__ __forceinline__ uint32_t rotate_pair(uint32_t w, float c, float s)
+{
+    const float a = bf16_lo(w), b = bf16_hi(w);
+    return pack_bf16x2(fmaf(a, c, -b * s), fmaf(a, s, b * c));
+}
+
+// The four pairs of one 16-byte vector; cs01 = (c0, s0, c1, s1), cs23 likewise.
+__device__ __forceinline__ uint4 rotate_pairs8(uint4 x, float4 cs01, float4 cs23)
+{
+    uint4 y;
+    y.x = rotate_pair(x.x, cs01.x, cs01.y);
+    y.y = rotate_pair(x.y, cs01.z, cs01.w);
+    y.z = rotate_pair(x.z, cs23.x, cs23.y);
+    y.w = rotate_pair(x.w, cs23.z, cs23.w);
+    return y;
+}
+
+} // namespace pkv

@@ -1,0 +1,790 @@
+// pkv_fused.cu -- the production split-KV decode kernel and its piece
+// combine.
+//
+// What it computes is the same as the split kernel in pkv_decode.cu (AstrAI
+// commit log, compare v1.3.12..6f09b1d, attention_ops.py attn_paged_decode):
+// out[b, h] = softmax(scale * q[b,h] K^T) V over the row's tokens, K/V of kv
+// head h / n_rep gathered token by token through the page table.  How the
+// work is cut differs from the pages' grid of (batch, head, split) blocks
+// (commits by author, "compute_num_splits ... target 512 blocks"):
+//
+//  - Persistent and token-balanced.  The grid has G blocks (one per SM).
+//    All rows' tokens, laid end to end, are cut into G equal contiguous
+//    ranges; block c streams range c, which may cover the tail of one row,
+//    whole rows and the head of another.  Each (block, row) overlap is a
+//    "piece".  No block waits on another and no block idles at the end.
+//  - All kv heads of a row in one block.  The pool is [page, slot, Hkv, D],
+//    so the HPC (<= 8) kv heads handled together are one contiguous run of
+//    HPC*D*2 bytes per token (2 KB at Hkv = 8, D = 128).  A producer warp
+//    copies one such run per token with cp.async.bulk (TMA engine) into a
+//    ring of 16-token stages (K rows, then V rows; rows padded by 16 bytes
+//    so ldmatrix reads are bank-conflict free), looked up through the page
+//    table token by token.  Full/empty mbarriers hand stages between the
+//    producer and the HPC consumer warps; every wait is time-bounded.
+//  - One consumer warp per kv head.  It serves that head's n_rep query heads
+//    (the M rows of m16n8k16 bf16 tensor-core products) from the shared
+//    stage: q.K^T, an fp32 online softmax in the log2 domain, then P.V with
+//    P rounded to bf16 and the running sum built from the same rounded P.
+//  - A piece that is a whole row writes the bf16 output directly.  Other
+//    pieces write (normalised o, m, l) partials to slot (block + row), and
+//    the piece combine kernel merges each row's consecutive pieces.
+#include <cmath>
+
+#include "pkv_device.cuh"
+#include "pkv_internal.h"
+
+namespace pkv {
+
+namespace {
+
+constexpr float kLn2f = 0.693147180559945309f;
+constexpr float kLog2ef = 1.4426950408889634f;
+constexpr int kSmemLimit = 232448;        // opt-in shared memory per block, sm_100 family
+constexpr unsigned kFull = 0xffffffffu;
+
+template <int D, int HPC>
+struct FusedCfg {
+    static constexpr int kTok = 16;
+    static constexpr int kThreads = (HPC + 1) * 32;
+    static constexpr int kRowBytes = HPC * D * 2;     // one token, HPC kv heads
+    static constexpr int kPitch = kRowBytes + 16;
+    static constexpr int kStageBytes = 2 * kTok * kPitch;
+    static constexpr int kFixedBytes = (kFusedMaxRows + 1) * 4 + 64 + 2 * 8 * 8;
+    static constexpr int kStagesFit = (kSmemLimit - kFixedBytes) / kStageBytes;
+    static constexpr int kStages = kStagesFit > 8 ? 8 : kStagesFit;
+    static_assert(kStages >= 2, "ring needs two stages");
+    static constexpr int kRingBytes = kStages * kStageBytes;
+    static constexpr int kBarOffset = kRingBytes;                    // full[], empty[]
+    static constexpr int kPrefixOffset = kBarOffset + 2 * kStages * 8;
+    static constexpr int kScratchOffset = kPrefixOffset + (kFusedMaxRows + 1) * 4;
+    static constexpr int kSmemBytes = kScratchOffset + 64;
+    static_assert(kSmemBytes <= kSmemLimit, "shared memory budget");
+};
+
+// Fused step: the stage holds the new token's raw K/V (copied from k_new /
+// v_new) in row jn.  This warp rotates its kv head's K slice there (the same
+// fp32 arithmetic as the append kernel, so the bits agree), and writes K and
+// V to the token's pool slot.  Lane l owns pairs 2l, 2l+1 of the head
+// (D = 128) or pair l (D = 64): cs holds their (cos, sin).
+template <int D, int kPitch, int kTok>
+__device__ __forceinline__ void insert_new_token(const FusedParams &p, unsigned char *stage_col,
+                                                 int jn, int lane, int b, int kvh, int tn,
+                                                 int page, float4 cs, bool rope_ok)
+{
+    const bool page_ok = page >= 0 && page < p.num_pages;
+    if (lane == 0) {
+        if (!page_ok)
+            atomicOr(p.status, kFlagBadPage);
+        if (!rope_ok)
+            atomicOr(p.status, kFlagBadPos);
+    }
+    unsigned char *krow = stage_col + jn * kPitch;
+    unsigned char *vrow = stage_col + (kTok + jn) * kPitch;
+    const int pin = p.ps_shift >= 0 ? (tn >> p.ps_shift) : (tn / p.page_size);
+    const size_t dst = (((size_t)page * p.page_size + (tn - pin * p.page_size)) * p.Hkv + kvh) * D;
+    if constexpr (D == 128) {
+        uint2 k = reinterpret_cast<uint2 *>(krow)[lane];
+        const uint2 v = reinterpret_cast<const uint2 *>(vrow)[lane];
+        if (p.rope != nullptr) {
+            if (rope_ok) {
+                k.x = rotate_pair(k.x, cs.x, cs.y);
+                k.y = rotate_pair(k.y, cs.z, cs.w);
+            } else {
+                k = make_uint2(0u, 0u);
+            }
+            reinterpret_cast<uint2 *>(krow)[lane] = k;
+        }
+        if (page_ok && rope_ok) {
+            reinterpret_cast<uint2 *>(p.k_pool_w + dst)[lane] = k;
+            reinterpret_cast<uint2 *>(p.v_pool_w + dst)[lane] = v;
+        }
+    } else {
+        uint32_t k = reinterpret_cast<uint32_t *>(krow)[lane];
+        const uint32_t v = reinterpret_cast<const uint32_t *>(vrow)[lane];
+        if (p.rope != nullptr) {
+            k = rope_ok ? rotate_pair(k, cs.x, cs.y) : 0u;
+            reinterpret_cast<uint32_t *>(krow)[lane] = k;
+        }
+        if (page_ok && rope_ok) {
+            reinterpret_cast<uint32_t *>(p.k_pool_w + dst)[lane] = k;
+            reinterpret_cast<uint32_t *>(p.v_pool_w + dst)[lane] = v;
+        }
+    }
+    // the stage is refilled by bulk copies later: order these generic writes
+    // before that async-proxy access, and make them visible to the warp
+    fence_proxy_async_smem();
+    __syncwarp();
+}
+
+// Block owning flattened token x under the partition x in [c*T/G, (c+1)*T/G).
+__device__ __forceinline__ int block_of(long long x, long long T, int G)
+{
+    return (int)(((x + 1) * G + T - 1) / T) - 1;
+}
+
+template <int D, int HPC>
+__global__ void __launch_bounds__(FusedCfg<D, HPC>::kThreads, 1)
+    fused_decode_kernel(const FusedParams p)
+{
+    using C = FusedCfg<D, HPC>;
+    constexpr int NST = C::kStages;
+    extern __shared__ __align__(128) unsigned char smem[];
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::kBarOffset);
+    uint64_t *empty = full + NST;
+    int *prefix = reinterpret_cast<int *>(smem + C::kPrefixOffset);
+    volatile int *scratch = reinterpret_cast<volatile int *>(smem + C::kScratchOffset);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int cta = blockIdx.x;
+    const int Bv = p.Bv;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < NST; ++i) {
+            mbar_init(&full[i], 32);     // every producer lane arrives
+            mbar_init(&empty[i], HPC);
+        }
+        fence_mbar_init();
+        scratch[0] = 0;   // abort flag
+    }
+    // inputs may come from the kernel just before (the append): wait for it
+    grid_dependency_wait();
+    grid_launch_dependents();
+
+    // ---- virtual-row lengths, checked, then their prefix sums -------------
+    for (int r = threadIdx.x; r < Bv; r += blockDim.x) {
+        const int b = r % p.B;
+        int L = p.seq_lens[b];
+        const int pg0 = p.kv_indptr[b];
+        const int pg1 = p.kv_indptr[b + 1];
+        unsigned bad = 0;
+        if (L < 0 || L > p.max_seq_len) {
+            bad |= kFlagBadLen;
+            L = L < 0 ? 0 : p.max_seq_len;
+        }
+        if (pg0 < 0 || pg1 < pg0 || pg1 > p.num_indices) {
+            bad |= kFlagBadPage;
+            L = 0;
+        } else if ((long long)(pg1 - pg0) * p.page_size < (long long)L) {
+            bad |= kFlagBadPage;
+            L = (pg1 - pg0) * p.page_size;
+        }
+        if (bad && cta == 0 && r < p.B)
+            atomicOr(p.status, bad);
+        prefix[r + 1] = L;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        int carry = 0;
+        for (int base = 0; base < Bv; base += 32) {
+            const int i = base + lane;
+            int v = i < Bv ? prefix[i + 1] : 0;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int n = __shfl_up_sync(kFull, v, off);
+                if (lane >= off)
+                    v += n;
+            }
+            v += carry;
+            if (i < Bv)
+                prefix[i + 1] = v;
+            carry = __shfl_sync(kFull, v, 31);
+        }
+        if (lane == 0)
+            prefix[0] = 0;
+    }
+    __syncthreads();
+
+    const long long T = prefix[Bv];
+    // fewer blocks when there is little work: at least kFusedMinTokens each
+    long long Ge = (T + kFusedMinTokens - 1) / kFusedMinTokens;
+    if (Ge > gridDim.x)
+        Ge = gridDim.x;
+    if (Ge < 1)
+        Ge = 1;
+    const int G = (int)Ge;
+
+    // rows with no tokens: zero output, no pieces (owner: block r mod grid)
+    for (int r = cta; r < Bv; r += gridDim.x) {
+        if (prefix[r + 1] == prefix[r]) {
+            const int b = r % p.B, hg = r / p.B;
+            uint4 *o = reinterpret_cast<uint4 *>(
+                p.out + ((size_t)b * p.Hq + (size_t)hg * HPC * p.n_rep) * D);
+            for (int i = threadIdx.x; i < HPC * p.n_rep * D / 8; i += blockDim.x)
+                o[i] = make_uint4(0u, 0u, 0u, 0u);
+            if (threadIdx.x == 0) {
+                p.row_info[2 * r] = 0;
+                p.row_info[2 * r + 1] = 0;
+            }
+        }
+    }
+    if (cta >= G)
+        return;
+    const long long start = T * cta / G;
+    const long long end = T * (cta + 1) / G;
+    if (start >= end)
+        return;
+
+    // first row with tokens in [start, end)
+    int r0 = 0;
+    {
+        int lo = 0, hi = Bv - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if ((long long)prefix[mid + 1] > start)
+                hi = mid;
+            else
+                lo = mid + 1;
+        }
+        r0 = lo;
+    }
+
+    if (warp == HPC) {
+        // ======================= producer warp ============================
+        const int my_t = lane & 15;
+        const bool my_v = lane >= 16;
+        const __nv_bfloat16 *pool = my_v ? p.v_pool : p.k_pool;
+        int it = 0;
+        bool aborted = false;
+        for (int r = r0; r < Bv && !aborted; ++r) {
+            const long long lo = prefix[r], hi = prefix[r + 1];
+            if (lo >= end)
+                break;
+            if (hi == lo)
+                continue;
+            const int t0 = (int)((start > lo ? start : lo) - lo);
+            const int t1 = (int)((end < hi ? end : hi) - lo);
+            const int b = r % p.B, hg = r / p.B;
+            const int pg0 = p.kv_indptr[b];
+            const int npg = p.kv_indptr[b + 1] - pg0;      // >= pages the row's tokens use
+            const size_t head_off = (size_t)hg * HPC * D;
+            // page-table window: lane l holds entries wb + l and wb + 32 + l of
+            // the row, loaded one window ahead of use; a 16-token tile spans at
+            // most 17 consecutive entries, which always lie inside the window
+            auto page_of_tok = [&](int t) {
+                return p.ps_shift >= 0 ? (t >> p.ps_shift) : (t / p.page_size);
+            };
+            int wb = (page_of_tok(t0) >> 5) << 5;
+            int idx0 = wb + lane < npg ? __ldg(p.kv_indices + pg0 + wb + lane) : 0;
+            int idx1 = wb + 32 + lane < npg ? __ldg(p.kv_indices + pg0 + wb + 32 + lane) : 0;
+            for (int tok = t0; tok < t1; tok += C::kTok, ++it) {
+                const int st = it % NST;
+                if (it >= NST) {
+                    const bool ok = mbar_wait_bounded(&empty[st], (uint32_t)(((it / NST) - 1) & 1));
+                    if (!__all_sync(kFull, ok) || scratch[0]) {
+                        aborted = true;
+                        if (lane == 0) {
+                            scratch[0] = 1;
+                            atomicOr(p.status, kFlagTimeout);
+                        }
+                        break;
+                    }
+                }
+                fence_proxy_async_smem();
+                const int nvalid = min(C::kTok, t1 - tok);
+                if (page_of_tok(tok) >= wb + 32) {       // slide the window by 32
+                    wb += 32;
+                    idx0 = idx1;
+                    idx1 = wb + 32 + lane < npg ? __ldg(p.kv_indices + pg0 + wb + 32 + lane) : 0;
+                }
+                unsigned char *row = smem + st * C::kStageBytes +
+                                     ((my_v ? C::kTok : 0) + my_t) * C::kPitch;
+                if (my_v && my_t >= nvalid) {
+                    // V rows past the piece's end must be finite (P is 0 there)
+                    uint4 *z = reinterpret_cast<uint4 *>(row);
+                    for (int k = 0; k < C::kRowBytes / 16; ++k)
+                        z[k] = make_uint4(0u, 0u, 0u, 0u);
+                }
+                // every lane joins the shuffles; only lanes with a token use them
+                const int t = tok + (my_t < nvalid ? my_t : 0);
+                const int pi = page_of_tok(t);
+                const int sl = t - pi * p.page_size;
+                const int wofs = pi - wb;                  // in [0, 64)
+                const int e0 = __shfl_sync(kFull, idx0, wofs & 31);
+                const int e1 = __shfl_sync(kFull, idx1, wofs & 31);
+                int page = wofs < 32 ? e0 : e1;
+                // fused step: the row's last token is this step's new token; its
+                // K/V come from k_new / v_new (the consumers rotate K in place)
+                const int jn = (p.step && t1 == (int)(hi - lo) && tok + nvalid == t1)
+                                   ? nvalid - 1 : -1;
+                if (lane == 0)
+                    mbar_arrive_expect_tx(&full[st], (uint32_t)(nvalid * 2 * C::kRowBytes));
+                else
+                    mbar_arrive(&full[st]);
+                if (my_t == jn) {
+                    const __nv_bfloat16 *src =
+                        (my_v ? p.v_new : p.k_new) + (size_t)b * p.Hkv * D + head_off;
+                    bulk_copy_g2s(row, src, C::kRowBytes, &full[st]);
+                }
+                if (my_t < nvalid && my_t != jn) {
+                    if (page < 0 || page >= p.num_pages) {
+                        atomicOr(p.status, kFlagBadPage);
+                        page = 0;
+                    }
+                    const __nv_bfloat16 *src =
+                        pool + ((size_t)page * p.page_size + sl) * (size_t)p.Hkv * D + head_off;
+                    bulk_copy_g2s(row, src, C::kRowBytes, &full[st]);
+                }
+            }
+        }
+        if (aborted) {
+            // let the copies already issued land before the block exits
+            for (int k = (it > NST ? it - NST : 0); k < it; ++k)
+                (void)mbar_wait_bounded(&full[k % NST], (uint32_t)((k / NST) & 1));
+        }
+        return;
+    }
+
+    // ========================= consumer warps ===============================
+    const int HQV = HPC * p.n_rep;          // query heads per virtual row
+    const int fr = lane >> 2;               // fragment row (and fr + 8)
+    const int cq = (lane & 3) * 2;          // fragment column pair
+    const int k_tok = (lane & 7) + ((lane >> 4) << 3);
+    const int k_col = ((lane >> 3) & 1) * 8;
+    const int v_tok = (lane & 7) + (((lane >> 3) & 1) << 3);
+    const int v_col = (lane >> 4) * 8;
+    const uint32_t smem_s = smem_addr(smem);
+    const uint32_t col_off = (uint32_t)(warp * D * 2);
+    int it = 0;
+    bool aborted = false;
+
+    for (int r = r0; r < Bv; ++r) {
+        const long long lo = prefix[r], hi = prefix[r + 1];
+        if (lo >= end)
+            break;
+        if (hi == lo)
+            continue;
+        const int t0 = (int)((start > lo ? start : lo) - lo);
+        const int t1 = (int)((end < hi ? end : hi) - lo);
+        const int b = r % p.B, hg = r / p.B;
+        const int kvh = hg * HPC + warp;
+        const size_t qrow0 = (size_t)b * p.Hq + (size_t)kvh * p.n_rep;
+        const int first = block_of(lo, T, G);
+        const int last = block_of(hi - 1, T, G);
+        if (t0 == 0 && warp == 0 && lane == 0) {
+            p.row_info[2 * r] = first;
+            p.row_info[2 * r + 1] = last - first + 1;
+        }
+
+        uint32_t qf[D / 16][4];
+        {
+            const uint32_t *q0 = reinterpret_cast<const uint32_t *>(p.q + (qrow0 + fr) * D);
+            const uint32_t *q1 = reinterpret_cast<const uint32_t *>(p.q + (qrow0 + fr + 8) * D);
+            const bool v0 = fr < p.n_rep, v1 = fr + 8 < p.n_rep;
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                qf[kk][0] = v0 ? __ldg(q0 + (kk * 16 + cq) / 2) : 0u;
+                qf[kk][1] = v1 ? __ldg(q1 + (kk * 16 + cq) / 2) : 0u;
+                qf[kk][2] = v0 ? __ldg(q0 + (kk * 16 + 8 + cq) / 2) : 0u;
+                qf[kk][3] = v1 ? __ldg(q1 + (kk * 16 + 8 + cq) / 2) : 0u;
+            }
+            // fused step: rotate q by the new token's position.  Each 32-bit
+            // word is one interleaved pair; words 0/1 hold pair kk*8 + lane%4,
+            // words 2/3 pair kk*8 + 4 + lane%4 (rows fr and fr + 8).
+            const int pos = (int)(hi - lo) - 1;
+            if (p.step && p.rope != nullptr && pos < p.rope_max_pos) {
+                const float2 *cs = reinterpret_cast<const float2 *>(p.rope + (size_t)pos * D);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const float2 ca = __ldg(cs + kk * 8 + (lane & 3));
+                    const float2 cb = __ldg(cs + kk * 8 + 4 + (lane & 3));
+                    qf[kk][0] = rotate_pair(qf[kk][0], ca.x, ca.y);
+                    qf[kk][1] = rotate_pair(qf[kk][1], ca.x, ca.y);
+                    qf[kk][2] = rotate_pair(qf[kk][2], cb.x, cb.y);
+                    qf[kk][3] = rotate_pair(qf[kk][3], cb.x, cb.y);
+                }
+            }
+        }
+        // fused step, piece ending the row: prefetch what the new token needs
+        // (its slot's page and the (cos, sin) of this lane's two pairs)
+        const int Lrow = (int)(hi - lo);
+        const bool has_new = p.step && t1 == Lrow;
+        int new_page = -1;
+        float4 new_cs = make_float4(1.f, 0.f, 1.f, 0.f);
+        bool new_rope_ok = true;
+        if (has_new) {
+            const int tn = Lrow - 1;
+            const int pin = p.ps_shift >= 0 ? (tn >> p.ps_shift) : (tn / p.page_size);
+            new_page = __ldg(p.kv_indices + p.kv_indptr[b] + pin);
+            if (p.rope != nullptr) {
+                new_rope_ok = tn < p.rope_max_pos;
+                if (new_rope_ok) {
+                    const float *row = p.rope + (size_t)tn * D;
+                    if constexpr (D == 128) {
+                        new_cs = __ldg(reinterpret_cast<const float4 *>(row) + lane);
+                    } else {
+                        const float2 c2 = __ldg(reinterpret_cast<const float2 *>(row) + lane);
+                        new_cs = make_float4(c2.x, c2.y, 1.f, 0.f);
+                    }
+                }
+            }
+        }
+
+        float m_run[2] = {-INFINITY, -INFINITY};
+        float l_run[2] = {0.f, 0.f};
+        float oacc[D / 8][4];
+#pragma unroll
+        for (int j = 0; j < D / 8; ++j)
+            oacc[j][0] = oacc[j][1] = oacc[j][2] = oacc[j][3] = 0.f;
+
+        for (int tok = t0; tok < t1; tok += C::kTok, ++it) {
+            const int st = it % NST;
+            if (!aborted) {
+                const bool ok = mbar_wait_bounded(&full[st], (uint32_t)((it / NST) & 1));
+                if (!__all_sync(kFull, ok) || scratch[0]) {
+                    aborted = true;
+                    if (lane == 0) {
+                        scratch[0] = 1;
+                        atomicOr(p.status, kFlagTimeout);
+                    }
+                }
+            }
+            if (!aborted) {
+                const int nvalid = min(C::kTok, t1 - tok);
+                const uint32_t kbase = smem_s + st * C::kStageBytes + col_off;
+                const uint32_t vbase = kbase + C::kTok * C::kPitch;
+                if (has_new && tok + nvalid == t1)
+                    insert_new_token<D, C::kPitch, C::kTok>(
+                        p, smem + st * C::kStageBytes + warp * D * 2, nvalid - 1, lane, b,
+                        kvh, Lrow - 1, new_page, new_cs, new_rope_ok);
+
+                float sacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                const uint32_t kaddr = kbase + k_tok * C::kPitch + k_col * 2;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    uint32_t b0, b1, b2, b3;
+                    ldmatrix_x4(b0, b1, b2, b3, kaddr + kk * 32);
+                    mma_bf16_16816(sacc[0], qf[kk], b0, b1);
+                    mma_bf16_16816(sacc[1], qf[kk], b2, b3);
+                }
+                float x[2][4];
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int tt = nt * 8 + cq + (e & 1);
+                        x[nt][e] = tt < nvalid ? sacc[nt][e] * p.scale_log2 : -INFINITY;
+                    }
+                float mx0 = fmaxf(fmaxf(x[0][0], x[0][1]), fmaxf(x[1][0], x[1][1]));
+                float mx1 = fmaxf(fmaxf(x[0][2], x[0][3]), fmaxf(x[1][2], x[1][3]));
+                mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, 1));
+                mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, 2));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, 1));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, 2));
+                const float mn0 = fmaxf(m_run[0], mx0);
+                const float mn1 = fmaxf(m_run[1], mx1);
+                const float base0 = mn0 == -INFINITY ? 0.f : mn0;
+                const float base1 = mn1 == -INFINITY ? 0.f : mn1;
+                const float alpha0 = exp2f(m_run[0] - base0);
+                const float alpha1 = exp2f(m_run[1] - base1);
+                m_run[0] = mn0;
+                m_run[1] = mn1;
+                uint32_t pa[4];
+                pa[0] = pack_bf16x2(exp2f(x[0][0] - base0), exp2f(x[0][1] - base0));
+                pa[1] = pack_bf16x2(exp2f(x[0][2] - base1), exp2f(x[0][3] - base1));
+                pa[2] = pack_bf16x2(exp2f(x[1][0] - base0), exp2f(x[1][1] - base0));
+                pa[3] = pack_bf16x2(exp2f(x[1][2] - base1), exp2f(x[1][3] - base1));
+                l_run[0] = l_run[0] * alpha0 + ((bf16_lo(pa[0]) + bf16_hi(pa[0])) +
+                                                (bf16_lo(pa[2]) + bf16_hi(pa[2])));
+                l_run[1] = l_run[1] * alpha1 + ((bf16_lo(pa[1]) + bf16_hi(pa[1])) +
+                                                (bf16_lo(pa[3]) + bf16_hi(pa[3])));
+#pragma unroll
+                for (int j = 0; j < D / 8; ++j) {
+                    oacc[j][0] *= alpha0;
+                    oacc[j][1] *= alpha0;
+                    oacc[j][2] *= alpha1;
+                    oacc[j][3] *= alpha1;
+                }
+                const uint32_t vaddr = vbase + v_tok * C::kPitch + v_col * 2;
+#pragma unroll
+                for (int jj = 0; jj < D / 16; ++jj) {
+                    uint32_t b0, b1, b2, b3;
+                    ldmatrix_x4_trans(b0, b1, b2, b3, vaddr + jj * 32);
+                    mma_bf16_16816(oacc[2 * jj], pa, b0, b1);
+                    mma_bf16_16816(oacc[2 * jj + 1], pa, b2, b3);
+                }
+            }
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&empty[st]);
+        }
+
+        // ---- end of the piece ----------------------------------------------
+        l_run[0] += __shfl_xor_sync(kFull, l_run[0], 1);
+        l_run[0] += __shfl_xor_sync(kFull, l_run[0], 2);
+        l_run[1] += __shfl_xor_sync(kFull, l_run[1], 1);
+        l_run[1] += __shfl_xor_sync(kFull, l_run[1], 2);
+        const float inv0 = l_run[0] > 0.f ? 1.f / l_run[0] : 0.f;
+        const float inv1 = l_run[1] > 0.f ? 1.f / l_run[1] : 0.f;
+        const bool w0 = fr < p.n_rep, w1 = fr + 8 < p.n_rep;
+        if (first == last) {
+            __nv_bfloat16 *o0 = p.out + (qrow0 + fr) * D + cq;
+            __nv_bfloat16 *o1 = p.out + (qrow0 + fr + 8) * D + cq;
+#pragma unroll
+            for (int j = 0; j < D / 8; ++j) {
+                if (w0)
+                    *reinterpret_cast<uint32_t *>(o0 + 8 * j) =
+                        pack_bf16x2(oacc[j][0] * inv0, oacc[j][1] * inv0);
+                if (w1)
+                    *reinterpret_cast<uint32_t *>(o1 + 8 * j) =
+                        pack_bf16x2(oacc[j][2] * inv1, oacc[j][3] * inv1);
+            }
+        } else {
+            const size_t slot0 = (size_t)(cta + r) * HQV + (size_t)warp * p.n_rep + fr;
+            float *o0 = p.o_part + slot0 * D + cq;
+            float *o1 = o0 + 8 * (size_t)D;
+#pragma unroll
+            for (int j = 0; j < D / 8; ++j) {
+                if (w0)
+                    *reinterpret_cast<float2 *>(o0 + 8 * j) =
+                        make_float2(oacc[j][0] * inv0, oacc[j][1] * inv0);
+                if (w1)
+                    *reinterpret_cast<float2 *>(o1 + 8 * j) =
+                        make_float2(oacc[j][2] * inv1, oacc[j][3] * inv1);
+            }
+            if ((lane & 3) == 0) {
+                float2 *ml = reinterpret_cast<float2 *>(p.ml_part);
+                if (w0)
+                    ml[slot0] = l_run[0] > 0.f ? make_float2(m_run[0] * kLn2f, l_run[0])
+                                               : make_float2(-INFINITY, 0.f);
+                if (w1)
+                    ml[slot0 + 8] = l_run[1] > 0.f ? make_float2(m_run[1] * kLn2f, l_run[1])
+                                                   : make_float2(-INFINITY, 0.f);
+            }
+        }
+    }
+}
+
+// ---- merge the pieces of every row that has more than one ------------------
+// A group of WPH warps merges one (virtual row, query head): warp w takes
+// pieces w, w + WPH, ... and keeps a running (M, den, acc) that it rescales
+// whenever a larger max arrives, so the loads of U pieces can be in flight
+// at once; the group then merges its warps' states in shared memory.
+template <int D, int WPH>
+__global__ void __launch_bounds__(WPH > 8 ? 32 * WPH : 256)
+    piece_combine_kernel(const PieceCombineParams p)
+{
+    constexpr int V = D / 32;                          // floats per lane
+    constexpr int U = WPH > 1 ? 8 : 4;                 // pieces loaded ahead per warp
+    constexpr int NWARP = WPH > 8 ? WPH : 8;
+    constexpr int GROUPS = NWARP / WPH;                // (row, head) pairs per block
+    __shared__ float s_m[NWARP], s_den[NWARP];
+    __shared__ float s_acc[NWARP][D];
+    grid_dependency_wait();
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int grp = warp / WPH, wi = warp % WPH;
+    const long long pair = (long long)blockIdx.x * GROUPS + grp;
+    const bool live = pair < (long long)p.Bv * p.HQV;
+    int n = 0, first = 0, r = 0, j = 0;
+    if (live) {
+        r = (int)(pair / p.HQV);
+        j = (int)(pair % p.HQV);
+        first = p.row_info[2 * r];
+        n = p.row_info[2 * r + 1];
+    }
+    const float2 *ml = reinterpret_cast<const float2 *>(p.ml_part);
+    float M = -INFINITY, den = 0.f;
+    float acc[V];
+#pragma unroll
+    for (int k = 0; k < V; ++k)
+        acc[k] = 0.f;
+    if (n > 1) {
+        for (int k0 = wi; k0 < n; k0 += WPH * U) {
+            float2 mlv[U];
+            float o[U][V];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int k = k0 + u * WPH;
+                if (k < n) {
+                    const size_t slot = (size_t)(first + k + r) * p.HQV + j;
+                    mlv[u] = __ldcg(ml + slot);
+                    const float *src = p.o_part + slot * D + lane * V;
+                    if constexpr (V == 4) {
+                        const float4 x = __ldcg(reinterpret_cast<const float4 *>(src));
+                        o[u][0] = x.x; o[u][1] = x.y; o[u][2] = x.z; o[u][3] = x.w;
+                    } else {
+                        const float2 x = __ldcg(reinterpret_cast<const float2 *>(src));
+                        o[u][0] = x.x; o[u][1] = x.y;
+                    }
+                } else {
+                    mlv[u] = make_float2(-INFINITY, 0.f);
+#pragma unroll
+                    for (int v = 0; v < V; ++v)
+                        o[u][v] = 0.f;
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                if (!(mlv[u].y > 0.f))
+                    continue;
+                const float mn = fmaxf(M, mlv[u].x);
+                const float a = exp2f((M - mn) * kLog2ef);            // 0 when M = -inf
+                const float w = mlv[u].y * exp2f((mlv[u].x - mn) * kLog2ef);
+                den = den * a + w;
+#pragma unroll
+                for (int v = 0; v < V; ++v)
+                    acc[v] = acc[v] * a + w * o[u][v];
+                M = mn;
+            }
+        }
+    }
+    if constexpr (WPH > 1) {
+        if (lane == 0) {
+            s_m[warp] = M;
+            s_den[warp] = den;
+        }
+#pragma unroll
+        for (int v = 0; v < V; ++v)
+            s_acc[warp][lane * V + v] = acc[v];
+        __syncthreads();
+        if (wi != 0)
+            return;
+        float Mg = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < WPH; ++w)
+            if (s_den[grp * WPH + w] > 0.f)
+                Mg = fmaxf(Mg, s_m[grp * WPH + w]);
+        den = 0.f;
+#pragma unroll
+        for (int v = 0; v < V; ++v)
+            acc[v] = 0.f;
+#pragma unroll
+        for (int w = 0; w < WPH; ++w) {
+            const int ww = grp * WPH + w;
+            if (!(s_den[ww] > 0.f))
+                continue;
+            const float f = exp2f((s_m[ww] - Mg) * kLog2ef);
+            den += s_den[ww] * f;
+#pragma unroll
+            for (int v = 0; v < V; ++v)
+                acc[v] += s_acc[ww][lane * V + v] * f;
+        }
+    }
+    if (n <= 1)
+        return;
+    const float inv = den > 0.f ? 1.f / den : 0.f;
+    const int b = r % p.B, hg = r / p.B;
+    __nv_bfloat16 *dst =
+        p.out + ((size_t)b * p.Hq + (size_t)hg * p.HQV + j) * D + lane * V;
+    if constexpr (V == 4) {
+        uint2 v;
+        v.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+        v.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+        *reinterpret_cast<uint2 *>(dst) = v;
+    } else {
+        *reinterpret_cast<uint32_t *>(dst) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+    }
+}
+
+template <typename Kernel, typename Params>
+cudaError_t launch_pdl(Kernel k, dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       const Params &p)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k, p);
+}
+
+template <int D, int HPC>
+cudaError_t launch_fused_cfg(const FusedParams &p, int grid, cudaStream_t stream)
+{
+    using C = FusedCfg<D, HPC>;
+    static bool attr_done = false;
+    if (!attr_done) {
+        cudaError_t e = cudaFuncSetAttribute(fused_decode_kernel<D, HPC>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             C::kSmemBytes);
+        if (e != cudaSuccess)
+            return e;
+        e = cudaFuncSetAttribute(fused_decode_kernel<D, HPC>,
+                                 cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 cudaSharedmemCarveoutMaxShared);
+        if (e != cudaSuccess)
+            return e;
+        attr_done = true;
+    }
+    cudaError_t e = launch_pdl(fused_decode_kernel<D, HPC>, dim3(grid), dim3(C::kThreads),
+                               C::kSmemBytes, stream, p);
+    if (e != cudaSuccess)
+        return e;
+    return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_fused_d(const FusedParams &p, int grid, cudaStream_t stream)
+{
+    switch (p.hpc) {
+    case 8:
+        return launch_fused_cfg<D, 8>(p, grid, stream);
+    case 4:
+        return launch_fused_cfg<D, 4>(p, grid, stream);
+    case 2:
+        return launch_fused_cfg<D, 2>(p, grid, stream);
+    default:
+        return launch_fused_cfg<D, 1>(p, grid, stream);
+    }
+}
+
+} // namespace
+
+int fused_heads_per_block(int Hkv)
+{
+    if (Hkv % 8 == 0)
+        return 8;
+    if (Hkv % 4 == 0)
+        return 4;
+    if (Hkv % 2 == 0)
+        return 2;
+    return 1;
+}
+
+cudaError_t launch_fused_decode(const FusedParams &p, int D, int grid, cudaStream_t stream)
+{
+    if (D == 64)
+        return launch_fused_d<64>(p, grid, stream);
+    return launch_fused_d<128>(p, grid, stream);
+}
+
+cudaError_t launch_piece_combine(const PieceCombineParams &p, int D, int grid_blocks,
+                                 cudaStream_t stream)
+{
+    // warps per (row, head): enough that each warp merges <= ~16 pieces of
+    // the expected G / Bv + 2 per row
+    const long long expect = grid_blocks / (p.Bv > 0 ? p.Bv : 1) + 2;
+    const int wph = expect <= 16 ? 1 : expect <= 32 ? 2 : expect <= 64 ? 4 : expect <= 128 ? 8 : 16;
+    const long long pairs = (long long)p.Bv * p.HQV;
+    const int warps = wph > 8 ? wph : 8;
+    const int groups = warps / wph;
+    const unsigned blocks = (unsigned)((pairs + groups - 1) / groups);
+    cudaError_t e;
+#define PKV_COMBINE_CASE(DD, W)                                                              \
+    e = launch_pdl(piece_combine_kernel<DD, W>, dim3(blocks), dim3(warps * 32), 0, stream, p)
+    if (D == 64) {
+        if (wph == 1) PKV_COMBINE_CASE(64, 1);
+        else if (wph == 2) PKV_COMBINE_CASE(64, 2);
+        else if (wph == 4) PKV_COMBINE_CASE(64, 4);
+        else if (wph == 8) PKV_COMBINE_CASE(64, 8);
+        else PKV_COMBINE_CASE(64, 16);
+    } else {
+        if (wph == 1) PKV_COMBINE_CASE(128, 1);
+        else if (wph == 2) PKV_COMBINE_CASE(128, 2);
+        else if (wph == 4) PKV_COMBINE_CASE(128, 4);
+        else if (wph == 8) PKV_COMBINE_CASE(128, 8);
+        else PKV_COMBINE_CASE(128, 16);
+    }
+#undef PKV_COMBINE_CASE
+    if (e != cudaSuccess)
+        return e;
+    return cudaGetLastError();
+}
+
+} // namespace pkv

@@ -40,6 +40,46 @@ struct DecodeParams {
     float scale_log2;      // scale * log2(e)
 };
 
+// Persistent token-balanced decode (pkv_fused.cu).
+constexpr int kFusedMaxRows = 4096;     // virtual rows whose prefix sums fit in smem
+constexpr int kFusedMinTokens = 64;     // fewest tokens a block is given
+
+struct FusedParams {
+    const __nv_bfloat16 *q;
+    const __nv_bfloat16 *k_pool;
+    const __nv_bfloat16 *v_pool;
+    const int32_t *kv_indices;
+    const int32_t *kv_indptr;
+    const int32_t *seq_lens;
+    __nv_bfloat16 *out;
+    float *o_part;         // [(grid + Bv) * HQV, D]  piece partials
+    float *ml_part;        // [(grid + Bv) * HQV, 2]
+    int32_t *row_info;     // [Bv, 2]: first block, piece count
+    uint32_t *status;
+    int B, Hq, Hkv, n_rep, page_size, ps_shift, num_pages, num_indices, max_seq_len;
+    int Bv;                // virtual rows: (Hkv / hpc) head groups x B
+    int hpc;               // kv heads per block (1, 2, 4 or 8)
+    float scale_log2;
+    // fused step: the new token (k_new, v_new at position seq_len - 1) is
+    // rotated, written to its pool slot and attended from shared memory; q
+    // is rotated in registers.  step == 0: plain decode over the pool.
+    int step;
+    __nv_bfloat16 *k_pool_w;          // the pools, writable (step only)
+    __nv_bfloat16 *v_pool_w;
+    const __nv_bfloat16 *k_new;       // [B, Hkv, D]
+    const __nv_bfloat16 *v_new;
+    const float *rope;                // [rope_max_pos, D/2, 2] or nullptr
+    int rope_max_pos;
+};
+
+struct PieceCombineParams {
+    const float *o_part;
+    const float *ml_part;
+    const int32_t *row_info;
+    __nv_bfloat16 *out;
+    int B, Bv, Hq, HQV;
+};
+
 struct CombineParams {
     const float *o_part;
     const float *ml_part;
@@ -52,6 +92,10 @@ cudaError_t launch_rope_table(float *cos_sin, int max_pos, int D, double base,
                               cudaStream_t stream);
 cudaError_t launch_split_decode(const DecodeParams &p, int D, cudaStream_t stream);
 cudaError_t launch_combine(const CombineParams &p, cudaStream_t stream);
+cudaError_t launch_fused_decode(const FusedParams &p, int D, int grid, cudaStream_t stream);
+cudaError_t launch_piece_combine(const PieceCombineParams &p, int D, int grid_blocks,
+                                 cudaStream_t stream);
+int fused_heads_per_block(int Hkv);
 
 // Resident split-decode blocks per SM for head dim D (shared-memory bound).
 int split_decode_blocks_per_sm(int D);

@@ -33,7 +33,8 @@ FLAG_TIMEOUT = 0x8
 EXPORTS = (
     "pkv_split_chunk", "pkv_workspace_bytes", "pkv_workspace_layout", "pkv_plan",
     "pkv_workspace_init", "pkv_rope_table", "paged_kv_append", "paged_decode_attn",
-    "paged_decode_partials", "decode_combine", "pkv_status_str", "pkv_version",
+    "paged_decode_step", "paged_decode_partials", "decode_combine", "pkv_status_str",
+    "pkv_version",
 )
 
 
@@ -81,6 +82,7 @@ def lib():
             "pkv_rope_table": (I, [P, I, I, ctypes.c_double, P]),
             "paged_kv_append": (I, [DP, P, P, P, P, P, P, P, P, P, I, I, P, P]),
             "paged_decode_attn": (I, [DP, P, P, P, P, P, P, I, P, Z, P, P]),
+            "paged_decode_step": (I, [DP, P, P, P, P, P, P, P, P, P, I, I, P, Z, P, P]),
             "paged_decode_partials": (I, [DP, P, P, P, P, P, P, I, P, Z, P]),
             "decode_combine": (I, [DP, P, P, I, P, P]),
             "pkv_status_str": (ctypes.c_char_p, [I]),
@@ -184,6 +186,16 @@ def paged_decode_attn(d: Dims, q, k_pool, v_pool, kv_indices, kv_indptr, seq_len
         ctypes.byref(d), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(kv_indices),
         _ptr(kv_indptr), _ptr(seq_lens), num_splits, _ptr(workspace), ws_bytes, _ptr(out),
         _stream(stream)))
+
+
+def paged_decode_step(d: Dims, q, k_new, v_new, k_pool, v_pool, kv_indices, kv_indptr,
+                      seq_lens, rope_cos_sin, rope_max_pos: int, num_splits: int, workspace,
+                      out, stream=None) -> None:
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check("paged_decode_step", lib().paged_decode_step(
+        ctypes.byref(d), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_pool), _ptr(v_pool),
+        _ptr(kv_indices), _ptr(kv_indptr), _ptr(seq_lens), _ptr(rope_cos_sin), rope_max_pos,
+        num_splits, _ptr(workspace), ws_bytes, _ptr(out), _stream(stream)))
 
 
 def paged_decode_partials(d: Dims, q, k_pool, v_pool, kv_indices, kv_indptr, seq_lens,

@@ -74,7 +74,7 @@ def test_workspace_layout_and_bytes():
     for S in (1, 5, 64):
         ml, o = pkv.workspace_layout(d, S)
         n = d.B * d.Hq * S
-        assert ml == 256 and ml % 256 == 0 and o % 256 == 0
+        assert ml >= 256 + d.B * 8 and ml % 256 == 0 and o % 256 == 0
         assert o >= ml + n * 8
         assert pkv.workspace_bytes(d, S) >= o + n * d.D * 4
         assert pkv.workspace_bytes(d, S) % 256 == 0
@@ -85,11 +85,20 @@ def test_workspace_layout_and_bytes():
 def test_plan_invariants(B, Hkv, max_len):
     d = _d(B=B, Hkv=Hkv, Hq=Hkv * 4, max_seq_len=max_len)
     S, ws = pkv.plan(d, num_sms=152)
-    assert 1 <= S <= max(1, -(-max_len // 256))       # never below 256 tokens a split
+    # persistent path: at most one block per SM, each with >= 64 tokens of capacity
+    assert 1 <= S <= 152
+    assert S <= max(1, -(-B * max_len // 64))
     assert ws == pkv.workspace_bytes(d, S)
-    # a long single row is split across the machine
-    if B == 1 and max_len >= 32768:
-        assert S >= 64
+    if B * max_len >= 152 * 64:
+        assert S == 152
+
+
+def test_plan_fallback_shape():
+    # more than 4096 virtual rows: the per-(split, head, row) kernel is used
+    d = _d(B=5000, Hq=2, Hkv=1, D=64, max_seq_len=4096)
+    S, ws = pkv.plan(d, num_sms=152)
+    assert 1 <= S <= -(-4096 // 256)
+    assert ws == pkv.workspace_bytes(d, S)
 
 
 def test_invalid_shapes_rejected():

@@ -86,6 +86,16 @@ def test_capacity_above_lengths():
         _full_step(w, num_splits=S)
 
 
+@pytest.mark.parametrize("S", [1, 4])
+def test_many_rows_fallback_path(S):
+    # more than 4096 virtual rows (Hkv = 1): the per-(split, head, row) kernel
+    # and the standalone combine serve the call
+    g = torch.Generator().manual_seed(3)
+    lens = torch.randint(0, 40, (4200,), generator=g).tolist()
+    w = wl.build("many", B=4200, Hq=2, Hkv=1, D=64, page_size=16, seq_lens=lens, seed=3)
+    _full_step(w, num_splits=S)
+
+
 def test_all_rows_empty():
     w = wl.build("empty", B=3, Hq=8, Hkv=2, D=64, page_size=16, seq_lens=[0, 0, 0], seed=1,
                  max_seq_len=64)

@@ -102,3 +102,33 @@ def test_graph_replay_bitwise_and_rebind(B):
     assert torch.equal(replay2.view(torch.int16), f.out.view(torch.int16))
     compare_out(replay2, oracle_step(w2)["out"])
     assert pkv.status_word(f.ws) == 0
+
+
+@pytest.mark.parametrize("B", [4, 64])
+def test_graph_fused_step(B):
+    """paged_decode_step captured once; replays with rebound inputs equal eager."""
+    need = max(sum(-(-L // 16) for L in wl.serving(B, seed=s).seq_lens.tolist())
+               for s in (0, 1))
+    num_pages = 2 * need + 16
+    f = Fixed(B, num_pages)
+
+    def fused():
+        pkv.paged_decode_step(f.d, f.q_in, f.k_new, f.v_new, f.k_pool, f.v_pool, f.kv_indices,
+                              f.kv_indptr, f.seq_lens, f.rope, CAP, f.S, f.ws, f.out)
+
+    w1, w2 = _serving_like(B, 0, num_pages), _serving_like(B, 1, num_pages)
+    f.load(w1)
+    fused()
+    eager = f.out.clone()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fused()
+    f.out.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(f.out.view(torch.int16), eager.view(torch.int16))
+    f.load(w2)
+    g.replay()
+    torch.cuda.synchronize()
+    compare_out(f.out, oracle_step(w2)["out"])
+    assert pkv.status_word(f.ws) == 0
