@@ -210,6 +210,35 @@ pkv_status decode_combine(const pkv_dims *dims, const float *o_part,
                           const float *ml_part, int num_splits, void *out,
                           pkv_stream_t stream);
 
+/* ---- for callers that cannot allocate ------------------------------------ */
+
+/* Size of the library-held scratch used by paged_decode_attn_noalloc. */
+#define PKV_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+/* paged_decode_attn without a caller workspace.  The pages have no
+ * counterpart: this exists for callers that cannot allocate device memory
+ * (a runtime whose memory pool owns every allocation, a plugin host that
+ * forbids allocation while it executes, a path that must not fail on
+ * out-of-memory), so they cannot provide the workspace the other calls need.
+ * The workspace is a 16 MiB array the library keeps in device memory on
+ * every GPU that loads it, until the process exits; this call allocates
+ * nothing (no cudaMalloc, cudaFree or allocating library routine).
+ * Arguments and results are those of paged_decode_attn.  A shape whose
+ * workspace (pkv_workspace_bytes(dims, num_splits)) exceeds
+ * PKV_NOALLOC_SCRATCH_BYTES is rejected with PKV_ERR_WORKSPACE_TOO_SMALL.
+ * status (nullable, device, 4-byte aligned) receives this call's PKV_FLAG_*
+ * word; the word is cleared at the start of every call.
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture.  All calls share the one array and keep the last call's contents:
+ * calls that can overlap on the GPU (other streams, other threads) race and
+ * must be serialised by the caller. */
+pkv_status paged_decode_attn_noalloc(const pkv_dims *dims, const void *q,
+                                     const void *k_pool, const void *v_pool,
+                                     const int32_t *kv_indices, const int32_t *kv_indptr,
+                                     const int32_t *seq_lens, int num_splits, void *out,
+                                     uint32_t *status, pkv_stream_t stream);
+
 const char *pkv_status_str(pkv_status s);
 
 /* ABI version: (major << 16) | minor. */

@@ -34,7 +34,7 @@ EXPORTS = (
     "pkv_split_chunk", "pkv_workspace_bytes", "pkv_workspace_layout", "pkv_plan",
     "pkv_workspace_init", "pkv_rope_table", "paged_kv_append", "paged_decode_attn",
     "paged_decode_step", "paged_decode_partials", "decode_combine", "pkv_status_str",
-    "pkv_version",
+    "pkv_version", "paged_decode_attn_noalloc",
 )
 
 
@@ -85,6 +85,7 @@ def lib():
             "paged_decode_step": (I, [DP, P, P, P, P, P, P, P, P, P, I, I, P, Z, P, P]),
             "paged_decode_partials": (I, [DP, P, P, P, P, P, P, I, P, Z, P]),
             "decode_combine": (I, [DP, P, P, I, P, P]),
+            "paged_decode_attn_noalloc": (I, [DP, P, P, P, P, P, P, I, P, P, P]),
             "pkv_status_str": (ctypes.c_char_p, [I]),
             "pkv_version": (I, []),
         }
@@ -196,6 +197,20 @@ def paged_decode_step(d: Dims, q, k_new, v_new, k_pool, v_pool, kv_indices, kv_i
         ctypes.byref(d), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_pool), _ptr(v_pool),
         _ptr(kv_indices), _ptr(kv_indptr), _ptr(seq_lens), _ptr(rope_cos_sin), rope_max_pos,
         num_splits, _ptr(workspace), ws_bytes, _ptr(out), _stream(stream)))
+
+
+NOALLOC_SCRATCH_BYTES = 16 << 20
+
+
+def paged_decode_attn_noalloc(d: Dims, q, k_pool, v_pool, kv_indices, kv_indptr, seq_lens,
+                              num_splits: int, out, status=None, stream=None) -> None:
+    """paged_decode_attn for callers that cannot allocate: the workspace is
+    the library's own 16 MiB device array, shared by every call (calls that
+    overlap on the GPU race)."""
+    _check("paged_decode_attn_noalloc", lib().paged_decode_attn_noalloc(
+        ctypes.byref(d), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(kv_indices),
+        _ptr(kv_indptr), _ptr(seq_lens), num_splits, _ptr(out), _ptr(status),
+        _stream(stream)))
 
 
 def paged_decode_partials(d: Dims, q, k_pool, v_pool, kv_indices, kv_indptr, seq_lens,
