@@ -565,7 +565,7 @@ __global__ void __launch_bounds__(WPH > 8 ? 32 * WPH : 256)
     piece_combine_kernel(const PieceCombineParams p)
 {
     constexpr int V = D / 32;                          // floats per lane
-    constexpr int U = WPH > 1 ? 8 : 4;                 // pieces loaded ahead per warp
+    constexpr int U = WPH >= 16 ? 16 : 8;              // pieces loaded ahead per warp
     constexpr int NWARP = WPH > 8 ? WPH : 8;
     constexpr int GROUPS = NWARP / WPH;                // (row, head) pairs per block
     __shared__ float s_m[NWARP], s_den[NWARP];
@@ -757,10 +757,11 @@ cudaError_t launch_fused_decode(const FusedParams &p, int D, int grid, cudaStrea
 cudaError_t launch_piece_combine(const PieceCombineParams &p, int D, int grid_blocks,
                                  cudaStream_t stream)
 {
-    // warps per (row, head): enough that each warp merges <= ~16 pieces of
-    // the expected G / Bv + 2 per row
-    const long long expect = grid_blocks / (p.Bv > 0 ? p.Bv : 1) + 2;
-    const int wph = expect <= 16 ? 1 : expect <= 32 ? 2 : expect <= 64 ? 4 : expect <= 128 ? 8 : 16;
+    // warps per (row, head): enough that each warp loads all its pieces in
+    // one round
+    // rows are uneven: size for three times the average pieces per row
+    const long long expect = 3 * (grid_blocks / (p.Bv > 0 ? p.Bv : 1)) + 2;
+    const int wph = expect <= 8 ? 1 : expect <= 16 ? 2 : expect <= 32 ? 4 : expect <= 64 ? 8 : 16;
     const long long pairs = (long long)p.Bv * p.HQV;
     const int warps = wph > 8 ? wph : 8;
     const int groups = warps / wph;

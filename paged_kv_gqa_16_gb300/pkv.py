@@ -16,7 +16,8 @@ import threading
 from typing import Optional
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "_build", "libpkv.so")
+# the in-tree build; PKV_LIB may name another build of the same library
+LIB_PATH = os.environ.get("PKV_LIB") or os.path.join(_PKG, "_build", "libpkv.so")
 
 PKV_OK = 0
 PKV_ERR_INVALID_ARG = -1
