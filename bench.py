@@ -40,8 +40,8 @@ if ROOT not in sys.path:
 
 METRIC = "paged GQA decode attn: µs/call and KV-read GB/s (% of GB300 HBM peak)"
 FALLBACK_HBM_GBS = 6800.0
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "split_decode_traffic.json")
-DECODE_SRC = os.path.join(ROOT, "paged_kv_gqa_16_gb300", "csrc", "pkv_decode.cu")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "fused_decode_traffic.json")
+DECODE_SRC = os.path.join(ROOT, "paged_kv_gqa_16_gb300", "csrc", "pkv_fused.cu")
 
 
 def parse_args(argv=None):
@@ -111,8 +111,8 @@ def load_peaks():
 
 
 def cached_traffic(workload: str, splits: int):
-    """DRAM bytes per split-decode launch from a committed ncu summary, valid
-    only while the kernel source is unchanged (else None)."""
+    """DRAM bytes per launch of the fused decode kernel from a committed ncu
+    summary, valid only while the kernel source is unchanged (else None)."""
     try:
         with open(TRAFFIC_FILE) as f:
             j = json.load(f)
