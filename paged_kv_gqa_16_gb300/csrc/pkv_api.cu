@@ -104,7 +104,8 @@ Layout layout_for(const pkv_dims *d, int num_splits)
 bool fused_path_ok(const pkv_dims *d)
 {
     const Layout L = layout_for(d, 1);
-    return L.Bv <= pkv::kFusedMaxRows && (long long)L.Bv * d->max_seq_len < (1ll << 31);
+    return L.Bv <= pkv::kFusedMaxRows &&
+           (long long)L.Bv * ((long long)d->max_seq_len + pkv::kFusedRowCost) < (1ll << 31);
 }
 
 pkv_status check_decode_args(const pkv_dims *dims, const void *q, const void *k_pool,
@@ -222,6 +223,7 @@ pkv_status launch_persistent(const pkv_dims *dims, const void *q, const void *k_
     p.num_indices = dims->num_indices;
     p.max_seq_len = dims->max_seq_len;
     p.Bv = L.Bv;
+    p.row_cost = pkv::kFusedRowCost;
     p.hpc = L.hpc;
     p.scale_log2 = (float)((double)dims->scale * 1.4426950408889634);
     p.step = k_new != nullptr ? 1 : 0;

@@ -9,10 +9,12 @@
 // (commits by author, "compute_num_splits ... target 512 blocks"):
 //
 //  - Persistent and token-balanced.  The grid has G blocks (one per SM).
-//    All rows' tokens, laid end to end, are cut into G equal contiguous
-//    ranges; block c streams range c, which may cover the tail of one row,
-//    whole rows and the head of another.  Each (block, row) overlap is a
-//    "piece".  No block waits on another and no block idles at the end.
+//    All rows, laid end to end, are cut into G equal contiguous ranges;
+//    block c streams range c, which may cover the tail of one row, whole
+//    rows and the head of another.  Each (block, row) overlap with tokens is
+//    a "piece".  A row weighs its tokens plus a fixed row cost (placed
+//    before its first token), so blocks that start more rows stream fewer
+//    tokens.  No block waits on another.
 //  - All kv heads of a row in one block.  The pool is [page, slot, Hkv, D],
 //    so the HPC (<= 8) kv heads handled together are one contiguous run of
 //    HPC*D*2 bytes per token (2 KB at Hkv = 8, D = 128).  A producer warp
@@ -57,8 +59,19 @@ struct FusedCfg {
     static constexpr int kBarOffset = kRingBytes;                    // full[], empty[]
     static constexpr int kPrefixOffset = kBarOffset + 2 * kStages * 8;
     static constexpr int kScratchOffset = kPrefixOffset + (kFusedMaxRows + 1) * 4;
-    static constexpr int kSmemBytes = kScratchOffset + 64;
+    // per-row q block and RoPE row, copied ahead by the producer: two
+    // mbarriers, the (cos, sin) row, then as many q bytes as fit
+    static constexpr int kQBarOffset = (kScratchOffset + 64 + 15) / 16 * 16;
+    static constexpr int kCsOffset = kQBarOffset + 16;
+    static constexpr int kQOffset = (kCsOffset + D * 4 + 127) / 128 * 128;
+    static constexpr int kQWant = 16 * HPC * D * 2;                   // n_rep up to 16
+    static constexpr int kQFree = (kSmemLimit - kQOffset) / 128 * 128;
+    static constexpr int kQCapBytes = kQWant < kQFree ? kQWant : kQFree;
+    static constexpr int kSmemBytes = kQOffset + kQCapBytes;
     static_assert(kSmemBytes <= kSmemLimit, "shared memory budget");
+    static_assert(kQBarOffset % 16 == 0 && kCsOffset % 16 == 0 && kQOffset % 16 == 0,
+                  "bulk-copy destinations and mbarriers need 16-byte alignment");
+    static_assert(kBarOffset % 16 == 0 && kPrefixOffset % 16 == 0, "alignment");
 };
 
 // Fused step: the stage holds the new token's raw K/V (copied from k_new /
@@ -133,6 +146,9 @@ __global__ void __launch_bounds__(FusedCfg<D, HPC>::kThreads, 1)
     uint64_t *empty = full + NST;
     int *prefix = reinterpret_cast<int *>(smem + C::kPrefixOffset);
     volatile int *scratch = reinterpret_cast<volatile int *>(smem + C::kScratchOffset);
+    uint64_t *qbar = reinterpret_cast<uint64_t *>(smem + C::kQBarOffset);
+    const float *s_cs = reinterpret_cast<const float *>(smem + C::kCsOffset);
+    const __nv_bfloat16 *s_q = reinterpret_cast<const __nv_bfloat16 *>(smem + C::kQOffset);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -144,12 +160,13 @@ __global__ void __launch_bounds__(FusedCfg<D, HPC>::kThreads, 1)
             mbar_init(&full[i], 32);     // every producer lane arrives
             mbar_init(&empty[i], HPC);
         }
+        mbar_init(&qbar[0], 1);          // q block landed
+        mbar_init(&qbar[1], HPC);        // every consumer has read it
         fence_mbar_init();
         scratch[0] = 0;   // abort flag
     }
     // inputs may come from the kernel just before (the append): wait for it
     grid_dependency_wait();
-    grid_launch_dependents();
 
     // ---- virtual-row lengths, checked, then their prefix sums -------------
     for (int r = threadIdx.x; r < Bv; r += blockDim.x) {
@@ -171,7 +188,7 @@ __global__ void __launch_bounds__(FusedCfg<D, HPC>::kThreads, 1)
         }
         if (bad && cta == 0 && r < p.B)
             atomicOr(p.status, bad);
-        prefix[r + 1] = L;
+        prefix[r + 1] = L > 0 ? L + p.row_cost : 0;
     }
     __syncthreads();
     if (warp == 0) {
@@ -195,6 +212,8 @@ __global__ void __launch_bounds__(FusedCfg<D, HPC>::kThreads, 1)
     }
     __syncthreads();
 
+    // T: the rows' total weight.  Token t of row r sits at position
+    // prefix[r] + row_cost + t; block c owns positions [T c / G, T (c+1) / G).
     const long long T = prefix[Bv];
     // fewer blocks when there is little work: at least kFusedMinTokens each
     long long Ge = (T + kFusedMinTokens - 1) / kFusedMinTokens;
@@ -225,7 +244,7 @@ __global__ void __launch_bounds__(FusedCfg<D, HPC>::kThreads, 1)
     if (start >= end)
         return;
 
-    // first row with tokens in [start, end)
+    // first row whose positions reach past start (never an empty row)
     int r0 = 0;
     {
         int lo = 0, hi = Bv - 1;
@@ -239,18 +258,49 @@ __global__ void __launch_bounds__(FusedCfg<D, HPC>::kThreads, 1)
         r0 = lo;
     }
 
+    // the row's q block (and RoPE row) is staged in shared memory by the
+    // producer when it fits, so consumers never stall on q at a row start
+    const int HQVb = HPC * p.n_rep;
+    const bool q_staged = HQVb * D * 2 <= C::kQCapBytes;
+    auto rope_row_needed = [&](long long lo_, long long hi_) {
+        const int pos = (int)(hi_ - lo_) - 1;
+        return p.step && p.rope != nullptr && pos < p.rope_max_pos;
+    };
+
     if (warp == HPC) {
         // ======================= producer warp ============================
         const int my_t = lane & 15;
         const bool my_v = lane >= 16;
         const __nv_bfloat16 *pool = my_v ? p.v_pool : p.k_pool;
-        int it = 0;
+        int it = 0, pc = 0;
         bool aborted = false;
+        auto page_of_tok = [&](int t) {
+            return p.ps_shift >= 0 ? (t >> p.ps_shift) : (t / p.page_size);
+        };
+        // the next row's first page-table window, loaded one row ahead
+        int n_r = -1, n_idx0 = 0, n_idx1 = 0;
+        auto prefetch_window = [&](int from) {
+            n_r = -1;
+            for (int rr = from; rr < Bv; ++rr) {
+                if ((long long)prefix[rr] + p.row_cost >= end)
+                    break;
+                if (prefix[rr + 1] == prefix[rr])
+                    continue;
+                const int bb = rr % p.B;
+                const int q0 = p.kv_indptr[bb];
+                const int nq = p.kv_indptr[bb + 1] - q0;
+                n_idx0 = lane < nq ? __ldg(p.kv_indices + q0 + lane) : 0;
+                n_idx1 = 32 + lane < nq ? __ldg(p.kv_indices + q0 + 32 + lane) : 0;
+                n_r = rr;
+                break;
+            }
+        };
         for (int r = r0; r < Bv && !aborted; ++r) {
-            const long long lo = prefix[r], hi = prefix[r + 1];
+            // [lo, hi): the positions of the row's tokens
+            const long long lo = (long long)prefix[r] + p.row_cost, hi = prefix[r + 1];
             if (lo >= end)
                 break;
-            if (hi == lo)
+            if (hi == prefix[r])
                 continue;
             const int t0 = (int)((start > lo ? start : lo) - lo);
             const int t1 = (int)((end < hi ? end : hi) - lo);
@@ -261,12 +311,42 @@ __global__ void __launch_bounds__(FusedCfg<D, HPC>::kThreads, 1)
             // page-table window: lane l holds entries wb + l and wb + 32 + l of
             // the row, loaded one window ahead of use; a 16-token tile spans at
             // most 17 consecutive entries, which always lie inside the window
-            auto page_of_tok = [&](int t) {
-                return p.ps_shift >= 0 ? (t >> p.ps_shift) : (t / p.page_size);
-            };
             int wb = (page_of_tok(t0) >> 5) << 5;
-            int idx0 = wb + lane < npg ? __ldg(p.kv_indices + pg0 + wb + lane) : 0;
-            int idx1 = wb + 32 + lane < npg ? __ldg(p.kv_indices + pg0 + wb + 32 + lane) : 0;
+            int idx0, idx1;
+            if (n_r == r && wb == 0) {
+                idx0 = n_idx0;
+                idx1 = n_idx1;
+            } else {
+                idx0 = wb + lane < npg ? __ldg(p.kv_indices + pg0 + wb + lane) : 0;
+                idx1 = wb + 32 + lane < npg ? __ldg(p.kv_indices + pg0 + wb + 32 + lane) : 0;
+            }
+            // stage the row's q block (and RoPE row) for the consumers
+            if (q_staged) {
+                if (pc > 0) {
+                    const bool ok = mbar_wait_bounded(&qbar[1], (uint32_t)((pc - 1) & 1));
+                    if (!__all_sync(kFull, ok) || scratch[0]) {
+                        aborted = true;
+                        if (lane == 0) {
+                            scratch[0] = 1;
+                            atomicOr(p.status, kFlagTimeout);
+                        }
+                        break;
+                    }
+                }
+                if (lane == 0) {
+                    const bool need_cs = rope_row_needed(lo, hi);
+                    const uint32_t qbytes = (uint32_t)(HQVb * D * 2);
+                    mbar_arrive_expect_tx(&qbar[0], qbytes + (need_cs ? D * 4 : 0));
+                    bulk_copy_g2s(const_cast<__nv_bfloat16 *>(s_q),
+                                  p.q + ((size_t)b * p.Hq + (size_t)hg * HQVb) * D, qbytes,
+                                  &qbar[0]);
+                    if (need_cs)
+                        bulk_copy_g2s(const_cast<float *>(s_cs),
+                                      p.rope + (size_t)(hi - lo - 1) * D, D * 4, &qbar[0]);
+                }
+                ++pc;
+            }
+            prefetch_window(r + 1);
             for (int tok = t0; tok < t1; tok += C::kTok, ++it) {
                 const int st = it % NST;
                 if (it >= NST) {
@@ -331,7 +411,13 @@ __global__ void __launch_bounds__(FusedCfg<D, HPC>::kThreads, 1)
             // let the copies already issued land before the block exits
             for (int k = (it > NST ? it - NST : 0); k < it; ++k)
                 (void)mbar_wait_bounded(&full[k % NST], (uint32_t)((k / NST) & 1));
+            if (pc > 0)
+                (void)mbar_wait_bounded(&qbar[0], (uint32_t)((pc - 1) & 1));
         }
+        // the piece combine may be scheduled once every block has signalled;
+        // signalling at the end (not the start) keeps its blocks from piling
+        // onto the first SMs to free up
+        grid_launch_dependents();
         return;
     }
 
@@ -345,14 +431,14 @@ __global__ void __launch_bounds__(FusedCfg<D, HPC>::kThreads, 1)
     const int v_col = (lane >> 4) * 8;
     const uint32_t smem_s = smem_addr(smem);
     const uint32_t col_off = (uint32_t)(warp * D * 2);
-    int it = 0;
+    int it = 0, pc = 0;
     bool aborted = false;
 
     for (int r = r0; r < Bv; ++r) {
-        const long long lo = prefix[r], hi = prefix[r + 1];
+        const long long lo = (long long)prefix[r] + p.row_cost, hi = prefix[r + 1];
         if (lo >= end)
             break;
-        if (hi == lo)
+        if (hi == prefix[r])
             continue;
         const int t0 = (int)((start > lo ? start : lo) - lo);
         const int t1 = (int)((end < hi ? end : hi) - lo);
@@ -368,31 +454,58 @@ __global__ void __launch_bounds__(FusedCfg<D, HPC>::kThreads, 1)
 
         uint32_t qf[D / 16][4];
         {
-            const uint32_t *q0 = reinterpret_cast<const uint32_t *>(p.q + (qrow0 + fr) * D);
-            const uint32_t *q1 = reinterpret_cast<const uint32_t *>(p.q + (qrow0 + fr + 8) * D);
             const bool v0 = fr < p.n_rep, v1 = fr + 8 < p.n_rep;
+            const bool rot = rope_row_needed(lo, hi);
+            const int pos = (int)(hi - lo) - 1;
+            const uint32_t *q0, *q1;
+            const float2 *cs;
+            if (q_staged) {
+                // staged by the producer when it started this row
+                if (!aborted) {
+                    const bool ok = mbar_wait_bounded(&qbar[0], (uint32_t)(pc & 1));
+                    if (!__all_sync(kFull, ok) || scratch[0]) {
+                        aborted = true;
+                        if (lane == 0) {
+                            scratch[0] = 1;
+                            atomicOr(p.status, kFlagTimeout);
+                        }
+                    }
+                }
+                const size_t lrow = (size_t)warp * p.n_rep + fr;
+                q0 = reinterpret_cast<const uint32_t *>(s_q + lrow * D);
+                q1 = reinterpret_cast<const uint32_t *>(s_q + (lrow + 8) * D);
+                cs = reinterpret_cast<const float2 *>(s_cs);
+            } else {
+                q0 = reinterpret_cast<const uint32_t *>(p.q + (qrow0 + fr) * D);
+                q1 = reinterpret_cast<const uint32_t *>(p.q + (qrow0 + fr + 8) * D);
+                cs = reinterpret_cast<const float2 *>(p.rope + (size_t)(rot ? pos : 0) * D);
+            }
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
-                qf[kk][0] = v0 ? __ldg(q0 + (kk * 16 + cq) / 2) : 0u;
-                qf[kk][1] = v1 ? __ldg(q1 + (kk * 16 + cq) / 2) : 0u;
-                qf[kk][2] = v0 ? __ldg(q0 + (kk * 16 + 8 + cq) / 2) : 0u;
-                qf[kk][3] = v1 ? __ldg(q1 + (kk * 16 + 8 + cq) / 2) : 0u;
+                qf[kk][0] = v0 ? q0[(kk * 16 + cq) / 2] : 0u;
+                qf[kk][1] = v1 ? q1[(kk * 16 + cq) / 2] : 0u;
+                qf[kk][2] = v0 ? q0[(kk * 16 + 8 + cq) / 2] : 0u;
+                qf[kk][3] = v1 ? q1[(kk * 16 + 8 + cq) / 2] : 0u;
             }
             // fused step: rotate q by the new token's position.  Each 32-bit
             // word is one interleaved pair; words 0/1 hold pair kk*8 + lane%4,
             // words 2/3 pair kk*8 + 4 + lane%4 (rows fr and fr + 8).
-            const int pos = (int)(hi - lo) - 1;
-            if (p.step && p.rope != nullptr && pos < p.rope_max_pos) {
-                const float2 *cs = reinterpret_cast<const float2 *>(p.rope + (size_t)pos * D);
+            if (rot) {
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const float2 ca = __ldg(cs + kk * 8 + (lane & 3));
-                    const float2 cb = __ldg(cs + kk * 8 + 4 + (lane & 3));
+                    const float2 ca = cs[kk * 8 + (lane & 3)];
+                    const float2 cb = cs[kk * 8 + 4 + (lane & 3)];
                     qf[kk][0] = rotate_pair(qf[kk][0], ca.x, ca.y);
                     qf[kk][1] = rotate_pair(qf[kk][1], ca.x, ca.y);
                     qf[kk][2] = rotate_pair(qf[kk][2], cb.x, cb.y);
                     qf[kk][3] = rotate_pair(qf[kk][3], cb.x, cb.y);
                 }
+            }
+            if (q_staged) {
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&qbar[1]);
+                ++pc;
             }
         }
         // fused step, piece ending the row: prefetch what the new token needs
@@ -553,6 +666,7 @@ __global__ void __launch_bounds__(FusedCfg<D, HPC>::kThreads, 1)
             }
         }
     }
+    grid_launch_dependents();
 }
 
 // ---- merge the pieces of every row that has more than one ------------------

@@ -43,6 +43,12 @@ struct DecodeParams {
 // Persistent token-balanced decode (pkv_fused.cu).
 constexpr int kFusedMaxRows = 4096;     // virtual rows whose prefix sums fit in smem
 constexpr int kFusedMinTokens = 64;     // fewest tokens a block is given
+// Partition weight of a row beyond its tokens: a block pays a fixed cost at
+// each row it starts (page-table window, q block, partial write), measured
+// at about 1.8 us per extra row, the time of ~20 streamed tokens.  Charging
+// it in the partition gives blocks that cross more row boundaries fewer
+// tokens; 32 measured best of {0, 16, 32, 48} on the serving mixes.
+constexpr int kFusedRowCost = 32;
 
 struct FusedParams {
     const __nv_bfloat16 *q;
@@ -58,6 +64,7 @@ struct FusedParams {
     uint32_t *status;
     int B, Hq, Hkv, n_rep, page_size, ps_shift, num_pages, num_indices, max_seq_len;
     int Bv;                // virtual rows: (Hkv / hpc) head groups x B
+    int row_cost;          // partition weight of a non-empty row beyond its tokens
     int hpc;               // kv heads per block (1, 2, 4 or 8)
     float scale_log2;
     // fused step: the new token (k_new, v_new at position seq_len - 1) is
