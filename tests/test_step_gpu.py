@@ -75,3 +75,18 @@ def test_step_fallback_path(S):
     lens = torch.randint(0, 40, (4200,), generator=g).tolist()
     w = wl.build("stf", B=4200, Hq=2, Hkv=1, D=64, page_size=16, seq_lens=lens, seed=4)
     _check(w, S)
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_step_many_short_rows(seed):
+    """Hundreds of rows of 0-40 tokens.  Every block's range holds several
+    rows' fixed partition weight, some ranges end inside a row's weight
+    before its first token, and most rows are single pieces."""
+    g = torch.Generator().manual_seed(seed)
+    lens = torch.randint(0, 41, (600,), generator=g)
+    lens[::7] = 0
+    lens[1::11] = 1
+    w = wl.build("short", B=600, Hq=8, Hkv=8, D=64, page_size=16, seq_lens=lens.tolist(),
+                 seed=seed)
+    _check(w)
+    _check(w, 152)
