@@ -79,6 +79,7 @@ def _load():
         lib.po_decode_partials.argtypes = [I, I, I, I, I, I, P, P, P, P, P, P, D, I, L, P, P]
         lib.po_combine.restype = I
         lib.po_combine.argtypes = [I, I, I, I, P, P, P]
+        lib.po_advance.argtypes = [I, I, I, I, P, P, P, P, I, P, P, P, P]
         lib.po_set_threads.argtypes = [I]
         lib.po_max_threads.restype = I
         _lib = lib
@@ -226,3 +227,23 @@ def combine(o_part, ml_part) -> np.ndarray:
     rc = _load().po_combine(B, Hq, D, S, _ptr(o_part), _ptr(ml_part), _ptr(out))
     _check(rc, "combine")
     return out
+
+
+def advance(seq_lens, kv_indptr, kv_indices, free_pages, head: int, page_size: int,
+            max_seq_len: int):
+    """One decode step's metadata advance (see po_advance).  Returns
+    (seq_lens, kv_indices, head, n_len, n_page, n_bad) as new int32 arrays /
+    ints; the inputs are not modified."""
+    sl = np.array(np.asarray(seq_lens), dtype=np.int32, copy=True)
+    ind = np.array(np.asarray(kv_indices), dtype=np.int32, copy=True)
+    ptr = np.ascontiguousarray(np.asarray(kv_indptr), dtype=np.int32)
+    fp = np.ascontiguousarray(np.asarray(free_pages if free_pages is not None else []),
+                              dtype=np.int32)
+    h = np.array([head], dtype=np.int32)
+    c = [ctypes.c_int(0), ctypes.c_int(0), ctypes.c_int(0)]
+    rc = _load().po_advance(len(sl), page_size, max_seq_len, len(ind), _ptr(sl), _ptr(ptr),
+                            _ptr(ind) if len(ind) else None, _ptr(fp) if len(fp) else None,
+                            len(fp), _ptr(h), ctypes.byref(c[0]), ctypes.byref(c[1]),
+                            ctypes.byref(c[2]))
+    _check(rc, "advance")
+    return sl, ind, int(h[0]), c[0].value, c[1].value, c[2].value

@@ -31,6 +31,9 @@
  *   - commits by author, split-KV decode ("split partials", "single combine
  *       kernel", "compute_num_splits"): per-split partial outputs and
  *       (max, sum) statistics merged by a combine pass.
+ *   - same diff, cache.py, PagePool.task_extend / _extend_slot and the
+ *       steady-state branch of bind_tasks: one more token per task, and a
+ *       page from the allocator when the token starts a page (po_advance).
  *
  * Readings where the pages are silent (each also listed in the design notes):
  *   - kv_indptr[b] .. kv_indptr[b+1] indexes the PAGES of row b in kv_indices;
@@ -416,6 +419,58 @@ int po_combine(int B, int Hq, int D, int num_splits, const double *o_part,
 }
 
 /* ------------------------------------------------------------- threads -- */
+
+/* ------------------------------------------------------------- advance -- */
+
+/* One steady-state decode step of metadata, in the pages' order (compare
+ * v1.3.12..6f09b1d, astrai/inference/core/cache.py: PagePool.task_extend
+ * refuses pos >= max_seq_len; _extend_slot computes page_idx = pos /
+ * page_size and, when that is past the pages the task holds, takes a page
+ * from the allocator, failing if it has none; task_extend then sets the
+ * length to pos + 1).  The tasks are the rows with seq_lens[b] > 0, visited
+ * in increasing b; the new token's position is pos = seq_lens[b]; the pages
+ * a row holds are ceil(pos / page_size), so page_idx is past them exactly
+ * when pos is a multiple of page_size; the allocator hands out
+ * free_pages[*head], free_pages[*head + 1], ... in the order of the calls.
+ * A row's page list lives at kv_indices[kv_indptr[b] ...] with room for
+ * kv_indptr[b+1] - kv_indptr[b] entries; a row with no room, or one that
+ * finds the list empty, keeps its length.
+ * Counts the rows refused for length (*n_len) and for want of a page or an
+ * entry (*n_page); rows whose kv_indptr pair is malformed count in *n_bad.
+ * Returns 0. */
+int po_advance(int B, int page_size, int max_seq_len, int num_indices, int32_t *seq_lens,
+               const int32_t *kv_indptr, int32_t *kv_indices, const int32_t *free_pages,
+               int num_free, int32_t *head, int *n_len, int *n_page, int *n_bad)
+{
+    *n_len = *n_page = *n_bad = 0;
+    for (int b = 0; b < B; ++b) {
+        const int L = seq_lens[b];
+        if (L <= 0)
+            continue;                       /* not a task this step */
+        const int pos = L;
+        if (pos >= max_seq_len) {
+            ++*n_len;
+            continue;
+        }
+        const int page_idx = pos / page_size;
+        const int held = (L + page_size - 1) / page_size;
+        if (page_idx >= held) {             /* the token starts a new page */
+            const int first = kv_indptr[b], room = kv_indptr[b + 1] - kv_indptr[b];
+            if (first < 0 || room < 0 || kv_indptr[b + 1] > num_indices) {
+                ++*n_bad;
+                continue;
+            }
+            if (page_idx >= room || *head >= num_free) {
+                ++*n_page;
+                continue;
+            }
+            kv_indices[first + page_idx] = free_pages[*head];
+            ++*head;
+        }
+        seq_lens[b] = pos + 1;
+    }
+    return 0;
+}
 
 void po_set_threads(int n)
 {

@@ -259,3 +259,82 @@ def make(name: str, seed: int = 0, **kw) -> Workload:
     if name.startswith("serving_b"):
         return serving(int(name[len("serving_b"):]), seed=seed)
     return CASES[name](seed=seed, **kw)
+
+
+# ------------------------------------------------------- multi-step decode loop
+@dataclass
+class LoopState:
+    """Inputs of a decode loop whose page table grows on the device.
+
+    Row b owns ``kv_indices[kv_indptr[b] : kv_indptr[b+1]]`` (``cap`` entries,
+    a strided table); its first ``ceil(seq_lens[b] / page_size)`` entries are
+    the pages it holds, the rest are -1.  ``free_pages`` lists every pool page
+    no row holds, shuffled.  ``seq_lens`` are the tokens already cached, before
+    the first step; rows with 0 are idle.  Step s appends ``k_new[s]`` /
+    ``v_new[s]``.  All bf16 arrays are uint16 bit patterns; pool pages that no
+    row holds, and slots past each row's tokens, are NaN."""
+    B: int
+    Hq: int
+    Hkv: int
+    D: int
+    page_size: int
+    num_pages: int
+    cap: int
+    max_seq_len: int
+    steps: int
+    seq_lens: np.ndarray      # int32 [B]
+    kv_indptr: np.ndarray     # int32 [B+1]
+    kv_indices: np.ndarray    # int32 [B*cap]
+    free_pages: np.ndarray    # int32 [n_free]
+    q: np.ndarray             # uint16 [B, Hq, D]
+    k_new: np.ndarray         # uint16 [steps, B, Hkv, D]
+    v_new: np.ndarray
+    k_pool: np.ndarray        # uint16 [num_pages, page_size, Hkv, D]
+    v_pool: np.ndarray
+    rope_base: float = 10000.0
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.D)
+
+
+def decode_loop(*, B: int, Hq: int, Hkv: int, D: int, page_size: int, seq_lens, steps: int,
+                cap: int, num_pages: int, seed: int = 0) -> LoopState:
+    gen = torch.Generator().manual_seed(seed)
+    lens = [int(x) for x in seq_lens]
+    assert len(lens) == B
+    held = [-(-L // page_size) for L in lens]
+    assert all(h + -(-steps // page_size) + 1 <= cap for h in held), "cap too small"
+    n_held = sum(held)
+    assert n_held <= num_pages
+    perm = torch.randperm(num_pages, generator=gen).to(torch.int32).numpy()
+    indptr = (np.arange(B + 1, dtype=np.int64) * cap).astype(np.int32)
+    indices = np.full(B * cap, -1, dtype=np.int32)
+    k = 0
+    for b in range(B):
+        indices[b * cap: b * cap + held[b]] = perm[k: k + held[b]]
+        k += held[b]
+    free = perm[k:].copy()
+
+    def bits(t: torch.Tensor) -> np.ndarray:
+        return t.contiguous().view(torch.int16).numpy().view(np.uint16).copy()
+
+    q = bits(_randn_bf16((B, Hq, D), gen))
+    k_new = bits(_randn_bf16((steps, B, Hkv, D), gen))
+    v_new = bits(_randn_bf16((steps, B, Hkv, D), gen))
+    k_pool = np.full((num_pages, page_size, Hkv, D), NAN_BF16_BITS, dtype=np.uint16)
+    v_pool = np.full_like(k_pool, NAN_BF16_BITS)
+    kv = bits(_randn_bf16((2, max(n_held, 1), page_size, Hkv, D), gen))
+    j = 0
+    for b in range(B):
+        for pj in range(held[b]):
+            page = indices[b * cap + pj]
+            n = min(page_size, lens[b] - pj * page_size)
+            k_pool[page, :n] = kv[0, j, :n]
+            v_pool[page, :n] = kv[1, j, :n]
+            j += 1
+    return LoopState(B=B, Hq=Hq, Hkv=Hkv, D=D, page_size=page_size, num_pages=num_pages,
+                     cap=cap, max_seq_len=cap * page_size, steps=steps,
+                     seq_lens=np.array(lens, dtype=np.int32), kv_indptr=indptr,
+                     kv_indices=indices, free_pages=free, q=q, k_new=k_new, v_new=v_new,
+                     k_pool=k_pool, v_pool=v_pool)

@@ -434,3 +434,59 @@ def test_combine_rules():
     assert np.all(oracle.combine(o, ml3) == 0.0)
     np.testing.assert_array_equal(oracle.combine(o[:, :, :1], ml[:, :, :1]),
                                   o[:, :, 0].astype(np.float64))
+
+
+# -------------------------------------------------------------- advance ---
+def test_advance_golden():
+    """Hand-worked steps (page_size 4, four table entries per row).
+
+    Row lengths 0, 3, 4, 8, 5, 12, 16: row 0 is idle; rows 1 and 4 grow
+    inside their last page (positions 3 and 5); rows 2, 3 and 5 start a page
+    (positions 4, 8, 12: page index 1, 2, 3) and take the free pages in row
+    order; row 6 (position 16, page index 4) has no fifth entry.  With the
+    list [100, 101] from head 0, row 5 finds it empty."""
+    ptr = np.arange(8, dtype=np.int32) * 4
+    ind = np.full(28, -1, np.int32)
+    sl, ind2, head, n_len, n_page, n_bad = oracle.advance(
+        [0, 3, 4, 8, 5, 12, 16], ptr, ind, [100, 101], 0, page_size=4, max_seq_len=64)
+    assert sl.tolist() == [0, 4, 5, 9, 6, 12, 16]
+    want = ind.copy()
+    want[2 * 4 + 1] = 100
+    want[3 * 4 + 2] = 101
+    assert ind2.tolist() == want.tolist()
+    assert (head, n_len, n_page, n_bad) == (2, 0, 2, 0)
+    # a longer list from head 1: row 5 now gets a page (the list's third)
+    sl, ind2, head, _, n_page, _ = oracle.advance(
+        [0, 3, 4, 8, 5, 12, 16], ptr, ind, [7, 100, 101, 102], 1, page_size=4, max_seq_len=64)
+    assert sl.tolist() == [0, 4, 5, 9, 6, 13, 16]
+    assert (ind2[9], ind2[14], ind2[23], head, n_page) == (100, 101, 102, 4, 1)
+    # the length bound: position max_seq_len - 1 is the last one allowed
+    sl, _, _, n_len, _, _ = oracle.advance([7, 8, 9], np.arange(4, dtype=np.int32) * 4,
+                                           np.full(12, 5, np.int32), [1], 0, page_size=4,
+                                           max_seq_len=8)
+    assert sl.tolist() == [8, 8, 9] and n_len == 2
+
+
+def test_advance_page_count_over_many_steps():
+    """After k steps with a large free list, each live row holds
+    ceil((L + k) / ps) pages: the pages taken are the difference, all distinct,
+    and they come off the list in order."""
+    g = torch.Generator().manual_seed(11)
+    B, ps, k, cap = 40, 8, 37, 24
+    lens = torch.randint(0, 120, (B,), generator=g).tolist()
+    lens[3] = 0
+    lens[4] = 8
+    ptr = np.arange(B + 1, dtype=np.int32) * cap
+    ind = np.full(B * cap, -1, np.int32)
+    free = np.arange(1000, 1000 + B * cap, dtype=np.int32)[::-1].copy()
+    sl, head = np.array(lens, np.int32), 0
+    for _ in range(k):
+        sl, ind, head, n_len, n_page, n_bad = oracle.advance(sl, ptr, ind, free, head, ps, 10 ** 6)
+        assert n_len == n_page == n_bad == 0
+    live = np.array(lens) > 0
+    assert np.array_equal(sl, np.where(live, np.array(lens) + k, 0))
+    taken = sum(-(-(L + k) // ps) - -(-L // ps) for L in lens if L > 0)
+    assert head == taken
+    got = ind[ind >= 0]
+    assert len(got) == taken and len(set(got.tolist())) == taken
+    assert set(got.tolist()) == set(free[:taken].tolist())
