@@ -56,6 +56,8 @@ def parse_args(argv=None):
     ap.add_argument("--impl", choices=["pkv", "reference"], default="pkv")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-loop", action="store_true",
+                    help="skip the decode-loop leg (paged_kv_advance + step per graph)")
     ap.add_argument("--no-flush", action="store_true", help="skip the L2 flush (not for reporting)")
     ap.add_argument("--flush-always", action="store_true",
                     help="flush the L2 before every step even when the inputs exceed it")
@@ -294,6 +296,7 @@ def run_reference(args):
 
 
 def run_pkv(args):
+    import numpy as np
     import torch
     from paged_kv_gqa_16_gb300 import build as pkv_build
     from paged_kv_gqa_16_gb300 import pkv
@@ -449,6 +452,89 @@ def run_pkv(args):
     if status != 0:
         raise SystemExit(f"device status {status:#x} after the timed run")
 
+    # decode loop: the same rows as a loop whose table grows on the device.
+    # LOOP steps per graph, each paged_kv_advance + paged_decode_step (the
+    # step's new token at the advanced length), against the same graph
+    # without the advance; the small state is reset between replays, outside
+    # the events, and nothing is flushed (consecutive steps, as in serving).
+    loop = None
+    if not args.no_loop:
+        LOOP, reps = 20, 20
+        before = (w.seq_lens - 1).clamp(min=0).tolist()     # cached tokens before a step
+        held_max = max(-(-L // w.page_size) for L in before)
+        cap = held_max + -(-LOOP // w.page_size) + 2
+        need = sum(-(-L // w.page_size) for L in before) + w.B * (-(-LOOP // w.page_size) + 1)
+        ls = wl.decode_loop(B=w.B, Hq=w.Hq, Hkv=w.Hkv, D=w.D, page_size=w.page_size,
+                            seq_lens=before, steps=LOOP, cap=cap, num_pages=need + 64,
+                            seed=1000 + rank)
+
+        def t16(a):
+            return torch.from_numpy(a.view(np.int16).copy()).view(torch.bfloat16).to(dev)
+
+        ld = pkv.dims(w.B, w.Hq, w.Hkv, w.D, w.page_size, ls.num_pages, len(ls.kv_indices),
+                      ls.max_seq_len, w.scale)
+        lS = args.splits or pkv.plan(ld)[0]
+        lws = pkv.alloc_workspace(ld, lS, dev)
+        lq, lkn, lvn = t16(ls.q), t16(ls.k_new), t16(ls.v_new)
+        lkp, lvp = t16(ls.k_pool), t16(ls.v_pool)
+        lrope = torch.empty(ls.max_seq_len, w.D // 2, 2, dtype=torch.float32, device=dev)
+        pkv.rope_table(lrope, ls.max_seq_len, w.D, w.rope_base or 10000.0)
+        lsl0 = torch.from_numpy(ls.seq_lens).to(dev)
+        lind0 = torch.from_numpy(ls.kv_indices).to(dev)
+        lsl, lind = lsl0.clone(), lind0.clone()
+        lptr = torch.from_numpy(ls.kv_indptr).to(dev)
+        lfree = torch.from_numpy(ls.free_pages).to(dev)
+        lhead = torch.zeros(1, dtype=torch.int32, device=dev)
+        lout = torch.empty(w.B, w.Hq, w.D, dtype=torch.bfloat16, device=dev)
+
+        def one(st, adv):
+            if adv:
+                pkv.paged_kv_advance(ld, lsl, lptr, lind, lfree, lhead, status=lws)
+            pkv.paged_decode_step(ld, lq, lkn[st], lvn[st], lkp, lvp, lind, lptr, lsl, lrope,
+                                  ls.max_seq_len, lS, lws, lout)
+
+        def reset():
+            lsl.copy_(lsl0)
+            lind.copy_(lind0)
+            lhead.zero_()
+
+        def loop_graph(adv):
+            reset()
+            for st in range(LOOP):
+                one(st, adv)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                for st in range(LOOP):
+                    one(st, adv)
+            return g
+
+        def loop_timed(g):
+            ms = []
+            for _ in range(reps + 3):
+                reset()
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                g.replay()
+                b.record(stream)
+                torch.cuda.synchronize(dev)
+                ms.append(a.elapsed_time(b) / LOOP)
+            return statistics.median(ms[3:])
+
+        g_adv, g_noadv = loop_graph(True), loop_graph(False)
+        ms_adv = loop_timed(g_adv)
+        pages_taken = int(lhead.item())
+        ms_noadv = loop_timed(g_noadv)
+        if pkv.status_word(lws) != 0:
+            raise SystemExit(f"device status {pkv.status_word(lws):#x} after the loop leg")
+        loop = {"steps_per_graph": LOOP, "replays": reps,
+                "us_per_step": round(1e3 * ms_adv, 2),
+                "us_per_step_without_advance": round(1e3 * ms_noadv, 2),
+                "advance_us": round(1e3 * (ms_adv - ms_noadv), 2),
+                "pages_taken_per_replay": pages_taken,
+                "note": "same rows; table strided with room to grow; steps back to back, "
+                        "no flush"}
+        del lkp, lvp, lkn, lvn, g_adv, g_noadv
+
     # roofline of the dominant kernel, the fused step kernel (its launch is
     # timed as the step call, so the small piece combine is included).
     # Algorithmic bytes per call: K and V of every token, q, the new token's
@@ -508,6 +594,7 @@ def run_pkv(args):
         "clocks": clocks,
         "wall_s_timed": round(wall, 3),
         "e2e": e2e,
+        "decode_loop": loop,
         "cpu_baseline": cpu,
     }
     print(json.dumps(line), flush=True)

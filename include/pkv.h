@@ -72,6 +72,8 @@ typedef enum {
 #define PKV_FLAG_BAD_LEN  0x2u  /* seq_lens[b] < 0 or > max_seq_len         */
 #define PKV_FLAG_BAD_POS  0x4u  /* new-token position >= RoPE table rows    */
 #define PKV_FLAG_TIMEOUT  0x8u  /* an internal copy wait gave up (~2 s)     */
+#define PKV_FLAG_NO_PAGE  0x10u /* paged_kv_advance: free list empty, or the
+                                   row's page-table capacity is full        */
 
 typedef struct {
     int B;            /* query rows in the batch                           */
@@ -209,6 +211,44 @@ pkv_status paged_decode_partials(const pkv_dims *dims, const void *q,
 pkv_status decode_combine(const pkv_dims *dims, const float *o_part,
                           const float *ml_part, int num_splits, void *out,
                           pkv_stream_t stream);
+
+/* ---- the decode loop on the device --------------------------------------- */
+
+/* Advance the decode metadata by one token per live row, on the device, so
+ * that a loop of decode steps can be one CUDA graph with no host work
+ * between steps.  It does what the pages' host code does at each steady-state
+ * step (compare v1.3.12..6f09b1d, astrai/inference/core/cache.py:
+ * PagePool.task_extend / _extend_slot claim the new token's slot, taking a
+ * fresh page from the allocator when the position starts a page, and set the
+ * length to pos + 1; bind_tasks' steady-state branch adds one to every
+ * row's length in place; commits by author, "DecodeBindCache: bind_tasks
+ * increments seq_lens/kv_indptr").
+ *
+ * For each row b with L = seq_lens[b] > 0 (rows with 0 are idle and left
+ * alone), the new token's position is pos = L:
+ *   - pos >= max_seq_len: PKV_FLAG_BAD_LEN, row unchanged;
+ *   - pos % page_size == 0 (the token starts a page): the row takes the next
+ *     free page and kv_indices[kv_indptr[b] + pos / page_size] = that page.
+ *     Rows take pages in increasing b from free_pages[*free_head],
+ *     free_pages[*free_head + 1], ..., so the assignment is deterministic.
+ *     If the row's capacity (kv_indptr[b+1] - kv_indptr[b] entries) has no
+ *     entry pos / page_size, or the list has run out (index >= num_free), the
+ *     row is unchanged and PKV_FLAG_NO_PAGE is set;
+ *   - otherwise seq_lens[b] = pos + 1.
+ * *free_head advances by the pages taken.  The page table therefore needs
+ * room to grow: a strided layout (kv_indptr[b] = b * cap) does it.
+ * kv_indptr is only read.
+ *
+ * Then paged_decode_step (or paged_kv_append) writes the new token at
+ * seq_lens[b] - 1, as usual.  seq_lens, kv_indices and free_head are device
+ * int32 arrays the call reads and writes; free_pages (num_free entries, may
+ * be NULL when num_free == 0) is read; status (device, nullable) receives
+ * PKV_FLAG_* bits.  Page ids are not range-checked here; the decode checks
+ * every id it reads.  One launch of one block; graph-capturable. */
+pkv_status paged_kv_advance(const pkv_dims *dims, int32_t *seq_lens,
+                            const int32_t *kv_indptr, int32_t *kv_indices,
+                            const int32_t *free_pages, int num_free, int32_t *free_head,
+                            uint32_t *status, pkv_stream_t stream);
 
 /* ---- for callers that cannot allocate ------------------------------------ */
 

@@ -308,7 +308,7 @@ extern "C" {
 
 int pkv_version(void)
 {
-    return (1 << 16) | 1;
+    return (1 << 16) | 2;
 }
 
 const char *pkv_status_str(pkv_status s)
@@ -422,6 +422,39 @@ pkv_status paged_kv_append(const pkv_dims *dims, void *q, const void *k_new, con
         return st;
     return launch_append(dims, q, k_new, v_new, k_pool, v_pool, kv_indices, kv_indptr,
                          seq_lens, rope_cos_sin, rope_max_pos, rope_q, status, stream);
+}
+
+pkv_status paged_kv_advance(const pkv_dims *dims, int32_t *seq_lens, const int32_t *kv_indptr,
+                            int32_t *kv_indices, const int32_t *free_pages, int num_free,
+                            int32_t *free_head, uint32_t *status, pkv_stream_t stream)
+{
+    pkv_status st = check_dims(dims);
+    if (st != PKV_OK)
+        return st;
+    if (dims->B == 0)
+        return PKV_OK;
+    if (seq_lens == nullptr || kv_indptr == nullptr || free_head == nullptr || num_free < 0 ||
+        (num_free > 0 && free_pages == nullptr) ||
+        (dims->num_indices > 0 && kv_indices == nullptr))
+        return PKV_ERR_INVALID_ARG;
+    if (!aligned(seq_lens, 4) || !aligned(kv_indptr, 4) || !aligned(free_head, 4) ||
+        (kv_indices != nullptr && !aligned(kv_indices, 4)) ||
+        (free_pages != nullptr && !aligned(free_pages, 4)) ||
+        (status != nullptr && !aligned(status, 4)))
+        return PKV_ERR_INVALID_ARG;
+    pkv::AdvanceParams p{};
+    p.seq_lens = seq_lens;
+    p.kv_indptr = kv_indptr;
+    p.kv_indices = kv_indices;
+    p.free_pages = free_pages;
+    p.free_head = free_head;
+    p.status = status;
+    p.B = dims->B;
+    p.page_size = dims->page_size;
+    p.max_seq_len = dims->max_seq_len;
+    p.num_indices = dims->num_indices;
+    p.num_free = num_free;
+    return launch_status(pkv::launch_advance(p, (cudaStream_t)stream));
 }
 
 pkv_status paged_decode_attn(const pkv_dims *dims, const void *q, const void *k_pool,

@@ -15,6 +15,7 @@ constexpr unsigned kFlagBadPage = 0x1u;
 constexpr unsigned kFlagBadLen = 0x2u;
 constexpr unsigned kFlagBadPos = 0x4u;
 constexpr unsigned kFlagTimeout = 0x8u;
+constexpr unsigned kFlagNoPage = 0x10u;
 
 // ~2 s: far beyond any legitimate copy latency.
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;

@@ -40,6 +40,17 @@ struct DecodeParams {
     float scale_log2;      // scale * log2(e)
 };
 
+// Device-side metadata advance (pkv_advance.cu).
+struct AdvanceParams {
+    int32_t *seq_lens;
+    const int32_t *kv_indptr;
+    int32_t *kv_indices;
+    const int32_t *free_pages;
+    int32_t *free_head;
+    uint32_t *status;      // nullable
+    int B, page_size, max_seq_len, num_indices, num_free;
+};
+
 // Persistent token-balanced decode (pkv_fused.cu).
 constexpr int kFusedMaxRows = 4096;     // virtual rows whose prefix sums fit in smem
 constexpr int kFusedMinTokens = 64;     // fewest tokens a block is given
@@ -95,6 +106,7 @@ struct CombineParams {
 };
 
 cudaError_t launch_append(const AppendParams &p, cudaStream_t stream);
+cudaError_t launch_advance(const AdvanceParams &p, cudaStream_t stream);
 cudaError_t launch_rope_table(float *cos_sin, int max_pos, int D, double base,
                               cudaStream_t stream);
 cudaError_t launch_split_decode(const DecodeParams &p, int D, cudaStream_t stream);

@@ -29,13 +29,14 @@ FLAG_BAD_PAGE = 0x1
 FLAG_BAD_LEN = 0x2
 FLAG_BAD_POS = 0x4
 FLAG_TIMEOUT = 0x8
+FLAG_NO_PAGE = 0x10
 
 # Every symbol include/pkv.h declares.
 EXPORTS = (
     "pkv_split_chunk", "pkv_workspace_bytes", "pkv_workspace_layout", "pkv_plan",
     "pkv_workspace_init", "pkv_rope_table", "paged_kv_append", "paged_decode_attn",
     "paged_decode_step", "paged_decode_partials", "decode_combine", "pkv_status_str",
-    "pkv_version", "paged_decode_attn_noalloc",
+    "pkv_version", "paged_decode_attn_noalloc", "paged_kv_advance",
 )
 
 
@@ -87,6 +88,7 @@ def lib():
             "paged_decode_partials": (I, [DP, P, P, P, P, P, P, I, P, Z, P]),
             "decode_combine": (I, [DP, P, P, I, P, P]),
             "paged_decode_attn_noalloc": (I, [DP, P, P, P, P, P, P, I, P, P, P]),
+            "paged_kv_advance": (I, [DP, P, P, P, P, I, P, P, P]),
             "pkv_status_str": (ctypes.c_char_p, [I]),
             "pkv_version": (I, []),
         }
@@ -198,6 +200,17 @@ def paged_decode_step(d: Dims, q, k_new, v_new, k_pool, v_pool, kv_indices, kv_i
         ctypes.byref(d), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_pool), _ptr(v_pool),
         _ptr(kv_indices), _ptr(kv_indptr), _ptr(seq_lens), _ptr(rope_cos_sin), rope_max_pos,
         num_splits, _ptr(workspace), ws_bytes, _ptr(out), _stream(stream)))
+
+
+def paged_kv_advance(d: Dims, seq_lens, kv_indptr, kv_indices, free_pages, free_head,
+                     status=None, stream=None) -> None:
+    """One more token for every row with seq_lens > 0, and a page from
+    free_pages (starting at free_head[0]) for each row whose new token starts
+    a page; seq_lens, kv_indices and free_head are updated on the device."""
+    num_free = 0 if free_pages is None else int(free_pages.numel())
+    _check("paged_kv_advance", lib().paged_kv_advance(
+        ctypes.byref(d), _ptr(seq_lens), _ptr(kv_indptr), _ptr(kv_indices), _ptr(free_pages),
+        num_free, _ptr(free_head), _ptr(status), _stream(stream)))
 
 
 NOALLOC_SCRATCH_BYTES = 16 << 20

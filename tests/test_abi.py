@@ -158,3 +158,27 @@ def test_argument_checks_before_launch():
     d0 = _d(B=0)
     assert L.paged_decode_attn(byref(d0), None, None, None, None, None, None, 4, None, 0, None,
                                None) == pkv.PKV_OK
+
+
+def test_advance_argument_checks():
+    L = pkv.lib()
+    d = _d(B=4)
+    byref = pkv.ctypes.byref
+    fake = 1 << 32
+    ok_args = dict(seq_lens=fake, ptr=fake, ind=fake, free=fake, n_free=8, head=fake, st=None)
+
+    def call(**kw):
+        a = dict(ok_args, **kw)
+        return L.paged_kv_advance(byref(d), a["seq_lens"], a["ptr"], a["ind"], a["free"],
+                                  a["n_free"], a["head"], a["st"], None)
+
+    assert call(seq_lens=None) == pkv.PKV_ERR_INVALID_ARG
+    assert call(ptr=None) == pkv.PKV_ERR_INVALID_ARG
+    assert call(head=None) == pkv.PKV_ERR_INVALID_ARG
+    assert call(n_free=-1) == pkv.PKV_ERR_INVALID_ARG
+    assert call(free=None) == pkv.PKV_ERR_INVALID_ARG          # num_free > 0 needs a list
+    assert call(seq_lens=fake + 2) == pkv.PKV_ERR_INVALID_ARG  # misaligned
+    assert call(st=fake + 1) == pkv.PKV_ERR_INVALID_ARG
+    d0 = _d(B=0)
+    assert L.paged_kv_advance(byref(d0), None, None, None, None, 0, None, None,
+                              None) == pkv.PKV_OK
