@@ -56,6 +56,9 @@ def parse_args(argv=None):
     ap.add_argument("--impl", choices=["pkv", "reference"], default="pkv")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--layout", choices=["paged", "contig"], default="paged",
+                    help="contig: the same rows in a contiguous cache [B, max_seq_len, Hkv, D] "
+                         "through decode_attn_contig")
     ap.add_argument("--no-loop", action="store_true",
                     help="skip the decode-loop leg (paged_kv_advance + step per graph)")
     ap.add_argument("--no-flush", action="store_true", help="skip the L2 flush (not for reporting)")
@@ -282,7 +285,8 @@ def run_reference(args):
         "n_gpus": args.gpus, "steps": steps, "warmup": warm,
         "ms_per_step": round(1e3 * tot_s / steps, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D,
+        "config": {"workload": w.name + ("" if args.layout == "paged" else " (contiguous cache)"),
+                   "layout": args.layout, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D,
                    "page_size": w.page_size, "num_pages": w.num_pages},
         "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": res["cores"],
                          "kind": "oracle",
@@ -348,7 +352,37 @@ def run_pkv(args):
         pkv.paged_decode_attn(d, q, t["k_pool"], t["v_pool"], kv_indices, kv_indptr,
                               seq_lens, S, ws, out)
 
-    launches_per_step = 1 if S == 1 else 2
+    if args.layout == "contig":
+        # the same rows in a contiguous cache: slot b holds row b's tokens in
+        # order (gathered from its pages), NaN past them
+        cache_len = w.max_seq_len
+        ck = torch.full((w.B, cache_len, w.Hkv, w.D), float("nan"), dtype=torch.bfloat16,
+                        device=dev)
+        cv = torch.full_like(ck, float("nan"))
+        ptr_h = w.kv_indptr.tolist()
+        for b in range(w.B):
+            L = int(w.seq_lens[b])
+            if L == 0:
+                continue
+            pages = t["kv_indices"][ptr_h[b]:ptr_h[b + 1]].long()
+            ck[b, :L] = t["k_pool"][pages].reshape(-1, w.Hkv, w.D)[:L]
+            cv[b, :L] = t["v_pool"][pages].reshape(-1, w.Hkv, w.D)[:L]
+        del t["k_pool"], t["v_pool"]
+        torch.cuda.empty_cache()
+        d = pkv.dims(w.B, w.Hq, w.Hkv, w.D, cache_len, w.B, w.B, cache_len, w.scale)
+        ws = pkv.alloc_workspace(d, S, dev)
+
+        def step(q, k_new, v_new, kv_indices, kv_indptr, seq_lens):
+            pkv.decode_attn_contig(d, q, ck, cv, seq_lens, S, ws, out, k_new=k_new, v_new=v_new,
+                                   rope_cos_sin=rope, rope_max_pos=rope_rows)
+
+        def decode(q, kv_indices, kv_indptr, seq_lens):
+            pkv.decode_attn_contig(d, q, ck, cv, seq_lens, S, ws, out)
+
+        args.no_e2e = True
+        args.no_loop = True
+
+    launches_per_step = (1 if S == 1 else 2) + (1 if args.layout == "contig" else 0)
     dev_args = (t["q"], t["k_new"], t["v_new"], t["kv_indices"], t["kv_indptr"], t["seq_lens"])
 
     for _ in range(max(3, args.warmup)):
@@ -547,7 +581,7 @@ def run_pkv(args):
     dec_bytes = kv_bytes + w.B * w.Hq * w.D * 2 * 2 + 4 * n_idx + 8 * w.B
     peak, peak_kind = load_peaks()
     achieved = alg_bytes / (ms_step * 1e-3) / 1e9
-    traffic = cached_traffic(w.name, S)
+    traffic = cached_traffic(w.name, S) if args.layout == "paged" else None
     clocks = clk.summary(wall0, wall0 + wall)
 
     if rank != 0:

@@ -212,6 +212,30 @@ pkv_status decode_combine(const pkv_dims *dims, const float *o_part,
                           const float *ml_part, int num_splits, void *out,
                           pkv_stream_t stream);
 
+/* ---- contiguous K/V cache -------------------------------------------------- */
+
+/* Decode (or, with k_new/v_new, the whole decode step) over a contiguous
+ * K/V cache, the pages' ContigKV layout (compare v1.3.12..6f09b1d,
+ * attention_backend.py: "Read K/V directly from flat pool via
+ * cache_batch_idx + cache_seqlens"; commits by author, "add attn_kv_source.cuh
+ * with ContigKV/PagedKV addressing policies").
+ * k_cache, v_cache: [num_slots, cache_len, Hkv, D] bf16 with
+ * dims->num_pages = num_slots and dims->page_size = cache_len.  Row b reads
+ * slot cache_batch_idx[b] (NULL: slot b) over its seq_lens[b] tokens, so
+ * the cache is a paged pool with one page of cache_len tokens per row.
+ * dims->num_indices is ignored.  The call writes that one-entry table into
+ * the workspace (a region every workspace has) and runs paged_decode_attn,
+ * or paged_decode_step when k_new and v_new are given (then the new token
+ * is written at seq_lens[b] - 1 of its slot; rope_cos_sin / rope_max_pos as
+ * for that call).  Errors and results are those calls'; a slot id outside
+ * [0, num_slots) sets PKV_FLAG_BAD_PAGE. */
+pkv_status decode_attn_contig(const pkv_dims *dims, const void *q, const void *k_new,
+                              const void *v_new, void *k_cache, void *v_cache,
+                              const int32_t *cache_batch_idx, const int32_t *seq_lens,
+                              const float *rope_cos_sin, int rope_max_pos, int num_splits,
+                              void *workspace, size_t ws_bytes, void *out,
+                              pkv_stream_t stream);
+
 /* ---- the decode loop on the device --------------------------------------- */
 
 /* Advance the decode metadata by one token per live row, on the device, so

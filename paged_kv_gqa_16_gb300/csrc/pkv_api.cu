@@ -69,14 +69,15 @@ int log2_exact(int x)
 }
 
 // Workspace: [header 256 B | row info, persistent path: Bv x 2 int32 |
-//             rotated-q scratch [B, Hq, D] bf16 | partials].
+//             rotated-q scratch [B, Hq, D] bf16 | one-page-per-row table of
+//             the contiguous-cache call, (2B + 1) int32 | partials].
 // The partial region holds either layout: the per-split one [B,Hq,S,(2|D)]
 // of paged_decode_partials, or the piece one [(S+Bv)*HQV, (2|D)] of the
 // persistent path.  Every region starts on a 256-byte boundary.
 struct Layout {
     int hpc, Bv, HQV;
-    size_t rowinfo_off, qscratch_off, split_ml_off, split_o_off, piece_ml_off, piece_o_off,
-        total;
+    size_t rowinfo_off, qscratch_off, table_off, split_ml_off, split_o_off, piece_ml_off,
+        piece_o_off, total;
 };
 
 Layout layout_for(const pkv_dims *d, int num_splits)
@@ -87,7 +88,8 @@ Layout layout_for(const pkv_dims *d, int num_splits)
     L.HQV = L.hpc * (d->Hq / d->Hkv);
     L.rowinfo_off = kHeaderBytes;
     L.qscratch_off = L.rowinfo_off + round_up((size_t)L.Bv * 2 * sizeof(int32_t), 256);
-    const size_t part = L.qscratch_off + round_up((size_t)d->B * d->Hq * d->D * 2, 256);
+    L.table_off = L.qscratch_off + round_up((size_t)d->B * d->Hq * d->D * 2, 256);
+    const size_t part = L.table_off + round_up(((size_t)2 * d->B + 1) * sizeof(int32_t), 256);
     const size_t rows = (size_t)d->B * d->Hq * num_splits;
     L.split_ml_off = part;
     L.split_o_off = part + round_up(rows * 2 * sizeof(float), 256);
@@ -516,6 +518,47 @@ pkv_status paged_decode_step(const pkv_dims *dims, const void *q, const void *k_
     if (st != PKV_OK || direct)
         return st;
     return launch_combine_split(dims, num_splits, workspace, out, stream);
+}
+
+pkv_status decode_attn_contig(const pkv_dims *dims, const void *q, const void *k_new,
+                              const void *v_new, void *k_cache, void *v_cache,
+                              const int32_t *cache_batch_idx, const int32_t *seq_lens,
+                              const float *rope_cos_sin, int rope_max_pos, int num_splits,
+                              void *workspace, size_t ws_bytes, void *out, pkv_stream_t stream)
+{
+    if (dims == nullptr)
+        return PKV_ERR_INVALID_ARG;
+    pkv_dims d = *dims;
+    d.num_indices = d.B;                       // one table entry per row
+    pkv_status st = check_dims(&d);
+    if (st != PKV_OK)
+        return st;
+    if (d.B == 0)
+        return PKV_OK;
+    if ((k_new == nullptr) != (v_new == nullptr) || workspace == nullptr ||
+        !aligned(workspace, 256) ||
+        (cache_batch_idx != nullptr && !aligned(cache_batch_idx, 4)))
+        return PKV_ERR_INVALID_ARG;
+    if (num_splits < 1 || num_splits > kMaxSplits)
+        return PKV_ERR_INVALID_ARG;
+    const size_t need = pkv_workspace_bytes(&d, num_splits);
+    if (need == 0)
+        return PKV_ERR_INVALID_ARG;
+    if (ws_bytes < need)
+        return PKV_ERR_WORKSPACE_TOO_SMALL;
+    const Layout L = layout_for(&d, num_splits);
+    int32_t *kv_indptr = reinterpret_cast<int32_t *>(static_cast<char *>(workspace) + L.table_off);
+    int32_t *kv_indices = kv_indptr + d.B + 1;
+    st = launch_status(
+        pkv::launch_contig_table(cache_batch_idx, d.B, kv_indptr, (cudaStream_t)stream));
+    if (st != PKV_OK)
+        return st;
+    if (k_new != nullptr)
+        return paged_decode_step(&d, q, k_new, v_new, k_cache, v_cache, kv_indices, kv_indptr,
+                                 seq_lens, rope_cos_sin, rope_max_pos, num_splits, workspace,
+                                 ws_bytes, out, stream);
+    return paged_decode_attn(&d, q, k_cache, v_cache, kv_indices, kv_indptr, seq_lens,
+                             num_splits, workspace, ws_bytes, out, stream);
 }
 
 pkv_status paged_decode_partials(const pkv_dims *dims, const void *q, const void *k_pool,

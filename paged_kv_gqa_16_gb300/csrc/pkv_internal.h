@@ -107,6 +107,8 @@ struct CombineParams {
 
 cudaError_t launch_append(const AppendParams &p, cudaStream_t stream);
 cudaError_t launch_advance(const AdvanceParams &p, cudaStream_t stream);
+// table[0..B] = 0..B (kv_indptr), table[B+1+b] = idx ? idx[b] : b (kv_indices)
+cudaError_t launch_contig_table(const int32_t *idx, int B, int32_t *table, cudaStream_t stream);
 cudaError_t launch_rope_table(float *cos_sin, int max_pos, int D, double base,
                               cudaStream_t stream);
 cudaError_t launch_split_decode(const DecodeParams &p, int D, cudaStream_t stream);

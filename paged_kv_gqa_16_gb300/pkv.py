@@ -36,7 +36,7 @@ EXPORTS = (
     "pkv_split_chunk", "pkv_workspace_bytes", "pkv_workspace_layout", "pkv_plan",
     "pkv_workspace_init", "pkv_rope_table", "paged_kv_append", "paged_decode_attn",
     "paged_decode_step", "paged_decode_partials", "decode_combine", "pkv_status_str",
-    "pkv_version", "paged_decode_attn_noalloc", "paged_kv_advance",
+    "pkv_version", "paged_decode_attn_noalloc", "paged_kv_advance", "decode_attn_contig",
 )
 
 
@@ -89,6 +89,7 @@ def lib():
             "decode_combine": (I, [DP, P, P, I, P, P]),
             "paged_decode_attn_noalloc": (I, [DP, P, P, P, P, P, P, I, P, P, P]),
             "paged_kv_advance": (I, [DP, P, P, P, P, I, P, P, P]),
+            "decode_attn_contig": (I, [DP, P, P, P, P, P, P, P, P, I, I, P, Z, P, P]),
             "pkv_status_str": (ctypes.c_char_p, [I]),
             "pkv_version": (I, []),
         }
@@ -211,6 +212,19 @@ def paged_kv_advance(d: Dims, seq_lens, kv_indptr, kv_indices, free_pages, free_
     _check("paged_kv_advance", lib().paged_kv_advance(
         ctypes.byref(d), _ptr(seq_lens), _ptr(kv_indptr), _ptr(kv_indices), _ptr(free_pages),
         num_free, _ptr(free_head), _ptr(status), _stream(stream)))
+
+
+def decode_attn_contig(d: Dims, q, k_cache, v_cache, seq_lens, num_splits: int, workspace,
+                       out, cache_batch_idx=None, k_new=None, v_new=None, rope_cos_sin=None,
+                       rope_max_pos: int = 0, stream=None) -> None:
+    """Decode over a contiguous cache [num_slots, cache_len, Hkv, D] (d.page_size =
+    cache_len, d.num_pages = num_slots); row b reads slot cache_batch_idx[b]
+    (None: slot b).  With k_new / v_new it is the whole decode step."""
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check("decode_attn_contig", lib().decode_attn_contig(
+        ctypes.byref(d), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+        _ptr(cache_batch_idx), _ptr(seq_lens), _ptr(rope_cos_sin), rope_max_pos, num_splits,
+        _ptr(workspace), ws_bytes, _ptr(out), _stream(stream)))
 
 
 NOALLOC_SCRATCH_BYTES = 16 << 20

@@ -255,7 +255,19 @@ CASES = {
 }
 
 
+def ragged_b32_ps1(seed: int = 0, num_pages: int = 65536 * 16) -> Workload:
+    """The ragged B=32 rows in the token-granular layout: page_size 1, every
+    token's slot drawn at random from a pool of the same 1,048,576 token
+    slots (the reference's req_to_token table is this case)."""
+    gen = torch.Generator().manual_seed(seed)
+    lens = torch.randint(512, 4097, (32,), generator=gen).tolist()
+    return build("ragged_b32_ps1", B=32, Hq=32, Hkv=8, D=128, page_size=1,
+                 seq_lens=lens, num_pages=num_pages, max_seq_len=4096, seed=seed, gen=gen)
+
+
 def make(name: str, seed: int = 0, **kw) -> Workload:
+    if name == "ragged_b32_ps1":
+        return ragged_b32_ps1(seed=seed, **kw)
     if name.startswith("serving_b"):
         return serving(int(name[len("serving_b"):]), seed=seed)
     return CASES[name](seed=seed, **kw)
@@ -338,3 +350,56 @@ def decode_loop(*, B: int, Hq: int, Hkv: int, D: int, page_size: int, seq_lens, 
                      seq_lens=np.array(lens, dtype=np.int32), kv_indptr=indptr,
                      kv_indices=indices, free_pages=free, q=q, k_new=k_new, v_new=v_new,
                      k_pool=k_pool, v_pool=v_pool)
+
+
+# ------------------------------------------------------------ contiguous cache
+@dataclass
+class ContigCase:
+    """A contiguous K/V cache [num_slots, cache_len, Hkv, D]; row b reads slot
+    ``idx[b]`` over ``seq_lens[b]`` tokens (the new token's slot, position
+    seq_len - 1, and everything after it is NaN).  uint16 bf16 bits."""
+    B: int
+    Hq: int
+    Hkv: int
+    D: int
+    cache_len: int
+    num_slots: int
+    seq_lens: np.ndarray      # int32 [B]
+    idx: np.ndarray           # int32 [B]
+    q: np.ndarray             # [B, Hq, D]
+    k_new: np.ndarray         # [B, Hkv, D]
+    v_new: np.ndarray
+    k_cache: np.ndarray       # [num_slots, cache_len, Hkv, D]
+    v_cache: np.ndarray
+    rope_base: float = 10000.0
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.D)
+
+
+def contig(*, Hq: int, Hkv: int, D: int, cache_len: int, num_slots: int, seq_lens, idx,
+           seed: int = 0, fill_new_slot: bool = False) -> ContigCase:
+    gen = torch.Generator().manual_seed(seed)
+    lens = np.asarray(seq_lens, dtype=np.int32)
+    idx = np.asarray(idx, dtype=np.int32)
+    B = len(lens)
+
+    def bits(t: torch.Tensor) -> np.ndarray:
+        return t.contiguous().view(torch.int16).numpy().view(np.uint16).copy()
+
+    q = bits(_randn_bf16((B, Hq, D), gen))
+    k_new = bits(_randn_bf16((B, Hkv, D), gen))
+    v_new = bits(_randn_bf16((B, Hkv, D), gen))
+    k_cache = bits(_randn_bf16((num_slots, cache_len, Hkv, D), gen))
+    v_cache = bits(_randn_bf16((num_slots, cache_len, Hkv, D), gen))
+    longest = {}
+    for b in range(B):
+        longest[int(idx[b])] = max(longest.get(int(idx[b]), 0), int(lens[b]))
+    for s, L in longest.items():
+        start = L if fill_new_slot else max(L - 1, 0)
+        k_cache[s, start:] = NAN_BF16_BITS
+        v_cache[s, start:] = NAN_BF16_BITS
+    return ContigCase(B=B, Hq=Hq, Hkv=Hkv, D=D, cache_len=cache_len, num_slots=num_slots,
+                      seq_lens=lens, idx=idx, q=q, k_new=k_new, v_new=v_new, k_cache=k_cache,
+                      v_cache=v_cache)
