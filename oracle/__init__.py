@@ -80,6 +80,7 @@ def _load():
         lib.po_combine.restype = I
         lib.po_combine.argtypes = [I, I, I, I, P, P, P]
         lib.po_advance.argtypes = [I, I, I, I, P, P, P, P, I, P, P, P, P]
+        lib.po_prefill.argtypes = [I, I, I, I, I, I, I, P, P, P, P, P, P, P, D, P]
         lib.po_set_threads.argtypes = [I]
         lib.po_max_threads.restype = I
         _lib = lib
@@ -191,6 +192,27 @@ def decode(q, k_pool, v_pool, kv_indices, kv_indptr, seq_lens, scale: float):
                            _ptr(kv_indices), _ptr(kv_indptr), _ptr(seq_lens),
                            float(scale), _ptr(out))
     _check(rc, "decode")
+    return out
+
+
+def prefill(q, qo_indptr, k_pool, v_pool, kv_indices, kv_indptr, seq_lens, scale: float):
+    """out [total_q,Hq,D] float64: query i of row b (the last q_len of its
+    seq_lens[b] tokens) attends causally up to its own position."""
+    q = _c(q, np.uint16)
+    qo_indptr = _c(qo_indptr, np.int32)
+    k_pool = _c(k_pool, np.uint16)
+    v_pool = _c(v_pool, np.uint16)
+    kv_indices = _c(kv_indices, np.int32)
+    kv_indptr = _c(kv_indptr, np.int32)
+    seq_lens = _c(seq_lens, np.int32)
+    total_q, Hq, D = q.shape
+    B = len(seq_lens)
+    P, ps, Hkv, _ = k_pool.shape
+    out = np.empty((total_q, Hq, D), dtype=np.float64)
+    rc = _load().po_prefill(B, Hq, Hkv, D, ps, P, total_q, _ptr(q), _ptr(qo_indptr),
+                            _ptr(k_pool), _ptr(v_pool), _ptr(kv_indices), _ptr(kv_indptr),
+                            _ptr(seq_lens), float(scale), _ptr(out))
+    _check(rc, "prefill")
     return out
 
 

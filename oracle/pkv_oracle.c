@@ -31,6 +31,9 @@
  *   - commits by author, split-KV decode ("split partials", "single combine
  *       kernel", "compute_num_splits"): per-split partial outputs and
  *       (max, sum) statistics merged by a combine pass.
+ *   - same diff, attention_ops.py, attn_paged_prefill / attn_prefill: a
+ *       ragged chunk of queries per request, the last of its tokens, each
+ *       attending causally up to its own position (po_prefill).
  *   - same diff, cache.py, PagePool.task_extend / _extend_slot and the
  *       steady-state branch of bind_tasks: one more token per task, and a
  *       page from the allocator when the token starts a page (po_advance).
@@ -328,6 +331,67 @@ int po_decode(int B, int Hq, int Hkv, int D, int page_size, int num_pages,
         free(qv);
         free(s);
     }
+    return err ? PO_ERR : PO_OK;
+}
+
+/* Prefill / extend over the paged pool (compare v1.3.12..6f09b1d,
+ * astrai/extension/attention_ops.py, docstring of attn_paged_prefill: a
+ * ragged batch, q [total_q, n_heads, head_dim] flattened across requests,
+ * qo_indptr the prefix sum of the requests' query lengths, causal; and
+ * attn_prefill, whose causal offset is kv_len - q_len).  Row b's
+ * q_len = qo_indptr[b+1] - qo_indptr[b] queries are the last q_len of its
+ * L = seq_lens[b] tokens, so query i sits at position L - q_len + i and
+ * attends keys 0 .. that position.  out [total_q, Hq, D] doubles.  A row
+ * with q_len > L, or a qo_indptr that is not a non-decreasing walk from 0
+ * to total_q, is an error. */
+int po_prefill(int B, int Hq, int Hkv, int D, int page_size, int num_pages, int total_q,
+               const uint16_t *q, const int32_t *qo_indptr, const uint16_t *k_pool,
+               const uint16_t *v_pool, const int32_t *kv_indices, const int32_t *kv_indptr,
+               const int32_t *seq_lens, double scale, double *out)
+{
+    if (Hkv <= 0 || Hq % Hkv != 0 || qo_indptr[0] != 0 || qo_indptr[B] != total_q)
+        return PO_ERR;
+    int *row_of = malloc(sizeof(int) * (size_t)(total_q > 0 ? total_q : 1));
+    for (int b = 0; b < B; ++b) {
+        const int q_len = qo_indptr[b + 1] - qo_indptr[b];
+        if (q_len < 0 || q_len > seq_lens[b]) {
+            free(row_of);
+            return PO_ERR;
+        }
+        for (int i = qo_indptr[b]; i < qo_indptr[b + 1]; ++i)
+            row_of[i] = b;
+    }
+    const int n_rep = Hq / Hkv;
+    const long Lmax = max_len(B, seq_lens);
+    int err = 0;
+#pragma omp parallel
+    {
+        double *qv = malloc(sizeof(double) * (size_t)D);
+        double *s = malloc(sizeof(double) * (size_t)(Lmax > 0 ? Lmax : 1));
+#pragma omp for collapse(2) schedule(dynamic)
+        for (int i = 0; i < total_q; ++i) {
+            for (int h = 0; h < Hq; ++h) {
+                const int b = row_of[i];
+                const long pos = (long)seq_lens[b] - (qo_indptr[b + 1] - qo_indptr[b]) +
+                                 (i - qo_indptr[b]);
+                int e = 0;
+                double m, l;
+                const uint16_t *qh = q + ((long)i * Hq + h) * D;
+                for (int d = 0; d < D; ++d)
+                    qv[d] = po_bf16_to_f64(qh[d]);
+                attend_range(qv, b, h / n_rep, 0, pos + 1, Hkv, D, page_size, num_pages,
+                             k_pool, v_pool, kv_indices, kv_indptr, scale, s,
+                             out + ((long)i * Hq + h) * D, &m, &l, &e);
+                if (e) {
+#pragma omp atomic write
+                    err = 1;
+                }
+            }
+        }
+        free(qv);
+        free(s);
+    }
+    free(row_of);
     return err ? PO_ERR : PO_OK;
 }
 

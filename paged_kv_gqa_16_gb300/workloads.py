@@ -403,3 +403,45 @@ def contig(*, Hq: int, Hkv: int, D: int, cache_len: int, num_slots: int, seq_len
     return ContigCase(B=B, Hq=Hq, Hkv=Hkv, D=D, cache_len=cache_len, num_slots=num_slots,
                       seq_lens=lens, idx=idx, q=q, k_new=k_new, v_new=v_new, k_cache=k_cache,
                       v_cache=v_cache)
+
+
+# ----------------------------------------------------------- prefill / extend
+@dataclass
+class PrefillCase:
+    """A ragged prefill/extend batch over a paged pool: row b's q_lens[b]
+    queries are the last q_lens[b] of its seq_lens[b] tokens (their K/V are
+    already in the pool).  ``w`` holds the pool, page table and lengths (every
+    one of a row's tokens valid); ``q`` [total_q, Hq, D] bf16, ``qo_indptr``
+    [B+1] int32 (prefix sum of q_lens)."""
+    w: Workload
+    q: torch.Tensor
+    qo_indptr: torch.Tensor
+
+    @property
+    def total_q(self) -> int:
+        return int(self.qo_indptr[-1])
+
+    def flops(self) -> int:
+        """2 D (q.k) + 2 D (p.v) per (query, head, attended key)."""
+        total = 0
+        ql = (self.qo_indptr[1:] - self.qo_indptr[:-1]).tolist()
+        for L, n in zip(self.w.seq_lens.tolist(), ql):
+            first = L - n + 1                     # keys seen by the first query
+            total += (first + L) * n // 2
+        return 4 * self.w.D * self.w.Hq * total
+
+
+def prefill(name: str, *, B: int, Hq: int, Hkv: int, D: int, page_size: int, seq_lens,
+            q_lens, seed: int = 0, num_pages: Optional[int] = None,
+            max_seq_len: Optional[int] = None) -> PrefillCase:
+    lens = [int(x) for x in seq_lens]
+    ql = [int(x) for x in q_lens]
+    assert len(ql) == B and all(0 <= n <= L for n, L in zip(ql, lens))
+    gen = torch.Generator().manual_seed(seed)
+    w = build(name, B=B, Hq=Hq, Hkv=Hkv, D=D, page_size=page_size, seq_lens=lens,
+              num_pages=num_pages, max_seq_len=max_seq_len, seed=seed, gen=gen,
+              fill_new_slot=True)
+    indptr = np.zeros(B + 1, dtype=np.int32)
+    indptr[1:] = np.cumsum(ql)
+    q = _randn_bf16((int(indptr[-1]), Hq, D), gen)
+    return PrefillCase(w=w, q=q, qo_indptr=torch.from_numpy(indptr))

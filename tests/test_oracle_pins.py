@@ -490,3 +490,82 @@ def test_advance_page_count_over_many_steps():
     got = ind[ind >= 0]
     assert len(got) == taken and len(set(got.tolist())) == taken
     assert set(got.tolist()) == set(free[:taken].tolist())
+
+
+# -------------------------------------------------------------- prefill ---
+def _prefill_args(c, full=True):
+    w = c.w
+    if full:
+        kp, vp = w.full_pool_host()
+        idx = w.host("kv_indices")
+    else:
+        kp, vp, idx = w.compact_host()
+    q = c.q.contiguous().view(torch.int16).numpy().view(np.uint16)
+    return q, c.qo_indptr.numpy(), kp, vp, idx, w.host("kv_indptr"), w.host("seq_lens")
+
+
+def _torch_prefill(q_bits, qo_indptr, kp_bits, vp_bits, kv_indices, kv_indptr, seq_lens, scale):
+    """Independent route: torch gathers each row's pages; fp64 SDPA with an
+    explicit boolean mask, query i of a chunk of n keeping keys <= L - n + i."""
+    to64 = lambda a: torch.from_numpy(a.astype(np.int16)).view(torch.bfloat16).to(torch.float64)
+    q, kp, vp = to64(q_bits), to64(kp_bits), to64(vp_bits)
+    total_q, Hq, D = q.shape
+    P, ps, Hkv, _ = kp.shape
+    out = torch.zeros(total_q, Hq, D, dtype=torch.float64)
+    for b in range(len(seq_lens)):
+        L = int(seq_lens[b])
+        a, e = int(qo_indptr[b]), int(qo_indptr[b + 1])
+        n = e - a
+        if n == 0:
+            continue
+        pages = torch.from_numpy(kv_indices[kv_indptr[b]:kv_indptr[b + 1]].astype(np.int64))
+        K = kp[pages].reshape(-1, Hkv, D)[:L].permute(1, 0, 2)[None]
+        V = vp[pages].reshape(-1, Hkv, D)[:L].permute(1, 0, 2)[None]
+        keep = torch.arange(L)[None, :] <= (L - n + torch.arange(n))[:, None]
+        o = F.scaled_dot_product_attention(q[a:e].permute(1, 0, 2)[None], K, V,
+                                           attn_mask=keep, scale=scale, enable_gqa=True)
+        out[a:e] = o[0].permute(1, 0, 2)
+    return out.numpy()
+
+
+@pytest.mark.parametrize("Hq,Hkv,ps", [(8, 2, 16), (4, 4, 1), (16, 2, 5), (8, 1, 32)])
+def test_prefill_matches_torch_sdpa(Hq, Hkv, ps):
+    lens = [40, 1, 70, 33, 0, 17]
+    qls = [40, 1, 9, 33, 0, 1]          # full prefills, extends, single tokens, an idle row
+    c = wl.prefill("pf", B=len(lens), Hq=Hq, Hkv=Hkv, D=64, page_size=ps, seq_lens=lens,
+                   q_lens=qls, seed=Hq + ps)
+    args = _prefill_args(c)
+    got = oracle.prefill(*args, scale=c.w.scale)
+    want = _torch_prefill(*args, scale=c.w.scale)
+    assert np.all(np.isfinite(got))
+    np.testing.assert_allclose(got, want, rtol=0, atol=1e-12)
+
+
+def test_prefill_special_cases():
+    lens, qls = [12, 20, 9], [12, 1, 4]
+    c = wl.prefill("pfs", B=3, Hq=4, Hkv=2, D=64, page_size=4, seq_lens=lens, q_lens=qls,
+                   seed=9)
+    args = _prefill_args(c)
+    got = oracle.prefill(*args, scale=c.w.scale)
+    q, qo, kp, vp, idx, ptr, sl = args
+    # a full prefill's first query sees only key 0: its output is V_0 exactly
+    for h in range(4):
+        v0 = oracle.bf16_to_f64(vp[idx[ptr[0]], 0, h // 2])
+        assert np.array_equal(got[0, h], v0)
+    # a one-query chunk is the decode of that row
+    dec = oracle.decode(q[12:13].reshape(1, 4, 64), kp, vp, idx[ptr[1]:ptr[2]],
+                        np.array([0, ptr[2] - ptr[1]], np.int32), np.array([20], np.int32),
+                        c.w.scale)
+    np.testing.assert_allclose(got[12], dec[0], rtol=0, atol=1e-13)
+    # causality: changing the K/V of row 2's last token moves only its last query
+    kp2, vp2 = kp.copy(), vp.copy()
+    page, slot = idx[ptr[2] + 8 // 4], 8 % 4
+    kp2[page, slot] ^= 0x0040
+    vp2[page, slot] ^= 0x0040
+    got2 = oracle.prefill(q, qo, kp2, vp2, idx, ptr, sl, scale=c.w.scale)
+    assert np.array_equal(got2[:16], got[:16])
+    assert not np.array_equal(got2[16], got[16])
+    # a chunk longer than its row is refused
+    with pytest.raises(ValueError):
+        oracle.prefill(q, np.array([0, 13, 14, 18], np.int32), kp, vp, idx, ptr, sl,
+                       scale=c.w.scale)
