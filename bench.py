@@ -59,6 +59,8 @@ def parse_args(argv=None):
     ap.add_argument("--layout", choices=["paged", "contig"], default="paged",
                     help="contig: the same rows in a contiguous cache [B, max_seq_len, Hkv, D] "
                          "through decode_attn_contig")
+    ap.add_argument("--no-prefill", action="store_true",
+                    help="skip the prefill leg (paged_prefill_attn on three shapes)")
     ap.add_argument("--no-loop", action="store_true",
                     help="skip the decode-loop leg (paged_kv_advance + step per graph)")
     ap.add_argument("--no-flush", action="store_true", help="skip the L2 flush (not for reporting)")
@@ -115,6 +117,15 @@ def load_peaks():
         return float(j["hbm_gbs"]), "measured"
     except Exception:
         return FALLBACK_HBM_GBS, "fallback"
+
+
+def load_bf16_peak() -> float:
+    """Measured dense bf16 TFLOP/s (burst), else the fallback 1900."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"])
+    except Exception:
+        return 1900.0
 
 
 def cached_traffic(workload: str, splits: int):
@@ -569,6 +580,62 @@ def run_pkv(args):
                         "no flush"}
         del lkp, lvp, lkn, lvn, g_adv, g_noadv
 
+    # prefill / extend: paged_prefill_attn on three shapes, one call per
+    # replay, L2 flushed before each; tensor roofline against the measured
+    # dense bf16 peak (burst: each call runs alone)
+    prefill = None
+    if not args.no_prefill and args.layout == "paged":
+        shapes = {
+            "prefill B=32 x 512 (Hq 32, Hkv 8, D 64)":
+                dict(B=32, Hq=32, Hkv=8, D=64, page_size=16, seq_lens=[512] * 32,
+                     q_lens=[512] * 32),
+            "prefill B=4 x 4096 (Hq 32, Hkv 8, D 128)":
+                dict(B=4, Hq=32, Hkv=8, D=128, page_size=16, seq_lens=[4096] * 4,
+                     q_lens=[4096] * 4),
+            "extend B=16, 256 new of 2048 (Hq 32, Hkv 8, D 128)":
+                dict(B=16, Hq=32, Hkv=8, D=128, page_size=16, seq_lens=[2048] * 16,
+                     q_lens=[256] * 16),
+        }
+        tf_peak = load_bf16_peak()
+        prefill = []
+        for label, kw in shapes.items():
+            c = wl.prefill("prefill", seed=rank, **kw)
+            pt = c.w.to_device(dev)
+            pd = pkv.dims(c.w.B, c.w.Hq, c.w.Hkv, c.w.D, c.w.page_size, pt["k_pool"].shape[0],
+                          int(c.w.kv_indices.numel()), c.w.max_seq_len, c.w.scale)
+            pq, pqo = c.q.to(dev), c.qo_indptr.to(dev)
+            pout = torch.empty(c.total_q, c.w.Hq, c.w.D, dtype=torch.bfloat16, device=dev)
+            pst = torch.zeros(1, dtype=torch.int32, device=dev)
+
+            def prun():
+                pkv.paged_prefill_attn(pd, pq, pqo, pt["k_pool"], pt["v_pool"], pt["kv_indices"],
+                                       pt["kv_indptr"], pt["seq_lens"], pout, status=pst)
+
+            for _ in range(3):
+                prun()
+            pg = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(pg):
+                prun()
+            ms = []
+            for _ in range(23):
+                flush_l2()
+                a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                pg.replay()
+                e.record(stream)
+                torch.cuda.synchronize(dev)
+                ms.append(a.elapsed_time(e))
+            if int(pst.item()) != 0:
+                raise SystemExit(f"prefill status {int(pst.item()):#x}")
+            us = 1e3 * statistics.median(ms[3:])
+            tf = c.flops() / (us * 1e-6) / 1e12
+            prefill.append({"shape": label, "us": round(us, 1), "tflops": round(tf, 1),
+                            "roofline": {"bound": "tensor", "achieved": round(tf, 1),
+                                         "peak": tf_peak, "unit": "TFLOP/s",
+                                         "frac": round(tf / tf_peak, 4)},
+                            "flops": c.flops()})
+            del pt, pg
+
     # roofline of the dominant kernel, the fused step kernel (its launch is
     # timed as the step call, so the small piece combine is included).
     # Algorithmic bytes per call: K and V of every token, q, the new token's
@@ -629,6 +696,7 @@ def run_pkv(args):
         "wall_s_timed": round(wall, 3),
         "e2e": e2e,
         "decode_loop": loop,
+        "prefill": prefill,
         "cpu_baseline": cpu,
     }
     print(json.dumps(line), flush=True)

@@ -212,6 +212,29 @@ pkv_status decode_combine(const pkv_dims *dims, const float *o_part,
                           const float *ml_part, int num_splits, void *out,
                           pkv_stream_t stream);
 
+/* ---- prefill / extend ----------------------------------------------------- */
+
+/* Paged ragged prefill / extend attention (compare v1.3.12..6f09b1d,
+ * astrai/extension/attention_ops.py, attn_paged_prefill: "SGLang-style paged
+ * prefill (ragged batch ...)"; attn_prefill's causal offset kv_len - q_len).
+ * q [total_q, Hq, D] bf16 holds every row's query chunk back to back;
+ * qo_indptr [B+1] int32 is the prefix sum of the chunk lengths (0 ..
+ * total_q).  Row b's chunk is the last q_len = qo_indptr[b+1] - qo_indptr[b]
+ * of its L = seq_lens[b] tokens, whose K/V must already be in the pools
+ * (same page table as the decode calls), so query i sits at position
+ * L - q_len + i and attends keys 0 .. that position:
+ *   out[qo_indptr[b] + i, h] = softmax(scale q K^T) V over those keys, kv
+ *   head h / (Hq/Hkv), fp32 softmax, bf16 output [total_q, Hq, D].
+ * A row with q_len < 0 or > L, or L > max_seq_len, sets PKV_FLAG_BAD_LEN
+ * and its outputs are left unwritten; bad page ids set PKV_FLAG_BAD_PAGE
+ * (page 0 is read instead).  B <= 4096 (else PKV_ERR_UNSUPPORTED).  status
+ * (device, nullable) receives the flags.  No workspace; graph-capturable. */
+pkv_status paged_prefill_attn(const pkv_dims *dims, const void *q, const int32_t *qo_indptr,
+                              int total_q, const void *k_pool, const void *v_pool,
+                              const int32_t *kv_indices, const int32_t *kv_indptr,
+                              const int32_t *seq_lens, void *out, uint32_t *status,
+                              pkv_stream_t stream);
+
 /* ---- contiguous K/V cache -------------------------------------------------- */
 
 /* Decode (or, with k_new/v_new, the whole decode step) over a contiguous

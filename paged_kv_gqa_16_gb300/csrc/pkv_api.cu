@@ -561,6 +561,55 @@ pkv_status decode_attn_contig(const pkv_dims *dims, const void *q, const void *k
                              num_splits, workspace, ws_bytes, out, stream);
 }
 
+pkv_status paged_prefill_attn(const pkv_dims *dims, const void *q, const int32_t *qo_indptr,
+                              int total_q, const void *k_pool, const void *v_pool,
+                              const int32_t *kv_indices, const int32_t *kv_indptr,
+                              const int32_t *seq_lens, void *out, uint32_t *status,
+                              pkv_stream_t stream)
+{
+    pkv_status st = check_dims(dims);
+    if (st != PKV_OK)
+        return st;
+    if (total_q < 0)
+        return PKV_ERR_INVALID_ARG;
+    if (dims->B == 0 || total_q == 0)
+        return PKV_OK;
+    if (dims->B > pkv::kPrefillMaxRows)
+        return PKV_ERR_UNSUPPORTED;
+    if (q == nullptr || qo_indptr == nullptr || k_pool == nullptr || v_pool == nullptr ||
+        kv_indptr == nullptr || seq_lens == nullptr || out == nullptr ||
+        (dims->num_indices > 0 && kv_indices == nullptr))
+        return PKV_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(out, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16) ||
+        !aligned(qo_indptr, 4) || !aligned(kv_indptr, 4) || !aligned(seq_lens, 4) ||
+        (kv_indices != nullptr && !aligned(kv_indices, 4)) ||
+        (status != nullptr && !aligned(status, 4)))
+        return PKV_ERR_INVALID_ARG;
+    pkv::PrefillParams p{};
+    p.q = static_cast<const __nv_bfloat16 *>(q);
+    p.qo_indptr = qo_indptr;
+    p.k_pool = static_cast<const __nv_bfloat16 *>(k_pool);
+    p.v_pool = static_cast<const __nv_bfloat16 *>(v_pool);
+    p.kv_indices = kv_indices;
+    p.kv_indptr = kv_indptr;
+    p.seq_lens = seq_lens;
+    p.out = static_cast<__nv_bfloat16 *>(out);
+    p.status = status;
+    p.B = dims->B;
+    p.Hq = dims->Hq;
+    p.Hkv = dims->Hkv;
+    p.n_rep = dims->Hq / dims->Hkv;
+    p.page_size = dims->page_size;
+    p.ps_shift = log2_exact(dims->page_size);
+    p.num_pages = dims->num_pages;
+    p.num_indices = dims->num_indices;
+    p.max_seq_len = dims->max_seq_len;
+    p.total_q = total_q;
+    p.tq = 64 / p.n_rep;
+    p.scale_log2 = (float)((double)dims->scale * 1.4426950408889634);
+    return launch_status(pkv::launch_prefill(p, dims->D, (cudaStream_t)stream));
+}
+
 pkv_status paged_decode_partials(const pkv_dims *dims, const void *q, const void *k_pool,
                                  const void *v_pool, const int32_t *kv_indices,
                                  const int32_t *kv_indptr, const int32_t *seq_lens,

@@ -51,6 +51,24 @@ struct AdvanceParams {
     int B, page_size, max_seq_len, num_indices, num_free;
 };
 
+// Paged ragged prefill / extend (pkv_prefill.cu).
+constexpr int kPrefillMaxRows = 4096;   // rows whose query-tile counts fit in smem
+
+struct PrefillParams {
+    const __nv_bfloat16 *q;        // [total_q, Hq, D]
+    const int32_t *qo_indptr;      // [B+1]
+    const __nv_bfloat16 *k_pool;
+    const __nv_bfloat16 *v_pool;
+    const int32_t *kv_indices;
+    const int32_t *kv_indptr;
+    const int32_t *seq_lens;
+    __nv_bfloat16 *out;            // [total_q, Hq, D]
+    uint32_t *status;              // nullable
+    int B, Hq, Hkv, n_rep, page_size, ps_shift, num_pages, num_indices, max_seq_len, total_q;
+    int tq;                        // query tokens per block: 64 / n_rep
+    float scale_log2;
+};
+
 // Persistent token-balanced decode (pkv_fused.cu).
 constexpr int kFusedMaxRows = 4096;     // virtual rows whose prefix sums fit in smem
 constexpr int kFusedMinTokens = 64;     // fewest tokens a block is given
@@ -107,6 +125,7 @@ struct CombineParams {
 
 cudaError_t launch_append(const AppendParams &p, cudaStream_t stream);
 cudaError_t launch_advance(const AdvanceParams &p, cudaStream_t stream);
+cudaError_t launch_prefill(const PrefillParams &p, int D, cudaStream_t stream);
 // table[0..B] = 0..B (kv_indptr), table[B+1+b] = idx ? idx[b] : b (kv_indices)
 cudaError_t launch_contig_table(const int32_t *idx, int B, int32_t *table, cudaStream_t stream);
 cudaError_t launch_rope_table(float *cos_sin, int max_pos, int D, double base,

@@ -37,6 +37,7 @@ EXPORTS = (
     "pkv_workspace_init", "pkv_rope_table", "paged_kv_append", "paged_decode_attn",
     "paged_decode_step", "paged_decode_partials", "decode_combine", "pkv_status_str",
     "pkv_version", "paged_decode_attn_noalloc", "paged_kv_advance", "decode_attn_contig",
+    "paged_prefill_attn",
 )
 
 
@@ -90,6 +91,7 @@ def lib():
             "paged_decode_attn_noalloc": (I, [DP, P, P, P, P, P, P, I, P, P, P]),
             "paged_kv_advance": (I, [DP, P, P, P, P, I, P, P, P]),
             "decode_attn_contig": (I, [DP, P, P, P, P, P, P, P, P, I, I, P, Z, P, P]),
+            "paged_prefill_attn": (I, [DP, P, P, I, P, P, P, P, P, P, P, P]),
             "pkv_status_str": (ctypes.c_char_p, [I]),
             "pkv_version": (I, []),
         }
@@ -225,6 +227,16 @@ def decode_attn_contig(d: Dims, q, k_cache, v_cache, seq_lens, num_splits: int, 
         ctypes.byref(d), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
         _ptr(cache_batch_idx), _ptr(seq_lens), _ptr(rope_cos_sin), rope_max_pos, num_splits,
         _ptr(workspace), ws_bytes, _ptr(out), _stream(stream)))
+
+
+def paged_prefill_attn(d: Dims, q, qo_indptr, k_pool, v_pool, kv_indices, kv_indptr, seq_lens,
+                       out, status=None, stream=None) -> None:
+    """Ragged prefill / extend: q [total_q, Hq, D], row b's chunk the last
+    q_len of its seq_lens[b] tokens, each query attending causally."""
+    _check("paged_prefill_attn", lib().paged_prefill_attn(
+        ctypes.byref(d), _ptr(q), _ptr(qo_indptr), int(q.shape[0]), _ptr(k_pool), _ptr(v_pool),
+        _ptr(kv_indices), _ptr(kv_indptr), _ptr(seq_lens), _ptr(out), _ptr(status),
+        _stream(stream)))
 
 
 NOALLOC_SCRATCH_BYTES = 16 << 20

@@ -1,0 +1,107 @@
+"""paged_prefill_attn on the GPU against the fp64 oracle's prefill: ragged
+query chunks (full prefills, extends, single tokens, idle rows), GQA ratios
+1..16, page sizes 1..32, head dims 64 and 128, several query and key tiles per
+row.  The pools hold NaN in every unreferenced page and past every row's
+tokens.  Tolerance: max-abs 2e-2, mean-abs 2e-3."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_cases import compare_out
+from paged_kv_gqa_16_gb300 import pkv
+from paged_kv_gqa_16_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+
+def _bits(t):
+    return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def _run(c, status=None):
+    w = c.w
+    t = w.to_device("cuda")
+    P = t["k_pool"].shape[0]
+    d = pkv.dims(w.B, w.Hq, w.Hkv, w.D, w.page_size, P, int(w.kv_indices.numel()),
+                 w.max_seq_len, w.scale)
+    out = torch.full((c.total_q, w.Hq, w.D), float("nan"), dtype=torch.bfloat16, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda") if status is None else status
+    pkv.paged_prefill_attn(d, c.q.cuda(), c.qo_indptr.cuda(), t["k_pool"], t["v_pool"],
+                           t["kv_indices"], t["kv_indptr"], t["seq_lens"], out, status=st)
+    torch.cuda.synchronize()
+    return out, int(st.item()) & 0xFFFFFFFF, (d, t)
+
+
+def _want(c):
+    w = c.w
+    kp, vp, idx = w.compact_host()
+    return oracle.prefill(_bits(c.q), c.qo_indptr.numpy(), kp, vp, idx, w.host("kv_indptr"),
+                          w.host("seq_lens"), w.scale)
+
+
+@pytest.mark.parametrize("Hq,Hkv,D", [(8, 8, 64), (16, 8, 128), (32, 8, 128), (64, 8, 128),
+                                      (12, 4, 64), (48, 8, 64), (16, 1, 64), (48, 3, 128)])
+def test_prefill_shapes(Hq, Hkv, D):
+    lens = [40, 1, 300, 133, 0, 17, 64, 65]
+    qls = [40, 1, 70, 133, 0, 1, 64, 2]
+    c = wl.prefill("pfg", B=len(lens), Hq=Hq, Hkv=Hkv, D=D, page_size=16, seq_lens=lens,
+                   q_lens=qls, seed=Hq * 7 + Hkv + D)
+    out, st, _ = _run(c)
+    assert st == 0
+    compare_out(out, _want(c))
+
+
+@pytest.mark.parametrize("ps", [1, 5, 32])
+def test_prefill_page_sizes(ps):
+    lens = [100, 7, 250]
+    qls = [37, 7, 129]
+    c = wl.prefill("pfp", B=3, Hq=16, Hkv=4, D=64, page_size=ps, seq_lens=lens, q_lens=qls,
+                   seed=ps)
+    out, st, _ = _run(c)
+    assert st == 0
+    compare_out(out, _want(c))
+
+
+def test_prefill_many_tiles():
+    """Chunks of several query tiles against several key tiles each."""
+    lens = [1000, 700, 513, 129]
+    qls = [700, 700, 200, 129]
+    c = wl.prefill("pfm", B=4, Hq=16, Hkv=4, D=64, page_size=16, seq_lens=lens, q_lens=qls,
+                   seed=21)
+    out, st, _ = _run(c)
+    assert st == 0
+    compare_out(out, _want(c))
+
+
+def test_prefill_graph_replay_bitwise():
+    lens, qls = [300, 90, 33], [120, 90, 1]
+    c = wl.prefill("pfr", B=3, Hq=32, Hkv=8, D=128, page_size=16, seq_lens=lens, q_lens=qls,
+                   seed=5)
+    eager, _, (d, t) = _run(c)
+    q, qo = c.q.cuda(), c.qo_indptr.cuda()
+    out = torch.empty_like(eager)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        pkv.paged_prefill_attn(d, q, qo, t["k_pool"], t["v_pool"], t["kv_indices"],
+                               t["kv_indptr"], t["seq_lens"], out)
+    out.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), eager.view(torch.int16))
+
+
+def test_prefill_flags_bad_chunk():
+    """A chunk longer than its row is refused with PKV_FLAG_BAD_LEN; the other
+    rows are still right."""
+    lens, qls = [50, 20, 80], [50, 20, 30]
+    c = wl.prefill("pfb", B=3, Hq=8, Hkv=2, D=64, page_size=16, seq_lens=lens, q_lens=qls,
+                   seed=2)
+    want = _want(c)
+    w = c.w
+    w.seq_lens[1] = 10                      # row 1's chunk of 20 now exceeds it
+    out, st, _ = _run(c)
+    assert st & pkv.FLAG_BAD_LEN
+    compare_out(out[:50], want[:50])
+    compare_out(out[70:], want[70:])
