@@ -225,12 +225,16 @@ pkv_status decode_combine(const pkv_dims *dims, const float *o_part,
  * L - q_len + i and attends keys 0 .. that position:
  *   out[qo_indptr[b] + i, h] = softmax(scale q K^T) V over those keys, kv
  *   head h / (Hq/Hkv), fp32 softmax, bf16 output [total_q, Hq, D].
- * A row with q_len < 0 or > L, or L > max_seq_len, sets PKV_FLAG_BAD_LEN
- * and its outputs are left unwritten; bad page ids set PKV_FLAG_BAD_PAGE
- * (page 0 is read instead).  B <= 4096 (else PKV_ERR_UNSUPPORTED).  status
- * (device, nullable) receives the flags.  No workspace; graph-capturable. */
+ * max_q_len (host int, >= every chunk length; the pages' "max per-request
+ * q_len ... for grid computation") sizes the grid.  A row with q_len < 0 or
+ * > L, L > max_seq_len, or a chunk longer than max_q_len sets
+ * PKV_FLAG_BAD_LEN and its outputs are left unwritten; bad page ids set
+ * PKV_FLAG_BAD_PAGE (page 0 is read instead).  B * Hkv <= 65535 (else
+ * PKV_ERR_UNSUPPORTED).  status (device, nullable) receives the flags.  No
+ * workspace; graph-capturable.  Runs on the 5th-generation tensor cores
+ * (tcgen05.mma, accumulators in tensor memory). */
 pkv_status paged_prefill_attn(const pkv_dims *dims, const void *q, const int32_t *qo_indptr,
-                              int total_q, const void *k_pool, const void *v_pool,
+                              int total_q, int max_q_len, const void *k_pool, const void *v_pool,
                               const int32_t *kv_indices, const int32_t *kv_indptr,
                               const int32_t *seq_lens, void *out, uint32_t *status,
                               pkv_stream_t stream);

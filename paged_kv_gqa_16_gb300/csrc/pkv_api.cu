@@ -562,7 +562,7 @@ pkv_status decode_attn_contig(const pkv_dims *dims, const void *q, const void *k
 }
 
 pkv_status paged_prefill_attn(const pkv_dims *dims, const void *q, const int32_t *qo_indptr,
-                              int total_q, const void *k_pool, const void *v_pool,
+                              int total_q, int max_q_len, const void *k_pool, const void *v_pool,
                               const int32_t *kv_indices, const int32_t *kv_indptr,
                               const int32_t *seq_lens, void *out, uint32_t *status,
                               pkv_stream_t stream)
@@ -570,11 +570,11 @@ pkv_status paged_prefill_attn(const pkv_dims *dims, const void *q, const int32_t
     pkv_status st = check_dims(dims);
     if (st != PKV_OK)
         return st;
-    if (total_q < 0)
+    if (total_q < 0 || max_q_len < 0)
         return PKV_ERR_INVALID_ARG;
-    if (dims->B == 0 || total_q == 0)
+    if (dims->B == 0 || total_q == 0 || max_q_len == 0)
         return PKV_OK;
-    if (dims->B > pkv::kPrefillMaxRows)
+    if ((long long)dims->B * dims->Hkv > 65535)
         return PKV_ERR_UNSUPPORTED;
     if (q == nullptr || qo_indptr == nullptr || k_pool == nullptr || v_pool == nullptr ||
         kv_indptr == nullptr || seq_lens == nullptr || out == nullptr ||
@@ -605,9 +605,9 @@ pkv_status paged_prefill_attn(const pkv_dims *dims, const void *q, const int32_t
     p.num_indices = dims->num_indices;
     p.max_seq_len = dims->max_seq_len;
     p.total_q = total_q;
-    p.tq = 64 / p.n_rep;
+    p.tq = 128 / p.n_rep;
     p.scale_log2 = (float)((double)dims->scale * 1.4426950408889634);
-    return launch_status(pkv::launch_prefill(p, dims->D, (cudaStream_t)stream));
+    return launch_status(pkv::launch_prefill(p, dims->D, max_q_len, (cudaStream_t)stream));
 }
 
 pkv_status paged_decode_partials(const pkv_dims *dims, const void *q, const void *k_pool,

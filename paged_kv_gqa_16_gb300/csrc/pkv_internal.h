@@ -52,8 +52,6 @@ struct AdvanceParams {
 };
 
 // Paged ragged prefill / extend (pkv_prefill.cu).
-constexpr int kPrefillMaxRows = 4096;   // rows whose query-tile counts fit in smem
-
 struct PrefillParams {
     const __nv_bfloat16 *q;        // [total_q, Hq, D]
     const int32_t *qo_indptr;      // [B+1]
@@ -65,7 +63,7 @@ struct PrefillParams {
     __nv_bfloat16 *out;            // [total_q, Hq, D]
     uint32_t *status;              // nullable
     int B, Hq, Hkv, n_rep, page_size, ps_shift, num_pages, num_indices, max_seq_len, total_q;
-    int tq;                        // query tokens per block: 64 / n_rep
+    int tq;                        // query tokens per block: 128 / n_rep
     float scale_log2;
 };
 
@@ -125,7 +123,8 @@ struct CombineParams {
 
 cudaError_t launch_append(const AppendParams &p, cudaStream_t stream);
 cudaError_t launch_advance(const AdvanceParams &p, cudaStream_t stream);
-cudaError_t launch_prefill(const PrefillParams &p, int D, cudaStream_t stream);
+// grid: (ceil(max_q_len / tq), B * Hkv)
+cudaError_t launch_prefill(const PrefillParams &p, int D, int max_q_len, cudaStream_t stream);
 // table[0..B] = 0..B (kv_indptr), table[B+1+b] = idx ? idx[b] : b (kv_indices)
 cudaError_t launch_contig_table(const int32_t *idx, int B, int32_t *table, cudaStream_t stream);
 cudaError_t launch_rope_table(float *cos_sin, int max_pos, int D, double base,

@@ -1,4 +1,5 @@
-// pkv_prefill.cu -- paged ragged prefill / extend attention.
+// pkv_prefill.cu -- paged ragged prefill / extend attention on the
+// 5th-generation tensor cores (tcgen05.mma, accumulators in tensor memory).
 //
 // What it computes (AstrAI commit log, compare v1.3.12..6f09b1d,
 // astrai/extension/attention_ops.py, attn_paged_prefill and attn_prefill):
@@ -9,20 +10,27 @@
 // 0 .. that position: out = softmax(scale q K^T) V with K/V of kv head
 // h / n_rep gathered through the page table.
 //
-// Layout of the work.  A block takes one (row, kv head, tile of query
-// tokens); its 64 query rows are the tile's tokens x the kv head's n_rep
-// query heads (token-major), so the tile holds 64 / n_rep tokens.  Per key
-// tile of 64 tokens:
-//  - a producer warp gathers the K and V rows of that kv head with 1-D bulk
-//    copies (one D*2-byte row per token, looked up through the page table)
-//    into a two-stage ring of padded rows (ldmatrix reads are bank-conflict
-//    free), handed over by full/empty mbarriers, every wait time-bounded;
-//  - four consumer warps, 16 query rows each, form S = q K^T with m16n8k16
-//    bf16 tensor-core products, mask keys past each row's position, update
-//    an fp32 online softmax (log2 domain), round P to bf16 and add P V.
-// Key tiles entirely at or before the tile's first position need no mask.
-// Row b's query tiles are handed out last tile first, so the blocks with the
-// most keys start first.
+// Layout of the work.  One block of 128 threads takes one (query tile, row,
+// kv head): 128 query rows = the tile's 128 / n_rep tokens x the kv head's
+// n_rep query heads (token-major).  Thread t owns query row t, which is lane t
+// of tensor memory.  Per key tile of 64 tokens:
+//  - every thread gathers 16-byte chunks of the tile's K and V rows through
+//    the page table with cp.async, straight into the no-swizzle canonical
+//    layout the MMA reads (8-row x 16-byte core matrices; consecutive threads
+//    fill consecutive 16 bytes), two stages;
+//  - one thread issues S = Q K^T (M 128, N 64, K = D in steps of 16; Q and K
+//    K-major) into 64 TMEM columns and commits it to an mbarrier;
+//  - each thread loads its row of S from TMEM, masks keys past its position,
+//    updates its own fp32 online softmax (log2 domain), writes P (bf16) into
+//    shared memory as the K-major A operand, and rescales its row of O in
+//    TMEM only when its max has grown by more than 2^8 (P stays below 2^8
+//    otherwise; l is summed from the same bf16 P);
+//  - one thread issues O += P V (M 128, N = D, K = 64; V read MN-major, its
+//    rows as they are) into D TMEM columns, then the next tile's S.
+// Descriptors: version 1, no swizzle; leading byte offset = stride between
+// core matrices along K, stride byte offset = along M/N, for both K-major and
+// MN-major operands.  Every mbarrier wait is time-bounded; tensor memory is
+// allocated by warp 0 at the start and released on every path.
 #include <cmath>
 
 #include "pkv_device.cuh"
@@ -32,375 +40,414 @@ namespace pkv {
 
 namespace {
 
-constexpr unsigned kAll = 0xffffffffu;
+constexpr unsigned kAllTc = 0xffffffffu;
 
-__device__ __forceinline__ void flag(uint32_t *status, unsigned bits)
+template <int D>
+struct TcCfg {
+    static constexpr int kRows = 128;
+    static constexpr int kKeys = 64;
+    static constexpr int kThreads = 128;
+    static constexpr int kGroup = D * 16;                  // 8 rows x D bf16, canonical
+    static constexpr int kQBytes = kRows / 8 * kGroup;
+    static constexpr int kKVBytes = kKeys / 8 * kGroup;    // one K or V tile
+    static constexpr int kPGroup = kKeys * 16;             // 8 rows x 64 keys
+    static constexpr int kPBytes = kRows / 8 * kPGroup;
+    static constexpr int kKVOff = kQBytes;                 // stage s: K, then V
+    static constexpr int kPOff = kKVOff + 2 * 2 * kKVBytes;
+    static constexpr int kBarOff = kPOff + kPBytes;        // mbar S, mbar O
+    static constexpr int kTmemSlot = kBarOff + 16;
+    static constexpr int kSmemBytes = kBarOff + 32;
+    static constexpr uint32_t kTmemCols = 256;             // S: [0, 64), O: [128, 128 + D)
+    static constexpr uint32_t kSCol = 0, kOCol = 128;
+};
+
+__device__ __forceinline__ void tc_flag(uint32_t *status, unsigned bits)
 {
     if (status != nullptr)
         atomicOr(status, bits);
 }
 
-template <int D>
-struct PrefillCfg {
-    static constexpr int kRows = 64;                  // query rows per block
-    static constexpr int kKeys = 64;                  // keys per tile
-    static constexpr int kStages = 2;
-    static constexpr int kConsumers = 4;
-    static constexpr int kThreads = (kConsumers + 1) * 32;
-    static constexpr int kRowBytes = D * 2;
-    static constexpr int kPitch = kRowBytes + 16;
-    static constexpr int kQBytes = kRows * kRowBytes;
-    static constexpr int kTileBytes = kKeys * kPitch;
-    static constexpr int kStageBytes = 2 * kTileBytes;   // K rows, then V rows
-    static constexpr int kRingOffset = kQBytes;
-    static constexpr int kBarOffset = kRingOffset + kStages * kStageBytes;
-    static constexpr int kPrefixOffset = kBarOffset + (2 * kStages + 1) * 8 + 8;
-    static constexpr int kSmemBytes = kPrefixOffset + (kPrefillMaxRows + 1) * 4;
-    static_assert(kRingOffset % 16 == 0 && kBarOffset % 8 == 0 && kPitch % 16 == 0,
-                  "bulk-copy destinations need 16-byte alignment");
-};
-
-template <int D>
-__global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 2)
-    prefill_kernel(const PrefillParams p)
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo)
 {
-    using C = PrefillCfg<D>;
-    constexpr int NST = C::kStages;
-    extern __shared__ __align__(128) unsigned char smem[];
-    unsigned char *s_q = smem;
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::kBarOffset);
-    uint64_t *empty = full + NST;
-    uint64_t *qbar = empty + NST;
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(qbar + 1);
-    int *prefix = reinterpret_cast<int *>(smem + C::kPrefixOffset);
+    return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+           ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | ((uint64_t)1 << 46);
+}
 
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int g = blockIdx.y;                         // kv head
+// kind::f16 instruction descriptor: f32 accumulate, bf16 A and B.
+__host__ __device__ constexpr uint32_t instr_desc(int M, int N, int b_mn_major)
+{
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)b_mn_major << 16) |
+           ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void umma(uint32_t tmem, uint64_t ad, uint64_t bd, uint32_t idesc,
+                                     uint32_t accumulate)
+{
+    asm volatile("{\n .reg .pred p;\n setp.ne.u32 p, %4, 0;\n"
+                 " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(tmem),
+                 "l"(ad), "l"(bd), "r"(idesc), "r"(accumulate)
+                 : "memory");
+}
+
+__device__ __forceinline__ void umma_commit(uint64_t *bar)
+{
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+            smem_addr(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before()
+{
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_fence_after()
+{
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// 16 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16])
+{
+    uint32_t r[16];
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+                 "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                   "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]),
+                   "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+                 : "r"(taddr)
+                 : "memory");
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+        v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16])
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+                 "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+                 "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])),
+                 "r"(__float_as_uint(v[2])), "r"(__float_as_uint(v[3])),
+                 "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+                 "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])),
+                 "r"(__float_as_uint(v[8])), "r"(__float_as_uint(v[9])),
+                 "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+                 "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])),
+                 "r"(__float_as_uint(v[14])), "r"(__float_as_uint(v[15]))
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_wait()
+{
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// 16-byte global -> shared copy; src_bytes 0 writes zeros.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32_t src_bytes)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+                 "r"(src_bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit()
+{
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all()
+{
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+}
+
+template <int D>
+__global__ void __launch_bounds__(TcCfg<D>::kThreads, 2) prefill_tc_kernel(const PrefillParams p)
+{
+    using C = TcCfg<D>;
+    constexpr int CH = D / 8;                      // 16-byte chunks per row
+    extern __shared__ __align__(1024) unsigned char smem[];
+    uint64_t *bar_s = reinterpret_cast<uint64_t *>(smem + C::kBarOff);
+    uint64_t *bar_o = bar_s + 1;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kTmemSlot);
+    const uint32_t sbase = smem_addr(smem);
+    const int tid = threadIdx.x, warp = tid >> 5;
+
+    const int b = blockIdx.y / p.Hkv, g = blockIdx.y % p.Hkv;
     const int n_rep = p.n_rep, tq = p.tq;
 
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < NST; ++i) {
-            mbar_init(&full[i], 32);
-            mbar_init(&empty[i], C::kConsumers);
-        }
-        mbar_init(qbar, 1);
+    if (tid == 0) {
+        mbar_init(bar_s, 1);
+        mbar_init(bar_o, 1);
         fence_mbar_init();
-        *abort_flag = 0;
     }
     grid_dependency_wait();
-
-    // ---- query tiles per row, checked, then their prefix sums -------------
-    for (int r = threadIdx.x; r < p.B; r += blockDim.x) {
-        const int a = p.qo_indptr[r], e = p.qo_indptr[r + 1];
-        const int L = p.seq_lens[r];
-        int n = e - a;
-        if (n < 0 || a < 0 || e > p.total_q || L < 0 || L > p.max_seq_len || n > L) {
-            if (blockIdx.x == 0 && g == 0)
-                flag(p.status, kFlagBadLen);
-            n = 0;
-        }
-        prefix[r + 1] = (n + tq - 1) / tq;
-    }
-    __syncthreads();
-    if (warp == 0) {
-        int carry = 0;
-        for (int base = 0; base < p.B; base += 32) {
-            const int i = base + lane;
-            int v = i < p.B ? prefix[i + 1] : 0;
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const int t = __shfl_up_sync(kAll, v, off);
-                if (lane >= off)
-                    v += t;
-            }
-            v += carry;
-            if (i < p.B)
-                prefix[i + 1] = v;
-            carry = __shfl_sync(kAll, v, 31);
-        }
-        if (lane == 0)
-            prefix[0] = 0;
-    }
-    __syncthreads();
-    const int tile_id = blockIdx.x;
-    if (tile_id >= prefix[p.B])
-        return;
-    int b = 0;
-    {
-        int lo = 0, hi = p.B - 1;                 // last row with prefix[row] <= tile_id
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (prefix[mid] <= tile_id)
-                lo = mid;
-            else
-                hi = mid - 1;
-        }
-        b = lo;
-    }
-    const int n_tiles = prefix[b + 1] - prefix[b];
-    const int t = n_tiles - 1 - (tile_id - prefix[b]);   // last tile first
-    const int q0 = p.qo_indptr[b];
-    const int q_len = p.qo_indptr[b + 1] - q0;
+    // the row's chunk, checked (a bad row is flagged once, by its tile 0)
+    const int q0 = p.qo_indptr[b], q1 = p.qo_indptr[b + 1];
     const int L = p.seq_lens[b];
-    const int i0 = t * tq;                               // first token of the tile
+    const int q_len = q1 - q0;
+    const bool row_ok = q_len >= 0 && q0 >= 0 && q1 <= p.total_q && L >= 0 &&
+                        L <= p.max_seq_len && q_len <= L;
+    if (!row_ok) {
+        if (blockIdx.x == 0 && g == 0 && tid == 0)
+            tc_flag(p.status, kFlagBadLen);
+        return;
+    }
+    const int n_tiles = (q_len + tq - 1) / tq;
+    if (n_tiles > (int)gridDim.x && blockIdx.x == 0 && g == 0 && tid == 0)
+        tc_flag(p.status, kFlagBadLen);                // chunk longer than max_q_len
+    if ((int)blockIdx.x >= n_tiles)
+        return;
+    const int t = n_tiles - 1 - (int)blockIdx.x;       // last tile (most keys) first
+    const int i0 = t * tq;
     const int ntok = min(tq, q_len - i0);
     const int pos_first = L - q_len + i0;
-    const int kv_end = pos_first + ntok;                 // keys [0, kv_end)
+    const int kv_end = pos_first + ntok;
     const int n_kt = (kv_end + C::kKeys - 1) / C::kKeys;
     const int pg0 = p.kv_indptr[b];
     const int npg = p.kv_indptr[b + 1] - pg0;
     const bool table_ok = pg0 >= 0 && npg >= 0 && p.kv_indptr[b + 1] <= p.num_indices &&
                           (long long)npg * p.page_size >= (long long)L;
+    if (!table_ok && tid == 0)
+        tc_flag(p.status, kFlagBadPage);
 
-    if (warp == C::kConsumers) {
-        // ======================= producer warp ============================
-        if (!table_ok) {
-            if (lane == 0)
-                flag(p.status, kFlagBadPage);
-        }
-        if (lane == 0) {
-            const uint32_t bytes = (uint32_t)(ntok * n_rep * C::kRowBytes);
-            mbar_arrive_expect_tx(qbar, bytes);
-            for (int i = 0; i < ntok; ++i)
-                bulk_copy_g2s(s_q + (size_t)i * n_rep * C::kRowBytes,
-                              p.q + ((size_t)(q0 + i0 + i) * p.Hq + (size_t)g * n_rep) * D,
-                              (uint32_t)(n_rep * C::kRowBytes), qbar);
-        }
-        int kt = 0;
-        for (; kt < n_kt; ++kt) {
-            const int st = kt % NST;
-            if (kt >= NST) {
-                const bool ok = mbar_wait_bounded(&empty[st], (uint32_t)(((kt / NST) - 1) & 1));
-                if (!__all_sync(kAll, ok) || *abort_flag) {
-                    if (lane == 0) {
-                        *abort_flag = 1;
-                        flag(p.status, kFlagTimeout);
-                    }
-                    break;
-                }
-            }
-            fence_proxy_async_smem();
-            const int tok0 = kt * C::kKeys;
-            const int nvalid = min(C::kKeys, kv_end - tok0);
-            unsigned char *krows = smem + C::kRingOffset + st * C::kStageBytes;
-            unsigned char *vrows = krows + C::kTileBytes;
-            // V rows past the last key must be finite (P is 0 there)
-            for (int j = nvalid; j < C::kKeys; ++j) {
-                uint4 *z = reinterpret_cast<uint4 *>(vrows + j * C::kPitch);
-                for (int k = lane; k < C::kRowBytes / 16; k += 32)
-                    z[k] = make_uint4(0u, 0u, 0u, 0u);
-            }
-            if (lane == 0)
-                mbar_arrive_expect_tx(&full[st], (uint32_t)(nvalid * 2 * C::kRowBytes));
-            else
-                mbar_arrive(&full[st]);
-            for (int j = lane; j < nvalid; j += 32) {
-                const int tok = tok0 + j;
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_addr(tmem_slot)),
+                     "r"(C::kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+
+    // ---- loads -------------------------------------------------------------
+    // Q: row m = token * n_rep + head; element e of this thread: the 16-byte
+    // chunk at canonical offset 16 e (row (e & 7) + 8 * group, chunk c).
+    const int rows_used = tq * n_rep;
+    for (int e = tid; e < C::kRows * CH; e += C::kThreads) {
+        const int r8 = e & 7, c = (e >> 3) % CH, grp = (e >> 3) / CH;
+        const int m = grp * 8 + r8;
+        const int tok = m / n_rep, hh = m - tok * n_rep;
+        const bool live = m < rows_used && tok < ntok;
+        const __nv_bfloat16 *src =
+            live ? p.q + ((size_t)(q0 + i0 + tok) * p.Hq + (size_t)g * n_rep + hh) * D + c * 8
+                 : p.q;
+        cp_async16(sbase + e * 16, src, live ? 16u : 0u);
+    }
+    auto load_kv = [&](int kt, int stage) {
+        const uint32_t kdst = sbase + C::kKVOff + stage * 2 * C::kKVBytes;
+        const uint32_t vdst = kdst + C::kKVBytes;
+        for (int e = tid; e < C::kKeys * CH; e += C::kThreads) {
+            const int r8 = e & 7, c = (e >> 3) % CH, grp = (e >> 3) / CH;
+            const int tok = kt * C::kKeys + grp * 8 + r8;
+            const bool live = tok < kv_end;
+            size_t off = 0;
+            if (live) {
                 const int pi = p.ps_shift >= 0 ? (tok >> p.ps_shift) : (tok / p.page_size);
                 const int sl = tok - pi * p.page_size;
                 int page = table_ok ? __ldg(p.kv_indices + pg0 + pi) : 0;
                 if (page < 0 || page >= p.num_pages) {
-                    flag(p.status, kFlagBadPage);
+                    tc_flag(p.status, kFlagBadPage);
                     page = 0;
                 }
-                const size_t off = (((size_t)page * p.page_size + sl) * p.Hkv + g) * D;
-                bulk_copy_g2s(krows + j * C::kPitch, p.k_pool + off, C::kRowBytes, &full[st]);
-                bulk_copy_g2s(vrows + j * C::kPitch, p.v_pool + off, C::kRowBytes, &full[st]);
+                off = (((size_t)page * p.page_size + sl) * p.Hkv + g) * D + c * 8;
             }
+            cp_async16(kdst + e * 16, p.k_pool + off, live ? 16u : 0u);
+            cp_async16(vdst + e * 16, p.v_pool + off, live ? 16u : 0u);
         }
-        // let the copies already issued land before the block exits
-        for (int k = (kt > NST ? kt - NST : 0); k < kt; ++k)
-            (void)mbar_wait_bounded(&full[k % NST], (uint32_t)((k / NST) & 1));
-        (void)mbar_wait_bounded(qbar, 0u);
-        return;
+    };
+    load_kv(0, 0);
+    cp_async_commit();
+    cp_async_wait_all();
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t t_s = tmem + C::kSCol, t_o = tmem + C::kOCol;
+    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+
+    constexpr uint32_t kIdescS = instr_desc(128, C::kKeys, 0);
+    constexpr uint32_t kIdescO = instr_desc(128, D, 1);
+    const uint32_t q_s = sbase, p_s = sbase + C::kPOff;
+    auto issue_s = [&](int stage) {
+        const uint32_t k_s = sbase + C::kKVOff + stage * 2 * C::kKVBytes;
+#pragma unroll
+        for (int s = 0; s < D / 16; ++s)
+            umma(t_s, smem_desc(q_s + s * 256, 128, C::kGroup),
+                 smem_desc(k_s + s * 256, 128, C::kGroup), kIdescS, s > 0);
+    };
+    auto issue_o = [&](int stage, bool first) {
+        const uint32_t v_s = sbase + C::kKVOff + stage * 2 * C::kKVBytes + C::kKVBytes;
+#pragma unroll
+        for (int s = 0; s < C::kKeys / 16; ++s)
+            umma(t_o, smem_desc(p_s + s * 256, 128, C::kPGroup),
+                 smem_desc(v_s + s * 2 * C::kGroup, C::kGroup, 128), kIdescO,
+                 (first && s == 0) ? 0u : 1u);
+    };
+    if (tid == 0) {
+        issue_s(0);
+        umma_commit(bar_s);
     }
 
-    // ========================= consumer warps ===============================
-    const int fr = lane >> 2, cq = (lane & 3) * 2;
-    const int k_tok = (lane & 7) + ((lane >> 4) << 3);
-    const int k_col = ((lane >> 3) & 1) * 8;
-    const int v_tok = (lane & 7) + (((lane >> 3) & 1) << 3);
-    const int v_col = (lane >> 4) * 8;
-    const uint32_t ring_s = smem_addr(smem + C::kRingOffset);
-    // this thread's two query rows (fragment rows fr and fr + 8)
-    const int rows_used = tq * n_rep;
-    int rr[2], pos[2];
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        rr[h] = warp * 16 + fr + 8 * h;
-        const int tok = rr[h] / n_rep;
-        pos[h] = (rr[h] < rows_used && tok < ntok) ? pos_first + tok : -1;
-    }
-    bool aborted = false;
-    {
-        const bool ok = mbar_wait_bounded(qbar, 0u);
-        if (!__all_sync(kAll, ok)) {
-            aborted = true;
-            if (lane == 0) {
-                *abort_flag = 1;
-                flag(p.status, kFlagTimeout);
-            }
-        }
-    }
-    uint32_t qf[D / 16][4];
-#pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk) {
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const uint32_t *qr = reinterpret_cast<const uint32_t *>(s_q + rr[h] * C::kRowBytes);
-            const bool live = pos[h] >= 0;
-            qf[kk][h] = live ? qr[(kk * 16 + cq) / 2] : 0u;
-            qf[kk][2 + h] = live ? qr[(kk * 16 + 8 + cq) / 2] : 0u;
-        }
-    }
-    const int pos_min_block = pos_first;   // rows of this block: positions >= pos_first
+    // this thread's query row
+    const int m = tid;
+    const int tok_m = m / n_rep;
+    const int pos = (m < rows_used && tok_m < ntok) ? pos_first + tok_m : -1;
+    float m_run = -INFINITY, l_run = 0.f;
+    bool ok = true;
+    unsigned char *p_row = smem + C::kPOff + (m >> 3) * C::kPGroup + (m & 7) * 16;
 
-    float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
-    float oacc[D / 8][4];
-#pragma unroll
-    for (int j = 0; j < D / 8; ++j)
-        oacc[j][0] = oacc[j][1] = oacc[j][2] = oacc[j][3] = 0.f;
-
-    for (int kt = 0; kt < n_kt; ++kt) {
-        const int st = kt % NST;
-        if (!aborted) {
-            const bool ok = mbar_wait_bounded(&full[st], (uint32_t)((kt / NST) & 1));
-            if (!__all_sync(kAll, ok) || *abort_flag) {
-                aborted = true;
-                if (lane == 0) {
-                    *abort_flag = 1;
-                    flag(p.status, kFlagTimeout);
-                }
-            }
+    for (int kt = 0; kt < n_kt && ok; ++kt) {
+        const int stage = kt & 1;
+        // S of this tile (and the previous tile's P V) are done
+        ok = mbar_wait_bounded(bar_s, (uint32_t)(kt & 1));
+        if (!__all_sync(kAllTc, ok)) {
+            ok = false;
+            if ((tid & 31) == 0)
+                tc_flag(p.status, kFlagTimeout);
         }
-        if (aborted)
+        ok = __syncthreads_and(ok);
+        if (!ok)
             break;
-        const int tok0 = kt * C::kKeys;
-        const uint32_t kbase = ring_s + st * C::kStageBytes;
-        const uint32_t vbase = kbase + C::kTileBytes;
-        // S = q K^T over 64 keys: sacc[kg][nt] covers keys tok0 + kg*16 + nt*8 ..
-        float sacc[4][2][4];
+        tc_fence_after();
+        if (kt + 1 < n_kt)
+            load_kv(kt + 1, stage ^ 1);
+        cp_async_commit();
+
+        // ---- softmax of this row over the tile's 64 keys ----------------
+        const int key0 = kt * C::kKeys;
+        const bool need_mask = key0 + C::kKeys - 1 > pos_first;
+        float sv[C::kKeys];
 #pragma unroll
-        for (int kg = 0; kg < 4; ++kg) {
+        for (int c0 = 0; c0 < C::kKeys; c0 += 16) {
+            float v[16];
+            tmem_ld16(t_s + lane_off + c0, v);
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
-                sacc[kg][nt][0] = sacc[kg][nt][1] = sacc[kg][nt][2] = sacc[kg][nt][3] = 0.f;
-            const uint32_t kaddr = kbase + (kg * 16 + k_tok) * C::kPitch + k_col * 2;
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-                uint32_t b0, b1, b2, b3;
-                ldmatrix_x4(b0, b1, b2, b3, kaddr + kk * 32);
-                mma_bf16_16816(sacc[kg][0], qf[kk], b0, b1);
-                mma_bf16_16816(sacc[kg][1], qf[kk], b2, b3);
+            for (int i = 0; i < 16; ++i) {
+                float x = v[i] * p.scale_log2;
+                if (need_mask && key0 + c0 + i > pos)
+                    x = -INFINITY;
+                sv[c0 + i] = x;
             }
         }
-        // scale to the log2 domain; mask keys past each row's position (and
-        // past the tile's last key) in tiles that reach the diagonal
-        const bool need_mask = tok0 + C::kKeys - 1 > pos_min_block;
-        float mx[2] = {-INFINITY, -INFINITY};
+        float mx = -INFINITY;
 #pragma unroll
-        for (int kg = 0; kg < 4; ++kg)
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int h = e >> 1;
-                    const int key = tok0 + kg * 16 + nt * 8 + cq + (e & 1);
-                    float x = sacc[kg][nt][e] * p.scale_log2;
-                    if (need_mask && key > pos[h])
-                        x = -INFINITY;
-                    sacc[kg][nt][e] = x;
-                    mx[h] = fmaxf(mx[h], x);
-                }
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            mx[h] = fmaxf(mx[h], __shfl_xor_sync(kAll, mx[h], 1));
-            mx[h] = fmaxf(mx[h], __shfl_xor_sync(kAll, mx[h], 2));
+        for (int i = 0; i < C::kKeys; ++i)
+            mx = fmaxf(mx, sv[i]);
+        // a new base only when the max grows by more than 2^8 (or first)
+        const bool rebase = mx > m_run + 8.f;
+        float alpha = 1.f;
+        if (rebase) {
+            alpha = exp2f(m_run - mx);                 // 0 while m_run is -inf
+            m_run = mx;
+            l_run *= alpha;
         }
-        float base[2], alpha[2];
+        if (__any_sync(kAllTc, rebase && kt > 0)) {
+            // rescale this warp's rows of O (the previous P V has completed)
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const float mn = fmaxf(m_run[h], mx[h]);
-            base[h] = mn == -INFINITY ? 0.f : mn;
-            alpha[h] = exp2f(m_run[h] - base[h]);
-            m_run[h] = mn;
+            for (int c0 = 0; c0 < D; c0 += 16) {
+                float v[16];
+                tmem_ld16(t_o + lane_off + c0, v);
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    v[i] *= alpha;
+                tmem_st16(t_o + lane_off + c0, v);
+            }
+            tmem_st_wait();
         }
-        uint32_t pa[4][4];
-        float lsum[2] = {0.f, 0.f};
+        const float base = m_run == -INFINITY ? 0.f : m_run;
+        float lsum = 0.f;
 #pragma unroll
-        for (int kg = 0; kg < 4; ++kg) {
-            pa[kg][0] = pack_bf16x2(exp2f(sacc[kg][0][0] - base[0]), exp2f(sacc[kg][0][1] - base[0]));
-            pa[kg][1] = pack_bf16x2(exp2f(sacc[kg][0][2] - base[1]), exp2f(sacc[kg][0][3] - base[1]));
-            pa[kg][2] = pack_bf16x2(exp2f(sacc[kg][1][0] - base[0]), exp2f(sacc[kg][1][1] - base[0]));
-            pa[kg][3] = pack_bf16x2(exp2f(sacc[kg][1][2] - base[1]), exp2f(sacc[kg][1][3] - base[1]));
-            lsum[0] += (bf16_lo(pa[kg][0]) + bf16_hi(pa[kg][0])) +
-                       (bf16_lo(pa[kg][2]) + bf16_hi(pa[kg][2]));
-            lsum[1] += (bf16_lo(pa[kg][1]) + bf16_hi(pa[kg][1])) +
-                       (bf16_lo(pa[kg][3]) + bf16_hi(pa[kg][3]));
+        for (int c = 0; c < C::kKeys / 8; ++c) {
+            uint32_t w[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                w[j] = pack_bf16x2(exp2f(sv[c * 8 + 2 * j] - base),
+                                   exp2f(sv[c * 8 + 2 * j + 1] - base));
+                lsum += bf16_lo(w[j]) + bf16_hi(w[j]);
+            }
+            *reinterpret_cast<uint4 *>(p_row + c * 128) = make_uint4(w[0], w[1], w[2], w[3]);
         }
-        l_run[0] = l_run[0] * alpha[0] + lsum[0];
-        l_run[1] = l_run[1] * alpha[1] + lsum[1];
-#pragma unroll
-        for (int j = 0; j < D / 8; ++j) {
-            oacc[j][0] *= alpha[0];
-            oacc[j][1] *= alpha[0];
-            oacc[j][2] *= alpha[1];
-            oacc[j][3] *= alpha[1];
-        }
-        // O += P V
-#pragma unroll
-        for (int kg = 0; kg < 4; ++kg) {
-            const uint32_t vaddr = vbase + (kg * 16 + v_tok) * C::kPitch + v_col * 2;
-#pragma unroll
-            for (int jj = 0; jj < D / 16; ++jj) {
-                uint32_t b0, b1, b2, b3;
-                ldmatrix_x4_trans(b0, b1, b2, b3, vaddr + jj * 32);
-                mma_bf16_16816(oacc[2 * jj], pa[kg], b0, b1);
-                mma_bf16_16816(oacc[2 * jj + 1], pa[kg], b2, b3);
+        l_run += lsum;
+
+        // ---- hand P (and the next tile) to the tensor cores --------------
+        cp_async_wait_all();
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        if (tid == 0) {
+            tc_fence_after();
+            issue_o(stage, kt == 0);
+            if (kt + 1 < n_kt) {
+                issue_s(stage ^ 1);
+                umma_commit(bar_s);
+            } else {
+                umma_commit(bar_o);
             }
         }
-        __syncwarp();
-        if (lane == 0)
-            mbar_arrive(&empty[st]);
     }
 
-    // ---- normalise and store ------------------------------------------------
+    // ---- normalise and store this row -------------------------------------
+    bool done = ok && mbar_wait_bounded(bar_o, 0u);
+    if (ok && !__all_sync(kAllTc, done) && (tid & 31) == 0)
+        tc_flag(p.status, kFlagTimeout);
+    done = __syncthreads_and(done);
+    tc_fence_after();
+    if (done) {
+        const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+        __nv_bfloat16 *orow = nullptr;
+        if (pos >= 0) {
+            const int hh = m - tok_m * n_rep;
+            orow = p.out + ((size_t)(q0 + i0 + tok_m) * p.Hq + (size_t)g * n_rep + hh) * D;
+        }
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        l_run[h] += __shfl_xor_sync(kAll, l_run[h], 1);
-        l_run[h] += __shfl_xor_sync(kAll, l_run[h], 2);
+        for (int c0 = 0; c0 < D; c0 += 16) {
+            float v[16];
+            tmem_ld16(t_o + lane_off + c0, v);
+            if (orow != nullptr) {
+                uint4 lo = make_uint4(pack_bf16x2(v[0] * inv, v[1] * inv),
+                                      pack_bf16x2(v[2] * inv, v[3] * inv),
+                                      pack_bf16x2(v[4] * inv, v[5] * inv),
+                                      pack_bf16x2(v[6] * inv, v[7] * inv));
+                uint4 hi = make_uint4(pack_bf16x2(v[8] * inv, v[9] * inv),
+                                      pack_bf16x2(v[10] * inv, v[11] * inv),
+                                      pack_bf16x2(v[12] * inv, v[13] * inv),
+                                      pack_bf16x2(v[14] * inv, v[15] * inv));
+                *reinterpret_cast<uint4 *>(orow + c0) = lo;
+                *reinterpret_cast<uint4 *>(orow + c0 + 8) = hi;
+            }
+        }
     }
-    if (aborted)
-        return;
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        if (pos[h] < 0)
-            continue;
-        const float inv = l_run[h] > 0.f ? 1.f / l_run[h] : 0.f;
-        const int tok = rr[h] / n_rep, hh = rr[h] - tok * n_rep;
-        __nv_bfloat16 *o = p.out + ((size_t)(q0 + i0 + tok) * p.Hq + (size_t)g * n_rep + hh) * D + cq;
-#pragma unroll
-        for (int j = 0; j < D / 8; ++j)
-            *reinterpret_cast<uint32_t *>(o + 8 * j) =
-                pack_bf16x2(oacc[j][2 * h] * inv, oacc[j][2 * h + 1] * inv);
-    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(C::kTmemCols)
+                     : "memory");
 }
 
 template <int D>
-cudaError_t launch_prefill_d(const PrefillParams &p, int grid_x, cudaStream_t stream)
+cudaError_t launch_tc_d(const PrefillParams &p, int max_q_len, cudaStream_t stream)
 {
-    using C = PrefillCfg<D>;
+    using C = TcCfg<D>;
     static bool attr_done = false;
     if (!attr_done) {
-        cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D>,
+        cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<D>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              C::kSmemBytes);
         if (e != cudaSuccess)
             return e;
         attr_done = true;
     }
+    const long long tiles = ((long long)max_q_len + p.tq - 1) / p.tq;
+    const long long rows = (long long)p.B * p.Hkv;
+    if (tiles <= 0 || rows <= 0)
+        return cudaSuccess;
+    if (tiles > 0x7fffffffLL || rows > 65535)
+        return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid_x, p.Hkv);
+    cfg.gridDim = dim3((unsigned)tiles, (unsigned)rows);
     cfg.blockDim = dim3(C::kThreads);
     cfg.dynamicSmemBytes = C::kSmemBytes;
     cfg.stream = stream;
@@ -409,7 +456,7 @@ cudaError_t launch_prefill_d(const PrefillParams &p, int grid_x, cudaStream_t st
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, prefill_kernel<D>, p);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, prefill_tc_kernel<D>, p);
     if (e != cudaSuccess)
         return e;
     return cudaGetLastError();
@@ -417,17 +464,11 @@ cudaError_t launch_prefill_d(const PrefillParams &p, int grid_x, cudaStream_t st
 
 } // namespace
 
-cudaError_t launch_prefill(const PrefillParams &p, int D, cudaStream_t stream)
+cudaError_t launch_prefill(const PrefillParams &p, int D, int max_q_len, cudaStream_t stream)
 {
-    // enough tile slots for any split of total_q tokens over B rows
-    const long long slots = ((long long)p.total_q + p.tq - 1) / p.tq + p.B;
-    if (slots <= 0)
-        return cudaSuccess;
-    if (slots > 0x7fffffffLL)
-        return cudaErrorInvalidValue;
     if (D == 64)
-        return launch_prefill_d<64>(p, (int)slots, stream);
-    return launch_prefill_d<128>(p, (int)slots, stream);
+        return launch_tc_d<64>(p, max_q_len, stream);
+    return launch_tc_d<128>(p, max_q_len, stream);
 }
 
 } // namespace pkv

@@ -91,7 +91,7 @@ def lib():
             "paged_decode_attn_noalloc": (I, [DP, P, P, P, P, P, P, I, P, P, P]),
             "paged_kv_advance": (I, [DP, P, P, P, P, I, P, P, P]),
             "decode_attn_contig": (I, [DP, P, P, P, P, P, P, P, P, I, I, P, Z, P, P]),
-            "paged_prefill_attn": (I, [DP, P, P, I, P, P, P, P, P, P, P, P]),
+            "paged_prefill_attn": (I, [DP, P, P, I, I, P, P, P, P, P, P, P, P]),
             "pkv_status_str": (ctypes.c_char_p, [I]),
             "pkv_version": (I, []),
         }
@@ -230,11 +230,14 @@ def decode_attn_contig(d: Dims, q, k_cache, v_cache, seq_lens, num_splits: int, 
 
 
 def paged_prefill_attn(d: Dims, q, qo_indptr, k_pool, v_pool, kv_indices, kv_indptr, seq_lens,
-                       out, status=None, stream=None) -> None:
+                       out, status=None, max_q_len: Optional[int] = None, stream=None) -> None:
     """Ragged prefill / extend: q [total_q, Hq, D], row b's chunk the last
-    q_len of its seq_lens[b] tokens, each query attending causally."""
+    q_len of its seq_lens[b] tokens, each query attending causally.
+    max_q_len (>= every chunk length) sizes the grid; None: total_q."""
+    total_q = int(q.shape[0])
     _check("paged_prefill_attn", lib().paged_prefill_attn(
-        ctypes.byref(d), _ptr(q), _ptr(qo_indptr), int(q.shape[0]), _ptr(k_pool), _ptr(v_pool),
+        ctypes.byref(d), _ptr(q), _ptr(qo_indptr), total_q,
+        total_q if max_q_len is None else int(max_q_len), _ptr(k_pool), _ptr(v_pool),
         _ptr(kv_indices), _ptr(kv_indptr), _ptr(seq_lens), _ptr(out), _ptr(status),
         _stream(stream)))
 
