@@ -576,6 +576,9 @@ pkv_status paged_prefill_attn(const pkv_dims *dims, const void *q, const int32_t
         return PKV_OK;
     if ((long long)dims->B * dims->Hkv > 65535)
         return PKV_ERR_UNSUPPORTED;
+    // the kernel keeps pool offsets in 16-byte units as 32-bit integers
+    if ((double)dims->num_pages * dims->page_size * dims->Hkv * dims->D / 8 >= 4294967295.0)
+        return PKV_ERR_UNSUPPORTED;
     if (q == nullptr || qo_indptr == nullptr || k_pool == nullptr || v_pool == nullptr ||
         kv_indptr == nullptr || seq_lens == nullptr || out == nullptr ||
         (dims->num_indices > 0 && kv_indices == nullptr))

@@ -56,7 +56,10 @@ struct TcCfg {
     static constexpr int kPOff = kKVOff + 2 * 2 * kKVBytes;
     static constexpr int kBarOff = kPOff + kPBytes;        // mbar S, mbar O
     static constexpr int kTmemSlot = kBarOff + 16;
-    static constexpr int kSmemBytes = kBarOff + 32;
+    static constexpr int kOffOff = kBarOff + 32;           // [2][64] key offsets
+    static constexpr int kSmemBytes = kOffOff + 2 * kKeys * 4;
+    // two blocks per SM: 2 x (kSmemBytes + 1 KB reserved) <= 228 KB
+    static_assert(2 * (kSmemBytes + 1024) <= 233472, "two blocks per SM");
     static constexpr uint32_t kTmemCols = 256;             // S: [0, 64), O: [128, 128 + D)
     static constexpr uint32_t kSCol = 0, kOCol = 128;
 };
@@ -234,15 +237,14 @@ __global__ void __launch_bounds__(TcCfg<D>::kThreads, 2) prefill_tc_kernel(const
                  : p.q;
         cp_async16(sbase + e * 16, src, live ? 16u : 0u);
     }
-    auto load_kv = [&](int kt, int stage) {
-        const uint32_t kdst = sbase + C::kKVOff + stage * 2 * C::kKVBytes;
-        const uint32_t vdst = kdst + C::kKVBytes;
-        for (int e = tid; e < C::kKeys * CH; e += C::kThreads) {
-            const int r8 = e & 7, c = (e >> 3) % CH, grp = (e >> 3) / CH;
-            const int tok = kt * C::kKeys + grp * 8 + r8;
-            const bool live = tok < kv_end;
-            size_t off = 0;
-            if (live) {
+    // pool offsets (16-byte units) of a tile's 64 keys, looked up once by
+    // threads 0..63 a tile ahead of the copies; all-ones for keys past kv_end
+    uint32_t *s_off = reinterpret_cast<uint32_t *>(smem + C::kOffOff);
+    auto lookup = [&](int kt) {
+        if (tid < C::kKeys) {
+            const int tok = kt * C::kKeys + tid;
+            uint32_t off = 0xFFFFFFFFu;
+            if (tok < kv_end) {
                 const int pi = p.ps_shift >= 0 ? (tok >> p.ps_shift) : (tok / p.page_size);
                 const int sl = tok - pi * p.page_size;
                 int page = table_ok ? __ldg(p.kv_indices + pg0 + pi) : 0;
@@ -250,12 +252,28 @@ __global__ void __launch_bounds__(TcCfg<D>::kThreads, 2) prefill_tc_kernel(const
                     tc_flag(p.status, kFlagBadPage);
                     page = 0;
                 }
-                off = (((size_t)page * p.page_size + sl) * p.Hkv + g) * D + c * 8;
+                off = (uint32_t)((((size_t)page * p.page_size + sl) * p.Hkv + g) * (D / 8));
             }
+            s_off[(kt & 1) * C::kKeys + tid] = off;
+        }
+    };
+    auto load_kv = [&](int kt, int stage) {
+        const uint32_t kdst = sbase + C::kKVOff + stage * 2 * C::kKVBytes;
+        const uint32_t vdst = kdst + C::kKVBytes;
+        const uint32_t *offs = s_off + (kt & 1) * C::kKeys;
+        for (int e = tid; e < C::kKeys * CH; e += C::kThreads) {
+            const int r8 = e & 7, c = (e >> 3) % CH, grp = (e >> 3) / CH;
+            const uint32_t o = offs[grp * 8 + r8];
+            const bool live = o != 0xFFFFFFFFu;
+            const size_t off = live ? ((size_t)o + c) * 8 : 0;
             cp_async16(kdst + e * 16, p.k_pool + off, live ? 16u : 0u);
             cp_async16(vdst + e * 16, p.v_pool + off, live ? 16u : 0u);
         }
     };
+    lookup(0);
+    if (n_kt > 1)
+        lookup(1);
+    __syncthreads();
     load_kv(0, 0);
     cp_async_commit();
     cp_async_wait_all();
@@ -372,6 +390,8 @@ __global__ void __launch_bounds__(TcCfg<D>::kThreads, 2) prefill_tc_kernel(const
         l_run += lsum;
 
         // ---- hand P (and the next tile) to the tensor cores --------------
+        if (kt + 2 < n_kt)
+            lookup(kt + 2);                    // published by the barrier below
         cp_async_wait_all();
         fence_proxy_async_smem();
         tc_fence_before();
