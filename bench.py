@@ -607,9 +607,12 @@ def run_pkv(args):
             pout = torch.empty(c.total_q, c.w.Hq, c.w.D, dtype=torch.bfloat16, device=dev)
             pst = torch.zeros(1, dtype=torch.int32, device=dev)
 
+            max_q = max(kw["q_lens"])
+
             def prun():
                 pkv.paged_prefill_attn(pd, pq, pqo, pt["k_pool"], pt["v_pool"], pt["kv_indices"],
-                                       pt["kv_indptr"], pt["seq_lens"], pout, status=pst)
+                                       pt["kv_indptr"], pt["seq_lens"], pout, status=pst,
+                                       max_q_len=max_q)
 
             for _ in range(3):
                 prun()

@@ -60,8 +60,11 @@ struct TcCfg {
     static constexpr int kSmemBytes = kOffOff + 2 * kKeys * 4;
     // two blocks per SM: 2 x (kSmemBytes + 1 KB reserved) <= 228 KB
     static_assert(2 * (kSmemBytes + 1024) <= 233472, "two blocks per SM");
-    static constexpr uint32_t kTmemCols = 256;             // S: [0, 64), O: [128, 128 + D)
-    static constexpr uint32_t kSCol = 0, kOCol = 128;
+    // S in columns [0, 64), O in [64, 64 + D): 128 columns at D = 64 (so the
+    // three blocks that fit an SM's shared memory all get tensor memory), 256
+    // at D = 128
+    static constexpr uint32_t kTmemCols = D <= 64 ? 128 : 256;
+    static constexpr uint32_t kSCol = 0, kOCol = 64;
 };
 
 __device__ __forceinline__ void tc_flag(uint32_t *status, unsigned bits)

@@ -233,7 +233,9 @@ def paged_prefill_attn(d: Dims, q, qo_indptr, k_pool, v_pool, kv_indices, kv_ind
                        out, status=None, max_q_len: Optional[int] = None, stream=None) -> None:
     """Ragged prefill / extend: q [total_q, Hq, D], row b's chunk the last
     q_len of its seq_lens[b] tokens, each query attending causally.
-    max_q_len (>= every chunk length) sizes the grid; None: total_q."""
+    max_q_len (>= every chunk length) sizes the grid; None: total_q, always
+    safe but many rows then launch many blocks that exit at once -- pass the
+    real maximum when it is known."""
     total_q = int(q.shape[0])
     _check("paged_prefill_attn", lib().paged_prefill_attn(
         ctypes.byref(d), _ptr(q), _ptr(qo_indptr), total_q,

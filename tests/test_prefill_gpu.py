@@ -105,3 +105,25 @@ def test_prefill_flags_bad_chunk():
     assert st & pkv.FLAG_BAD_LEN
     compare_out(out[:50], want[:50])
     compare_out(out[70:], want[70:])
+
+
+def test_prefill_max_q_len():
+    """The exact max chunk length gives the same bits as the always-safe
+    default (total_q); a bound below a chunk's length is flagged."""
+    lens, qls = [300, 90, 33], [120, 90, 1]
+    c = wl.prefill("pfq", B=3, Hq=16, Hkv=4, D=128, page_size=16, seq_lens=lens, q_lens=qls,
+                   seed=8)
+    ref, st, (d, t) = _run(c)
+    assert st == 0
+    q, qo = c.q.cuda(), c.qo_indptr.cuda()
+    out = torch.empty_like(ref)
+    st2 = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pkv.paged_prefill_attn(d, q, qo, t["k_pool"], t["v_pool"], t["kv_indices"], t["kv_indptr"],
+                           t["seq_lens"], out, status=st2, max_q_len=max(qls))
+    torch.cuda.synchronize()
+    assert int(st2.item()) == 0
+    assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+    pkv.paged_prefill_attn(d, q, qo, t["k_pool"], t["v_pool"], t["kv_indices"], t["kv_indptr"],
+                           t["seq_lens"], out, status=st2, max_q_len=64)
+    torch.cuda.synchronize()
+    assert int(st2.item()) & pkv.FLAG_BAD_LEN
