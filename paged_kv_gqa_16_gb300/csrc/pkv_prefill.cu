@@ -260,11 +260,15 @@ __global__ void __launch_bounds__(TcCfg<D>::kThreads, 2) prefill_tc_kernel(const
             s_off[(kt & 1) * C::kKeys + tid] = off;
         }
     };
-    auto load_kv = [&](int kt, int stage) {
+    // this thread's copies of a tile are NI rounds (element e = tid + 128 i);
+    // load_kv issues rounds [i0, i1)
+    constexpr int NI = C::kKeys * CH / C::kThreads;
+    auto load_kv = [&](int kt, int stage, int i0, int i1) {
         const uint32_t kdst = sbase + C::kKVOff + stage * 2 * C::kKVBytes;
         const uint32_t vdst = kdst + C::kKVBytes;
         const uint32_t *offs = s_off + (kt & 1) * C::kKeys;
-        for (int e = tid; e < C::kKeys * CH; e += C::kThreads) {
+        for (int i = i0; i < i1; ++i) {
+            const int e = tid + i * C::kThreads;
             const int r8 = e & 7, c = (e >> 3) % CH, grp = (e >> 3) / CH;
             const uint32_t o = offs[grp * 8 + r8];
             const bool live = o != 0xFFFFFFFFu;
@@ -277,7 +281,7 @@ __global__ void __launch_bounds__(TcCfg<D>::kThreads, 2) prefill_tc_kernel(const
     if (n_kt > 1)
         lookup(1);
     __syncthreads();
-    load_kv(0, 0);
+    load_kv(0, 0, 0, NI);
     cp_async_commit();
     cp_async_wait_all();
     fence_proxy_async_smem();
@@ -332,9 +336,11 @@ __global__ void __launch_bounds__(TcCfg<D>::kThreads, 2) prefill_tc_kernel(const
         if (!ok)
             break;
         tc_fence_after();
-        if (kt + 1 < n_kt)
-            load_kv(kt + 1, stage ^ 1);
-        cp_async_commit();
+        // the next tile's copies: half now, the rest spread through the P
+        // loop below, so load-store issue overlaps the softmax arithmetic
+        const bool more = kt + 1 < n_kt;
+        if (more)
+            load_kv(kt + 1, stage ^ 1, 0, NI / 2);
 
         // ---- softmax of this row over the tile's 64 keys ----------------
         const int key0 = kt * C::kKeys;
@@ -380,6 +386,8 @@ __global__ void __launch_bounds__(TcCfg<D>::kThreads, 2) prefill_tc_kernel(const
         const float base = m_run == -INFINITY ? 0.f : m_run;
         float lsum = 0.f;
 #pragma unroll
+        constexpr int kRest = NI - NI / 2;                // rounds left, kRest | 8
+        constexpr int kEvery = (C::kKeys / 8) / kRest;
         for (int c = 0; c < C::kKeys / 8; ++c) {
             uint32_t w[4];
 #pragma unroll
@@ -389,7 +397,12 @@ __global__ void __launch_bounds__(TcCfg<D>::kThreads, 2) prefill_tc_kernel(const
                 lsum += bf16_lo(w[j]) + bf16_hi(w[j]);
             }
             *reinterpret_cast<uint4 *>(p_row + c * 128) = make_uint4(w[0], w[1], w[2], w[3]);
+            if (more && (c + 1) % kEvery == 0) {
+                const int i = NI / 2 + (c + 1) / kEvery - 1;
+                load_kv(kt + 1, stage ^ 1, i, i + 1);
+            }
         }
+        cp_async_commit();
         l_run += lsum;
 
         // ---- hand P (and the next tile) to the tensor cores --------------
