@@ -225,6 +225,7 @@ pkv_status decode_combine(const pkv_dims *dims, const float *o_part,
  * L - q_len + i and attends keys 0 .. that position:
  *   out[qo_indptr[b] + i, h] = softmax(scale q K^T) V over those keys, kv
  *   head h / (Hq/Hkv), fp32 softmax, bf16 output [total_q, Hq, D].
+ * dims->scale must be > 0.
  * max_q_len (host int, >= every chunk length; the pages' "max per-request
  * q_len ... for grid computation") sizes the grid.  A row with q_len < 0 or
  * > L, L > max_seq_len, or a chunk longer than max_q_len sets

@@ -570,7 +570,7 @@ pkv_status paged_prefill_attn(const pkv_dims *dims, const void *q, const int32_t
     pkv_status st = check_dims(dims);
     if (st != PKV_OK)
         return st;
-    if (total_q < 0 || max_q_len < 0)
+    if (total_q < 0 || max_q_len < 0 || !(dims->scale > 0.f))
         return PKV_ERR_INVALID_ARG;
     if (dims->B == 0 || total_q == 0 || max_q_len == 0)
         return PKV_OK;

@@ -21,10 +21,10 @@
 //  - one thread issues S = Q K^T (M 128, N 64, K = D in steps of 16; Q and K
 //    K-major) into 64 TMEM columns and commits it to an mbarrier;
 //  - each thread loads its row of S from TMEM, masks keys past its position,
-//    updates its own fp32 online softmax (log2 domain), writes P (bf16) into
-//    shared memory as the K-major A operand, and rescales its row of O in
-//    TMEM only when its max has grown by more than 2^8 (P stays below 2^8
-//    otherwise; l is summed from the same bf16 P);
+//    updates its own fp32 online softmax (log2 domain, the scale folded into
+//    one FFMA per exponent), writes P (bf16) into shared memory as the K-major
+//    A operand, and rescales its row of O in TMEM only when its max has grown
+//    by more than 2^8 (P stays below 2^8 otherwise); l sums the fp32 terms;
 //  - one thread issues O += P V (M 128, N = D, K = 64; V read MN-major, its
 //    rows as they are) into D TMEM columns, then the next tile's S.
 // Descriptors: version 1, no swizzle; leading byte offset = stride between
@@ -345,23 +345,22 @@ __global__ void __launch_bounds__(TcCfg<D>::kThreads, 2) prefill_tc_kernel(const
         // ---- softmax of this row over the tile's 64 keys ----------------
         const int key0 = kt * C::kKeys;
         const bool need_mask = key0 + C::kKeys - 1 > pos_first;
+        // raw scores; the scale (> 0) is applied once to the max and folded
+        // into each exponent's FFMA
         float sv[C::kKeys];
 #pragma unroll
         for (int c0 = 0; c0 < C::kKeys; c0 += 16) {
             float v[16];
             tmem_ld16(t_s + lane_off + c0, v);
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                float x = v[i] * p.scale_log2;
-                if (need_mask && key0 + c0 + i > pos)
-                    x = -INFINITY;
-                sv[c0 + i] = x;
-            }
+            for (int i = 0; i < 16; ++i)
+                sv[c0 + i] = (need_mask && key0 + c0 + i > pos) ? -INFINITY : v[i];
         }
-        float mx = -INFINITY;
+        float mraw = -INFINITY;
 #pragma unroll
         for (int i = 0; i < C::kKeys; ++i)
-            mx = fmaxf(mx, sv[i]);
+            mraw = fmaxf(mraw, sv[i]);
+        const float mx = mraw * p.scale_log2;
         // a new base only when the max grows by more than 2^8 (or first)
         const bool rebase = mx > m_run + 8.f;
         float alpha = 1.f;
@@ -383,18 +382,20 @@ __global__ void __launch_bounds__(TcCfg<D>::kThreads, 2) prefill_tc_kernel(const
             }
             tmem_st_wait();
         }
-        const float base = m_run == -INFINITY ? 0.f : m_run;
+        const float nbase = m_run == -INFINITY ? 0.f : -m_run;
+        const float sl2 = p.scale_log2;
         float lsum = 0.f;
-#pragma unroll
         constexpr int kRest = NI - NI / 2;                // rounds left, kRest | 8
         constexpr int kEvery = (C::kKeys / 8) / kRest;
+#pragma unroll
         for (int c = 0; c < C::kKeys / 8; ++c) {
             uint32_t w[4];
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                w[j] = pack_bf16x2(exp2f(sv[c * 8 + 2 * j] - base),
-                                   exp2f(sv[c * 8 + 2 * j + 1] - base));
-                lsum += bf16_lo(w[j]) + bf16_hi(w[j]);
+                const float e0 = exp2f(fmaf(sv[c * 8 + 2 * j], sl2, nbase));
+                const float e1 = exp2f(fmaf(sv[c * 8 + 2 * j + 1], sl2, nbase));
+                w[j] = pack_bf16x2(e0, e1);
+                lsum += e0 + e1;                      // l from the fp32 terms
             }
             *reinterpret_cast<uint4 *>(p_row + c * 128) = make_uint4(w[0], w[1], w[2], w[3]);
             if (more && (c + 1) % kEvery == 0) {

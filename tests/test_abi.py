@@ -182,3 +182,25 @@ def test_advance_argument_checks():
     d0 = _d(B=0)
     assert L.paged_kv_advance(byref(d0), None, None, None, None, 0, None, None,
                               None) == pkv.PKV_OK
+
+
+def test_prefill_argument_checks():
+    L = pkv.lib()
+    byref = pkv.ctypes.byref
+    fake = 1 << 32
+
+    def call(d, total_q=16, max_q=16, **kw):
+        a = dict(q=fake, qo=fake, k=fake, v=fake, ind=fake, ptr=fake, sl=fake, out=fake, st=None)
+        a.update(kw)
+        return L.paged_prefill_attn(byref(d), a["q"], a["qo"], total_q, max_q, a["k"], a["v"],
+                                    a["ind"], a["ptr"], a["sl"], a["out"], a["st"], None)
+
+    d = _d(B=4)
+    assert call(_d(B=4, scale=0.0)) == pkv.PKV_ERR_INVALID_ARG      # the scale must be > 0
+    assert call(d, total_q=-1) == pkv.PKV_ERR_INVALID_ARG
+    assert call(d, max_q=-1) == pkv.PKV_ERR_INVALID_ARG
+    assert call(d, q=None) == pkv.PKV_ERR_INVALID_ARG
+    assert call(d, out=fake + 8) == pkv.PKV_ERR_INVALID_ARG          # misaligned
+    assert call(d, qo=fake + 2) == pkv.PKV_ERR_INVALID_ARG
+    assert call(_d(B=70000 // 8, Hkv=8)) == pkv.PKV_ERR_UNSUPPORTED  # B * Hkv > 65535
+    assert call(d, total_q=0) == pkv.PKV_OK                           # nothing to do
