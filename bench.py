@@ -61,6 +61,9 @@ def parse_args(argv=None):
                          "through decode_attn_contig")
     ap.add_argument("--no-prefill", action="store_true",
                     help="skip the prefill leg (paged_prefill_attn on three shapes)")
+    ap.add_argument("--only-prefill", default=None,
+                    choices=["all", "prefill_b32_512", "prefill_b4_4096", "extend_b16"],
+                    help="run only the prefill leg on one shape (or all) and print its line")
     ap.add_argument("--no-loop", action="store_true",
                     help="skip the decode-loop leg (paged_kv_advance + step per graph)")
     ap.add_argument("--no-flush", action="store_true", help="skip the L2 flush (not for reporting)")
@@ -307,6 +310,101 @@ def run_reference(args):
                 "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
+    return 0
+
+
+
+# Prefill / extend shapes: the pages' 512-token prompts at the 1B-class head
+# shape, a long prefill, and an extend of 256 new tokens on 2,048-token rows.
+PREFILL_SHAPES = {
+    "prefill_b32_512": ("prefill B=32 x 512 (Hq 32, Hkv 8, D 64)",
+                        dict(B=32, Hq=32, Hkv=8, D=64, page_size=16, seq_lens=[512] * 32,
+                             q_lens=[512] * 32)),
+    "prefill_b4_4096": ("prefill B=4 x 4096 (Hq 32, Hkv 8, D 128)",
+                        dict(B=4, Hq=32, Hkv=8, D=128, page_size=16, seq_lens=[4096] * 4,
+                             q_lens=[4096] * 4)),
+    "extend_b16": ("extend B=16, 256 new of 2048 (Hq 32, Hkv 8, D 128)",
+                   dict(B=16, Hq=32, Hkv=8, D=128, page_size=16, seq_lens=[2048] * 16,
+                        q_lens=[256] * 16)),
+}
+
+
+def prefill_leg(pkv, wl, dev, stream, flush_l2, rank, names, reps=20):
+    """paged_prefill_attn on each named shape: one call per graph replay, the
+    L2 flushed before each, median of `reps`; tensor roofline against the
+    measured dense bf16 peak (burst: each call runs alone)."""
+    import torch
+    tf_peak = load_bf16_peak()
+    out_rows = []
+    for name in names:
+        label, kw = PREFILL_SHAPES[name]
+        c = wl.prefill("prefill", seed=rank, **kw)
+        pt = c.w.to_device(dev)
+        pd = pkv.dims(c.w.B, c.w.Hq, c.w.Hkv, c.w.D, c.w.page_size, pt["k_pool"].shape[0],
+                      int(c.w.kv_indices.numel()), c.w.max_seq_len, c.w.scale)
+        pq, pqo = c.q.to(dev), c.qo_indptr.to(dev)
+        pout = torch.empty(c.total_q, c.w.Hq, c.w.D, dtype=torch.bfloat16, device=dev)
+        pst = torch.zeros(1, dtype=torch.int32, device=dev)
+        max_q = max(kw["q_lens"])
+
+        def prun():
+            pkv.paged_prefill_attn(pd, pq, pqo, pt["k_pool"], pt["v_pool"], pt["kv_indices"],
+                                   pt["kv_indptr"], pt["seq_lens"], pout, status=pst,
+                                   max_q_len=max_q)
+
+        for _ in range(3):
+            prun()
+        pg = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(pg):
+            prun()
+        ms = []
+        for _ in range(reps + 3):
+            flush_l2()
+            a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            pg.replay()
+            e.record(stream)
+            torch.cuda.synchronize(dev)
+            ms.append(a.elapsed_time(e))
+        if int(pst.item()) != 0:
+            raise SystemExit(f"prefill status {int(pst.item()):#x}")
+        us = 1e3 * statistics.median(ms[3:])
+        tf = c.flops() / (us * 1e-6) / 1e12
+        out_rows.append({"shape": label, "us": round(us, 1), "tflops": round(tf, 1),
+                         "roofline": {"bound": "tensor", "achieved": round(tf, 1),
+                                      "peak": tf_peak, "unit": "TFLOP/s",
+                                      "frac": round(tf / tf_peak, 4)},
+                         "flops": c.flops()})
+        del pt, pg
+    return out_rows
+
+
+def run_prefill_only(args):
+    """--only-prefill: the prefill leg alone, one JSON line (for profiling)."""
+    import torch
+    from paged_kv_gqa_16_gb300 import build as pkv_build
+    from paged_kv_gqa_16_gb300 import pkv
+    from paged_kv_gqa_16_gb300 import workloads as wl
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device (the library has no CPU path)")
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    pkv_build.build()
+    pkv.lib()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush_w = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+    flush_r = torch.zeros(max(2 * l2, 256 << 20) // 4, dtype=torch.int32, device=dev)
+    sink = torch.empty((), dtype=torch.int64, device=dev)
+
+    def flush_l2():
+        flush_w.zero_()
+        torch.sum(flush_r, dim=0, out=sink)
+
+    names = list(PREFILL_SHAPES) if args.only_prefill == "all" else [args.only_prefill]
+    rows = prefill_leg(pkv, wl, dev, torch.cuda.current_stream(dev), flush_l2, 0, names,
+                       reps=max(1, args.steps))
+    print(json.dumps({"metric": "paged prefill / extend attention TFLOP/s", "unit": "TFLOP/s",
+                      "n_gpus": 1, "prefill": rows}), flush=True)
     return 0
 
 
@@ -580,64 +678,10 @@ def run_pkv(args):
                         "no flush"}
         del lkp, lvp, lkn, lvn, g_adv, g_noadv
 
-    # prefill / extend: paged_prefill_attn on three shapes, one call per
-    # replay, L2 flushed before each; tensor roofline against the measured
-    # dense bf16 peak (burst: each call runs alone)
+    # prefill / extend: paged_prefill_attn on three shapes (see prefill_leg)
     prefill = None
     if not args.no_prefill and args.layout == "paged":
-        shapes = {
-            "prefill B=32 x 512 (Hq 32, Hkv 8, D 64)":
-                dict(B=32, Hq=32, Hkv=8, D=64, page_size=16, seq_lens=[512] * 32,
-                     q_lens=[512] * 32),
-            "prefill B=4 x 4096 (Hq 32, Hkv 8, D 128)":
-                dict(B=4, Hq=32, Hkv=8, D=128, page_size=16, seq_lens=[4096] * 4,
-                     q_lens=[4096] * 4),
-            "extend B=16, 256 new of 2048 (Hq 32, Hkv 8, D 128)":
-                dict(B=16, Hq=32, Hkv=8, D=128, page_size=16, seq_lens=[2048] * 16,
-                     q_lens=[256] * 16),
-        }
-        tf_peak = load_bf16_peak()
-        prefill = []
-        for label, kw in shapes.items():
-            c = wl.prefill("prefill", seed=rank, **kw)
-            pt = c.w.to_device(dev)
-            pd = pkv.dims(c.w.B, c.w.Hq, c.w.Hkv, c.w.D, c.w.page_size, pt["k_pool"].shape[0],
-                          int(c.w.kv_indices.numel()), c.w.max_seq_len, c.w.scale)
-            pq, pqo = c.q.to(dev), c.qo_indptr.to(dev)
-            pout = torch.empty(c.total_q, c.w.Hq, c.w.D, dtype=torch.bfloat16, device=dev)
-            pst = torch.zeros(1, dtype=torch.int32, device=dev)
-
-            max_q = max(kw["q_lens"])
-
-            def prun():
-                pkv.paged_prefill_attn(pd, pq, pqo, pt["k_pool"], pt["v_pool"], pt["kv_indices"],
-                                       pt["kv_indptr"], pt["seq_lens"], pout, status=pst,
-                                       max_q_len=max_q)
-
-            for _ in range(3):
-                prun()
-            pg = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(pg):
-                prun()
-            ms = []
-            for _ in range(23):
-                flush_l2()
-                a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                a.record(stream)
-                pg.replay()
-                e.record(stream)
-                torch.cuda.synchronize(dev)
-                ms.append(a.elapsed_time(e))
-            if int(pst.item()) != 0:
-                raise SystemExit(f"prefill status {int(pst.item()):#x}")
-            us = 1e3 * statistics.median(ms[3:])
-            tf = c.flops() / (us * 1e-6) / 1e12
-            prefill.append({"shape": label, "us": round(us, 1), "tflops": round(tf, 1),
-                            "roofline": {"bound": "tensor", "achieved": round(tf, 1),
-                                         "peak": tf_peak, "unit": "TFLOP/s",
-                                         "frac": round(tf / tf_peak, 4)},
-                            "flops": c.flops()})
-            del pt, pg
+        prefill = prefill_leg(pkv, wl, dev, stream, flush_l2, rank, list(PREFILL_SHAPES))
 
     # roofline of the dominant kernel, the fused step kernel (its launch is
     # timed as the step call, so the small piece combine is included).
@@ -710,6 +754,8 @@ def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
         return run_reference(args)
+    if args.only_prefill:
+        return run_prefill_only(args)
     return run_pkv(args)
 
 
