@@ -81,6 +81,7 @@ def _load():
         lib.po_combine.argtypes = [I, I, I, I, P, P, P]
         lib.po_advance.argtypes = [I, I, I, I, P, P, P, P, I, P, P, P, P]
         lib.po_prefill.argtypes = [I, I, I, I, I, I, I, P, P, P, P, P, P, P, D, P]
+        lib.po_extend.argtypes = [I, I, I, I, I, I, I, P, P, P, P, P, P, P, P, P, I, D, I]
         lib.po_set_threads.argtypes = [I]
         lib.po_max_threads.restype = I
         _lib = lib
@@ -157,6 +158,33 @@ def append(q, k_new, v_new, k_pool, v_pool, kv_indices, kv_indptr, seq_lens,
                            int(rope_base is not None),
                            float(rope_base or 0.0), int(bool(rope_q)))
     _check(rc, "append")
+    return q, k_pool, v_pool
+
+
+def extend(q, k_new, v_new, qo_indptr, k_pool, v_pool, kv_indices, kv_indptr, seq_lens,
+           *, rope_base: float | None, rope_q: bool):
+    """Return (q', k_pool', v_pool') after writing every row's chunk of new
+    tokens (the last q_len of its seq_lens[b]) at their slots.
+    q [total_q,Hq,D], k_new/v_new [total_q,Hkv,D], pools [P,ps,Hkv,D] (uint16
+    bf16 bits).  Inputs are not modified; copies are returned."""
+    q = _c(q, np.uint16).copy()
+    k_pool = _c(k_pool, np.uint16).copy()
+    v_pool = _c(v_pool, np.uint16).copy()
+    k_new = _c(k_new, np.uint16)
+    v_new = _c(v_new, np.uint16)
+    qo_indptr = _c(qo_indptr, np.int32)
+    kv_indices = _c(kv_indices, np.int32)
+    kv_indptr = _c(kv_indptr, np.int32)
+    seq_lens = _c(seq_lens, np.int32)
+    total_q, Hq, D = q.shape
+    P, ps, Hkv, D2 = k_pool.shape
+    B = len(seq_lens)
+    assert D2 == D and k_new.shape == (total_q, Hkv, D)
+    rc = _load().po_extend(B, Hq, Hkv, D, ps, P, total_q, _ptr(q), _ptr(k_new), _ptr(v_new),
+                           _ptr(qo_indptr), _ptr(k_pool), _ptr(v_pool), _ptr(kv_indices),
+                           _ptr(kv_indptr), _ptr(seq_lens), int(rope_base is not None),
+                           float(rope_base or 0.0), int(bool(rope_q)))
+    _check(rc, "extend")
     return q, k_pool, v_pool
 
 

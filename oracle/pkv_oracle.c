@@ -31,6 +31,7 @@
  *   - commits by author, split-KV decode ("split partials", "single combine
  *       kernel", "compute_num_splits"): per-split partial outputs and
  *       (max, sum) statistics merged by a combine pass.
+ *   - the same appends for a chunk of tokens per row (po_extend).
  *   - same diff, attention_ops.py, attn_paged_prefill / attn_prefill: a
  *       ragged chunk of queries per request, the last of its tokens, each
  *       attending causally up to its own position (po_prefill).
@@ -292,6 +293,74 @@ static long max_len(int B, const int32_t *seq_lens)
         if (seq_lens[b] > mx)
             mx = seq_lens[b];
     return mx;
+}
+
+/* Extend: write a chunk of new tokens per row, the multi-token form of
+ * po_append (compare v1.3.12..6f09b1d, attention_backend.py: the prefill path
+ * stores every new token's K/V at its slot, k_buffer[layer, out_cache_loc];
+ * cache.py: the slot of position pos is page_table[pos / page_size] *
+ * page_size + pos % page_size).  Row b's q_len = qo_indptr[b+1] -
+ * qo_indptr[b] tokens are the last q_len of its L = seq_lens[b]: token i
+ * (input row qo_indptr[b] + i) sits at position L - q_len + i.  K is rotated
+ * by that position (when use_rope), V copied; with rope_q the token's query
+ * heads are rotated the same way, in place.  A row with q_len < 0 or > L, or
+ * a qo_indptr that does not walk from 0 to total_q, is an error. */
+int po_extend(int B, int Hq, int Hkv, int D, int page_size, int num_pages, int total_q,
+              uint16_t *q, const uint16_t *k_new, const uint16_t *v_new,
+              const int32_t *qo_indptr, uint16_t *k_pool, uint16_t *v_pool,
+              const int32_t *kv_indices, const int32_t *kv_indptr, const int32_t *seq_lens,
+              int use_rope, double rope_base, int rope_q)
+{
+    if (qo_indptr[0] != 0 || qo_indptr[B] != total_q)
+        return PO_ERR;
+    double *x = malloc(sizeof(double) * (size_t)D);
+    double *y = malloc(sizeof(double) * (size_t)D);
+    int rc = PO_OK;
+    for (int b = 0; b < B && rc == PO_OK; ++b) {
+        const long L = seq_lens[b];
+        const long q_len = (long)qo_indptr[b + 1] - qo_indptr[b];
+        if (q_len < 0 || q_len > L) {
+            rc = PO_ERR;
+            break;
+        }
+        for (long i = 0; i < q_len && rc == PO_OK; ++i) {
+            const long t = qo_indptr[b] + i;
+            const long pos = L - q_len + i;
+            long page, slot;
+            if (locate(b, pos, page_size, num_pages, kv_indices, kv_indptr, &page, &slot)) {
+                rc = PO_ERR;
+                break;
+            }
+            for (int g = 0; g < Hkv; ++g) {
+                const uint16_t *kin = k_new + (t * Hkv + g) * D;
+                const uint16_t *vin = v_new + (t * Hkv + g) * D;
+                const long off = pool_offset(page, slot, g, page_size, Hkv, D);
+                for (int d = 0; d < D; ++d)
+                    x[d] = po_bf16_to_f64(kin[d]);
+                if (use_rope)
+                    po_rope_rotate(x, y, D, pos, rope_base);
+                else
+                    memcpy(y, x, sizeof(double) * (size_t)D);
+                for (int d = 0; d < D; ++d) {
+                    k_pool[off + d] = po_f64_to_bf16_rne(y[d]);
+                    v_pool[off + d] = vin[d];
+                }
+            }
+            if (use_rope && rope_q) {
+                for (int h = 0; h < Hq; ++h) {
+                    uint16_t *qh = q + (t * Hq + h) * D;
+                    for (int d = 0; d < D; ++d)
+                        x[d] = po_bf16_to_f64(qh[d]);
+                    po_rope_rotate(x, y, D, pos, rope_base);
+                    for (int d = 0; d < D; ++d)
+                        qh[d] = po_f64_to_bf16_rne(y[d]);
+                }
+            }
+        }
+    }
+    free(x);
+    free(y);
+    return rc;
 }
 
 /* out[b, h, :] = softmax(q[b,h] K_{b,g}^T * scale) V_{b,g}, g = h / (Hq/Hkv),

@@ -569,3 +569,68 @@ def test_prefill_special_cases():
     with pytest.raises(ValueError):
         oracle.prefill(q, np.array([0, 13, 14, 18], np.int32), kp, vp, idx, ptr, sl,
                        scale=c.w.scale)
+
+
+# --------------------------------------------------------------- extend ---
+def _extend_case(lens, qls, ps, seed, Hq=4, Hkv=2, D=16):
+    """Pools with NaN in every chunk slot (the tokens about to be written),
+    chunk K/V and q drawn separately."""
+    c = wl.prefill("ext", B=len(lens), Hq=Hq, Hkv=Hkv, D=D, page_size=ps, seq_lens=lens,
+                   q_lens=qls, seed=seed)
+    kp, vp = c.w.full_pool_host()
+    idx, ptr = c.w.host("kv_indices"), c.w.host("kv_indptr")
+    slots = []
+    for b, (L, n) in enumerate(zip(lens, qls)):
+        for i in range(n):
+            pos = L - n + i
+            slots.append((idx[ptr[b] + pos // ps], pos % ps, pos))
+    for page, slot, _ in slots:
+        kp[page, slot] = wl.NAN_BF16_BITS
+        vp[page, slot] = wl.NAN_BF16_BITS
+    g = torch.Generator().manual_seed(seed + 1)
+    total = int(c.qo_indptr[-1])
+    bits = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16)
+    k_new = bits(torch.randn(total, Hkv, D, generator=g).to(torch.bfloat16))
+    v_new = bits(torch.randn(total, Hkv, D, generator=g).to(torch.bfloat16))
+    q = bits(c.q)
+    return c, q, k_new, v_new, kp, vp, idx, ptr, slots
+
+
+def test_extend_writes_exactly_the_chunk_slots():
+    lens, qls, ps = [6, 3, 9, 0], [3, 3, 1, 0], 4
+    c, q, kn, vn, kp, vp, idx, ptr, slots = _extend_case(lens, qls, ps, seed=3)
+    q2, kp2, vp2 = oracle.extend(q, kn, vn, c.qo_indptr.numpy(), kp, vp, idx, ptr,
+                                 c.w.host("seq_lens"), rope_base=10000.0, rope_q=False)
+    assert np.array_equal(q2, q)
+    assert len(np.argwhere(kp2 != kp)) == len(slots) * 2 * 16     # NaN -> finite, all of it
+    assert len(np.argwhere(vp2 != vp)) == len(slots) * 2 * 16
+    for t, (page, slot, pos) in enumerate(slots):
+        assert np.array_equal(vp2[page, slot], vn[t])              # V copied
+        kf = oracle.bf16_to_f64(kn[t])
+        for gg in range(2):
+            want = _torch_complex_rope(kf[gg], pos, 10000.0)
+            got = oracle.bf16_to_f64(kp2[page, slot, gg])
+            assert np.all(np.abs(got - want) <= np.abs(want) * 2.0**-8 + 1e-30)
+        if pos == 0:
+            assert np.array_equal(kp2[page, slot], kn[t])          # angle 0: identity
+
+
+def test_extend_one_token_is_append_and_rotates_q():
+    lens, ps = [5, 1, 12], 4
+    c, q, kn, vn, kp, vp, idx, ptr, slots = _extend_case(lens, [1, 1, 1], ps, seed=4)
+    e = oracle.extend(q, kn, vn, c.qo_indptr.numpy(), kp, vp, idx, ptr, c.w.host("seq_lens"),
+                      rope_base=10000.0, rope_q=True)
+    a = oracle.append(q, kn, vn, kp, vp, idx, ptr, c.w.host("seq_lens"), rope_base=10000.0,
+                      rope_q=True)
+    for x, y in zip(e, a):
+        assert np.array_equal(x, y)
+    # the chunk's query heads are rotated by their token's position
+    qf = oracle.bf16_to_f64(q)
+    for t, (_, _, pos) in enumerate(slots):
+        for h in range(4):
+            want = _torch_complex_rope(qf[t, h], pos, 10000.0)
+            got = oracle.bf16_to_f64(e[0][t, h])
+            assert np.all(np.abs(got - want) <= np.abs(want) * 2.0**-8 + 1e-30)
+    with pytest.raises(ValueError):                                 # chunk longer than its row
+        oracle.extend(q, kn, vn, np.array([0, 1, 3, 3], np.int32), kp, vp, idx, ptr,
+                      c.w.host("seq_lens"), rope_base=None, rope_q=False)
