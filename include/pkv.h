@@ -240,6 +240,26 @@ pkv_status paged_prefill_attn(const pkv_dims *dims, const void *q, const int32_t
                               const int32_t *seq_lens, void *out, uint32_t *status,
                               pkv_stream_t stream);
 
+/* Extend: the K/V write of a prefill / extend chunk, the multi-token form of
+ * paged_kv_append (compare v1.3.12..6f09b1d, attention_backend.py: the
+ * prefill path stores every new token's K/V at its slot).  Row b's
+ * q_len = qo_indptr[b+1] - qo_indptr[b] new tokens are the last q_len of its
+ * L = seq_lens[b] (seq_lens already count them): token i of the chunk (input
+ * row qo_indptr[b] + i of k_new / v_new [total_q, Hkv, D] and q
+ * [total_q, Hq, D]) sits at position L - q_len + i.  K is rotated by that
+ * position as paged_kv_append does, V copied, both stored at the token's
+ * slot; with rope_q its query heads are rotated in place (q may be NULL
+ * otherwise).  A row with q_len < 0 or > L, or L > max_seq_len, sets
+ * PKV_FLAG_BAD_LEN and writes nothing; page and position errors as for
+ * paged_kv_append.  One block per new token; graph-capturable.  Followed by
+ * paged_prefill_attn on the same chunks, it is the whole extend step. */
+pkv_status paged_kv_extend(const pkv_dims *dims, void *q, const void *k_new, const void *v_new,
+                           const int32_t *qo_indptr, int total_q, void *k_pool, void *v_pool,
+                           const int32_t *kv_indices, const int32_t *kv_indptr,
+                           const int32_t *seq_lens, const float *rope_cos_sin,
+                           int rope_max_pos, int rope_q, uint32_t *status,
+                           pkv_stream_t stream);
+
 /* ---- contiguous K/V cache -------------------------------------------------- */
 
 /* Decode (or, with k_new/v_new, the whole decode step) over a contiguous

@@ -306,6 +306,53 @@ pkv_status launch_append(const pkv_dims *dims, void *q, const void *k_new, const
 
 } // namespace
 
+extern "C" pkv_status paged_kv_extend(const pkv_dims *dims, void *q, const void *k_new,
+                                      const void *v_new, const int32_t *qo_indptr, int total_q,
+                                      void *k_pool, void *v_pool, const int32_t *kv_indices,
+                                      const int32_t *kv_indptr, const int32_t *seq_lens,
+                                      const float *rope_cos_sin, int rope_max_pos, int rope_q,
+                                      uint32_t *status, pkv_stream_t stream)
+{
+    pkv_status st = check_dims(dims);
+    if (st != PKV_OK)
+        return st;
+    if (total_q < 0)
+        return PKV_ERR_INVALID_ARG;
+    if (dims->B == 0 || total_q == 0)
+        return PKV_OK;
+    if (qo_indptr == nullptr || !aligned(qo_indptr, 4))
+        return PKV_ERR_INVALID_ARG;
+    // the same checks as the one-token append (q, pools, tables, RoPE table)
+    st = check_append_args(dims, q, k_new, v_new, k_pool, v_pool, kv_indices, kv_indptr,
+                           seq_lens, rope_cos_sin, rope_max_pos, rope_q, status);
+    if (st != PKV_OK)
+        return st;
+    pkv::AppendParams p{};
+    p.q = static_cast<__nv_bfloat16 *>(q);
+    p.k_new = static_cast<const __nv_bfloat16 *>(k_new);
+    p.v_new = static_cast<const __nv_bfloat16 *>(v_new);
+    p.k_pool = static_cast<__nv_bfloat16 *>(k_pool);
+    p.v_pool = static_cast<__nv_bfloat16 *>(v_pool);
+    p.kv_indices = kv_indices;
+    p.kv_indptr = kv_indptr;
+    p.seq_lens = seq_lens;
+    p.rope = rope_cos_sin;
+    p.status = status;
+    p.B = dims->B;
+    p.Hq = dims->Hq;
+    p.Hkv = dims->Hkv;
+    p.D = dims->D;
+    p.page_size = dims->page_size;
+    p.num_pages = dims->num_pages;
+    p.num_indices = dims->num_indices;
+    p.max_seq_len = dims->max_seq_len;
+    p.rope_max_pos = rope_max_pos;
+    p.rope_q = rope_q ? 1 : 0;
+    p.qo_indptr = qo_indptr;
+    p.total_q = total_q;
+    return launch_status(pkv::launch_extend(p, (cudaStream_t)stream));
+}
+
 extern "C" {
 
 int pkv_version(void)

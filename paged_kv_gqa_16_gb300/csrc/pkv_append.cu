@@ -12,9 +12,10 @@
 // interleaved pair is multiplied by the unit complex number (cos, sin) of
 // pos * theta_i.
 //
-// Layout of the work: one block per row; each thread moves 16-byte vectors
-// (8 bf16 = 4 rotation pairs) of the row's Hkv K/V head vectors and, when
-// asked, its Hq query heads.  The row's page lookup happens once per block.
+// Layout of the work: one block per row (append) or per new token (extend);
+// each thread moves 16-byte vectors (8 bf16 = 4 rotation pairs) of the
+// token's Hkv K/V head vectors and, when asked, its Hq query heads.  The page
+// lookup happens once per block.
 #include "pkv_device.cuh"
 #include "pkv_internal.h"
 
@@ -22,19 +23,11 @@ namespace pkv {
 
 namespace {
 
-__global__ void __launch_bounds__(128) append_kernel(const AppendParams p)
+// One token: row b, position pos; its K/V (and, with rope_q, its query
+// heads) are input row t of k_new / v_new / q.  Page lookup, checks, K
+// rotated by pos, V copied, both stored at the token's slot.
+__device__ __forceinline__ void write_token(const AppendParams &p, int b, int pos, size_t t)
 {
-    // the decode launched next may start its prologue; it waits for this
-    // grid's completion before it reads q or the pools
-    grid_launch_dependents();
-    const int b = blockIdx.x;
-    const int L = p.seq_lens[b];
-    if (L <= 0) {
-        if (L < 0 && p.status != nullptr && threadIdx.x == 0)
-            atomicOr(p.status, kFlagBadLen);
-        return;
-    }
-    const int pos = L - 1;
     const int pg0 = p.kv_indptr[b], pg1 = p.kv_indptr[b + 1];
     unsigned bad = 0;
     int page = 0;
@@ -59,8 +52,8 @@ __global__ void __launch_bounds__(128) append_kernel(const AppendParams p)
     const size_t row_off = ((size_t)page * p.page_size + slot) * (size_t)p.Hkv * D;
     const float *cs = p.rope != nullptr ? p.rope + (size_t)pos * D : nullptr;
 
-    const uint4 *kin = reinterpret_cast<const uint4 *>(p.k_new + (size_t)b * p.Hkv * D);
-    const uint4 *vin = reinterpret_cast<const uint4 *>(p.v_new + (size_t)b * p.Hkv * D);
+    const uint4 *kin = reinterpret_cast<const uint4 *>(p.k_new + t * p.Hkv * D);
+    const uint4 *vin = reinterpret_cast<const uint4 *>(p.v_new + t * p.Hkv * D);
     uint4 *kout = reinterpret_cast<uint4 *>(p.k_pool + row_off);
     uint4 *vout = reinterpret_cast<uint4 *>(p.v_pool + row_off);
     for (int it = threadIdx.x; it < p.Hkv * vpr; it += blockDim.x) {
@@ -74,13 +67,55 @@ __global__ void __launch_bounds__(128) append_kernel(const AppendParams p)
         vout[it] = vin[it];
     }
     if (cs != nullptr && p.rope_q) {
-        uint4 *qrow = reinterpret_cast<uint4 *>(p.q + (size_t)b * p.Hq * D);
+        uint4 *qrow = reinterpret_cast<uint4 *>(p.q + t * p.Hq * D);
         for (int it = threadIdx.x; it < p.Hq * vpr; it += blockDim.x) {
             const int c = it % vpr;
             const float4 *c4 = reinterpret_cast<const float4 *>(cs + 8 * c);
             qrow[it] = rotate_pairs8(qrow[it], c4[0], c4[1]);
         }
     }
+}
+
+__global__ void __launch_bounds__(128) append_kernel(const AppendParams p)
+{
+    // the decode launched next may start its prologue; it waits for this
+    // grid's completion before it reads q or the pools
+    grid_launch_dependents();
+    const int b = blockIdx.x;
+    const int L = p.seq_lens[b];
+    if (L <= 0) {
+        if (L < 0 && p.status != nullptr && threadIdx.x == 0)
+            atomicOr(p.status, kFlagBadLen);
+        return;
+    }
+    write_token(p, b, L - 1, (size_t)b);
+}
+
+// Extend: one block per new token t of the flattened chunks.  Its row is the
+// last b with qo_indptr[b] <= t; row b's chunk is the last q_len of its L
+// tokens, so token t sits at position L - q_len + (t - qo_indptr[b]).
+__global__ void __launch_bounds__(128) extend_kernel(const AppendParams p)
+{
+    grid_launch_dependents();
+    const int t = blockIdx.x;
+    int lo = 0, hi = p.B - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (p.qo_indptr[mid] <= t)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    const int b = lo;
+    const int a = p.qo_indptr[b], e = p.qo_indptr[b + 1];
+    const int L = p.seq_lens[b];
+    const int q_len = e - a;
+    if (t < a || t >= e || q_len > L || L > p.max_seq_len) {
+        if (p.status != nullptr && threadIdx.x == 0)
+            atomicOr(p.status, kFlagBadLen);
+        return;
+    }
+    write_token(p, b, L - q_len + (t - a), (size_t)t);
 }
 
 // (cos, sin) of pos * base^(-2i/D), in double, rounded once to fp32.
@@ -104,6 +139,14 @@ __global__ void rope_table_kernel(float *cos_sin, int max_pos, int half, double 
 cudaError_t launch_append(const AppendParams &p, cudaStream_t stream)
 {
     append_kernel<<<p.B, 128, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_extend(const AppendParams &p, cudaStream_t stream)
+{
+    if (p.total_q <= 0)
+        return cudaSuccess;
+    extend_kernel<<<p.total_q, 128, 0, stream>>>(p);
     return cudaGetLastError();
 }
 

@@ -22,6 +22,8 @@ struct AppendParams {
     uint32_t *status;      // nullable
     int B, Hq, Hkv, D, page_size, num_pages, num_indices, max_seq_len;
     int rope_max_pos, rope_q;
+    const int32_t *qo_indptr;  // extend: [B+1] chunk offsets (append: unused)
+    int total_q;               // extend: tokens in all chunks
 };
 
 struct DecodeParams {
@@ -122,6 +124,7 @@ struct CombineParams {
 };
 
 cudaError_t launch_append(const AppendParams &p, cudaStream_t stream);
+cudaError_t launch_extend(const AppendParams &p, cudaStream_t stream);
 cudaError_t launch_advance(const AdvanceParams &p, cudaStream_t stream);
 // grid: (ceil(max_q_len / tq), B * Hkv)
 cudaError_t launch_prefill(const PrefillParams &p, int D, int max_q_len, cudaStream_t stream);

@@ -37,7 +37,7 @@ EXPORTS = (
     "pkv_workspace_init", "pkv_rope_table", "paged_kv_append", "paged_decode_attn",
     "paged_decode_step", "paged_decode_partials", "decode_combine", "pkv_status_str",
     "pkv_version", "paged_decode_attn_noalloc", "paged_kv_advance", "decode_attn_contig",
-    "paged_prefill_attn",
+    "paged_prefill_attn", "paged_kv_extend",
 )
 
 
@@ -92,6 +92,7 @@ def lib():
             "paged_kv_advance": (I, [DP, P, P, P, P, I, P, P, P]),
             "decode_attn_contig": (I, [DP, P, P, P, P, P, P, P, P, I, I, P, Z, P, P]),
             "paged_prefill_attn": (I, [DP, P, P, I, I, P, P, P, P, P, P, P, P]),
+            "paged_kv_extend": (I, [DP, P, P, P, P, I, P, P, P, P, P, P, I, I, P, P]),
             "pkv_status_str": (ctypes.c_char_p, [I]),
             "pkv_version": (I, []),
         }
@@ -242,6 +243,18 @@ def paged_prefill_attn(d: Dims, q, qo_indptr, k_pool, v_pool, kv_indices, kv_ind
         total_q if max_q_len is None else int(max_q_len), _ptr(k_pool), _ptr(v_pool),
         _ptr(kv_indices), _ptr(kv_indptr), _ptr(seq_lens), _ptr(out), _ptr(status),
         _stream(stream)))
+
+
+def paged_kv_extend(d: Dims, q, k_new, v_new, qo_indptr, k_pool, v_pool, kv_indices, kv_indptr,
+                    seq_lens, rope_cos_sin=None, rope_max_pos: int = 0, rope_q: bool = False,
+                    status=None, stream=None) -> None:
+    """Write every row's chunk of new tokens (the last q_len of its seq_lens)
+    at their slots: K rotated by position, V copied, q rotated if rope_q."""
+    total_q = int(k_new.shape[0])
+    _check("paged_kv_extend", lib().paged_kv_extend(
+        ctypes.byref(d), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(qo_indptr), total_q,
+        _ptr(k_pool), _ptr(v_pool), _ptr(kv_indices), _ptr(kv_indptr), _ptr(seq_lens),
+        _ptr(rope_cos_sin), rope_max_pos, int(bool(rope_q)), _ptr(status), _stream(stream)))
 
 
 NOALLOC_SCRATCH_BYTES = 16 << 20
