@@ -631,6 +631,15 @@ def run_pkv(args):
         lout = torch.empty(w.B, w.Hq, w.D, dtype=torch.bfloat16, device=dev)
 
         def one(st, adv):
+            if adv == "fused":
+                # the loop opens with one advance; each step then advances
+                # for the next inside its own combine launch
+                if st == 0:
+                    pkv.paged_kv_advance(ld, lsl, lptr, lind, lfree, lhead, status=lws)
+                pkv.paged_decode_step_advance(ld, lq, lkn[st], lvn[st], lkp, lvp, lind, lptr,
+                                              lsl, lrope, ls.max_seq_len, lS, lws, lout,
+                                              lfree, lhead)
+                return
             if adv:
                 pkv.paged_kv_advance(ld, lsl, lptr, lind, lfree, lhead, status=lws)
             pkv.paged_decode_step(ld, lq, lkn[st], lvn[st], lkp, lvp, lind, lptr, lsl, lrope,
@@ -663,9 +672,10 @@ def run_pkv(args):
                 ms.append(a.elapsed_time(b) / LOOP)
             return statistics.median(ms[3:])
 
-        g_adv, g_noadv = loop_graph(True), loop_graph(False)
+        g_adv, g_noadv, g_fused = loop_graph(True), loop_graph(False), loop_graph("fused")
         ms_adv = loop_timed(g_adv)
         pages_taken = int(lhead.item())
+        ms_fused = loop_timed(g_fused)
         ms_noadv = loop_timed(g_noadv)
         if pkv.status_word(lws) != 0:
             raise SystemExit(f"device status {pkv.status_word(lws):#x} after the loop leg")
@@ -673,10 +683,13 @@ def run_pkv(args):
                 "us_per_step": round(1e3 * ms_adv, 2),
                 "us_per_step_without_advance": round(1e3 * ms_noadv, 2),
                 "advance_us": round(1e3 * (ms_adv - ms_noadv), 2),
+                "us_per_step_fused_advance": round(1e3 * ms_fused, 2),
+                "fused_advance_us": round(1e3 * (ms_fused - ms_noadv), 2),
                 "pages_taken_per_replay": pages_taken,
                 "note": "same rows; table strided with room to grow; steps back to back, "
-                        "no flush"}
-        del lkp, lvp, lkn, lvn, g_adv, g_noadv
+                        "no flush; fused: paged_decode_step_advance (its graph holds one "
+                        "extra advance launch, counted in its per-step time)"}
+        del lkp, lvp, lkn, lvn, g_adv, g_noadv, g_fused
 
     # prefill / extend: paged_prefill_attn on three shapes (see prefill_leg)
     prefill = None

@@ -322,6 +322,27 @@ pkv_status paged_kv_advance(const pkv_dims *dims, int32_t *seq_lens,
                             const int32_t *free_pages, int num_free, int32_t *free_head,
                             uint32_t *status, pkv_stream_t stream);
 
+/* paged_decode_step followed by paged_kv_advance, for a decode loop: the
+ * step attends and appends at the current seq_lens, then the metadata moves
+ * on to the next step's token (the same two host steps of the pages as
+ * paged_kv_advance, run after the step instead of before it).  Results are
+ * bit-identical to the two calls in that order.  Arguments are those of the
+ * two calls; the advance's PKV_FLAG_* bits go to the workspace status word.
+ * On the persistent path with num_splits > 1 the advance is one extra block
+ * of the piece-combine launch (that launch starts after the decode grid has
+ * completed, and its other blocks never read the metadata), so the step
+ * stays two launches; otherwise it is paged_decode_step plus the one-block
+ * advance launch.  A loop starts with one paged_kv_advance and then calls
+ * this once per step; the state after K of these calls is that after K + 1
+ * advances and K steps.  Graph-capturable. */
+pkv_status paged_decode_step_advance(const pkv_dims *dims, const void *q, const void *k_new,
+                                     const void *v_new, void *k_pool, void *v_pool,
+                                     int32_t *kv_indices, const int32_t *kv_indptr,
+                                     int32_t *seq_lens, const float *rope_cos_sin,
+                                     int rope_max_pos, int num_splits, void *workspace,
+                                     size_t ws_bytes, void *out, const int32_t *free_pages,
+                                     int num_free, int32_t *free_head, pkv_stream_t stream);
+
 /* ---- for callers that cannot allocate ------------------------------------ */
 
 /* Size of the library-held scratch used by paged_decode_attn_noalloc. */

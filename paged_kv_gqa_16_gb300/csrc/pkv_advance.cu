@@ -10,20 +10,20 @@
 // place.  Here pos = seq_lens[b] for every row with seq_lens[b] > 0, and the
 // allocator is a device free list consumed in row order.
 //
-// Layout of the work: one block of 1024 threads walks the rows 1024 at a
-// time.  Each thread decides for its row whether it wants a page; a block
-// scan of those wants gives each row its rank, so row b takes
-// free_pages[head + rank], the same assignment a sequential walk in
-// increasing b makes.  Each thread reads and writes only its own row.
-#include "pkv_device.cuh"
-#include "pkv_internal.h"
+// Layout of the work: one block (advance_block, pkv_advance.cuh): its
+// threads walk the rows a block at a time.  Each thread decides for its row
+// whether it wants a page; a block scan of those wants gives each row its
+// rank, so row b takes free_pages[head + rank], the same assignment a
+// sequential walk in increasing b makes.  Each thread reads and writes only
+// its own row.  The same block also runs inside the piece combine of
+// paged_decode_step_advance.
+#include "pkv_advance.cuh"
 
 namespace pkv {
 
 namespace {
 
 constexpr int kAdvanceThreads = 1024;
-constexpr unsigned kAll = 0xffffffffu;
 
 __global__ void __launch_bounds__(kAdvanceThreads) advance_kernel(const AdvanceParams p)
 {
@@ -31,75 +31,7 @@ __global__ void __launch_bounds__(kAdvanceThreads) advance_kernel(const AdvanceP
     // may start its prologue and waits for this grid before reading them
     grid_dependency_wait();
     grid_launch_dependents();
-    __shared__ int s_warp[kAdvanceThreads / 32];
-    __shared__ unsigned s_flags;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    if (threadIdx.x == 0)
-        s_flags = 0u;
-    const int head = *p.free_head;
-    int taken = 0;                                    // wants in earlier chunks
-    unsigned flags = 0u;
-    for (int base = 0; base < p.B; base += kAdvanceThreads) {
-        const int b = base + (int)threadIdx.x;
-        const int L = b < p.B ? p.seq_lens[b] : 0;
-        const int pos = L;
-        bool advance = L > 0;
-        bool want = false;
-        int slot = -1;
-        if (advance && pos >= p.max_seq_len) {
-            flags |= kFlagBadLen;
-            advance = false;
-        }
-        if (advance && pos % p.page_size == 0) {
-            const int pg0 = p.kv_indptr[b], pg1 = p.kv_indptr[b + 1];
-            const int idx = pos / p.page_size;
-            if (pg0 < 0 || pg1 < pg0 || pg1 > p.num_indices) {
-                flags |= kFlagBadPage;
-                advance = false;
-            } else if (idx >= pg1 - pg0) {
-                flags |= kFlagNoPage;                 // the row's table is full
-                advance = false;
-            } else {
-                want = true;
-                slot = pg0 + idx;
-            }
-        }
-        // exclusive scan of the wants over the chunk, in row order
-        const unsigned bal = __ballot_sync(kAll, want);
-        const int in_warp = __popc(bal & ((1u << lane) - 1u));
-        if (lane == 0)
-            s_warp[warp] = __popc(bal);
-        __syncthreads();
-        int before = 0, chunk_total = 0;
-        for (int w = 0; w < kAdvanceThreads / 32; ++w) {
-            const int c = s_warp[w];
-            before += w < warp ? c : 0;
-            chunk_total += c;
-        }
-        __syncthreads();                              // s_warp is rewritten next chunk
-        if (want) {
-            const long long k = (long long)head + taken + before + in_warp;
-            if (k < p.num_free) {
-                p.kv_indices[slot] = p.free_pages[k];
-            } else {
-                flags |= kFlagNoPage;                 // the free list ran out
-                advance = false;
-            }
-        }
-        if (advance)
-            p.seq_lens[b] = pos + 1;
-        taken += chunk_total;
-    }
-    if (flags != 0u)
-        atomicOr(&s_flags, flags);
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        const long long left = (long long)p.num_free - head;
-        const long long got = taken < left ? taken : (left > 0 ? left : 0);
-        *p.free_head = head + (int)got;
-        if (s_flags != 0u && p.status != nullptr)
-            atomicOr(p.status, s_flags);
-    }
+    advance_block(p);
 }
 
 // A contiguous cache [num_slots, cache_len, Hkv, D] read through cache_batch_idx

@@ -199,7 +199,7 @@ pkv_status launch_persistent(const pkv_dims *dims, const void *q, const void *k_
                              const int32_t *kv_indptr, const int32_t *seq_lens,
                              int num_splits, void *workspace, void *out, const void *k_new,
                              const void *v_new, const float *rope, int rope_max_pos,
-                             pkv_stream_t stream)
+                             pkv_stream_t stream, const pkv::AdvanceParams *adv = nullptr)
 {
     const Layout L = layout_for(dims, num_splits);
     char *ws = static_cast<char *>(workspace);
@@ -248,6 +248,8 @@ pkv_status launch_persistent(const pkv_dims *dims, const void *q, const void *k_
     c.Bv = L.Bv;
     c.Hq = dims->Hq;
     c.HQV = L.HQV;
+    if (adv != nullptr)
+        c.adv = *adv;
     return launch_status(
         pkv::launch_piece_combine(c, dims->D, num_splits, (cudaStream_t)stream));
 }
@@ -304,6 +306,43 @@ pkv_status launch_append(const pkv_dims *dims, void *q, const void *k_new, const
     return launch_status(pkv::launch_append(p, (cudaStream_t)stream));
 }
 
+pkv_status check_advance_args(const pkv_dims *dims, const int32_t *seq_lens,
+                              const int32_t *kv_indptr, const int32_t *kv_indices,
+                              const int32_t *free_pages, int num_free, const int32_t *free_head,
+                              const uint32_t *status)
+{
+    if (seq_lens == nullptr || kv_indptr == nullptr || free_head == nullptr || num_free < 0 ||
+        (num_free > 0 && free_pages == nullptr) ||
+        (dims->num_indices > 0 && kv_indices == nullptr))
+        return PKV_ERR_INVALID_ARG;
+    if (!aligned(seq_lens, 4) || !aligned(kv_indptr, 4) || !aligned(free_head, 4) ||
+        (kv_indices != nullptr && !aligned(kv_indices, 4)) ||
+        (free_pages != nullptr && !aligned(free_pages, 4)) ||
+        (status != nullptr && !aligned(status, 4)))
+        return PKV_ERR_INVALID_ARG;
+    return PKV_OK;
+}
+
+pkv::AdvanceParams advance_params(const pkv_dims *dims, int32_t *seq_lens,
+                                  const int32_t *kv_indptr, int32_t *kv_indices,
+                                  const int32_t *free_pages, int num_free, int32_t *free_head,
+                                  uint32_t *status)
+{
+    pkv::AdvanceParams p{};
+    p.seq_lens = seq_lens;
+    p.kv_indptr = kv_indptr;
+    p.kv_indices = kv_indices;
+    p.free_pages = free_pages;
+    p.free_head = free_head;
+    p.status = status;
+    p.B = dims->B;
+    p.page_size = dims->page_size;
+    p.max_seq_len = dims->max_seq_len;
+    p.num_indices = dims->num_indices;
+    p.num_free = num_free;
+    return p;
+}
+
 } // namespace
 
 extern "C" pkv_status paged_kv_extend(const pkv_dims *dims, void *q, const void *k_new,
@@ -357,7 +396,7 @@ extern "C" {
 
 int pkv_version(void)
 {
-    return (1 << 16) | 2;
+    return (1 << 16) | 3;
 }
 
 const char *pkv_status_str(pkv_status s)
@@ -482,27 +521,12 @@ pkv_status paged_kv_advance(const pkv_dims *dims, int32_t *seq_lens, const int32
         return st;
     if (dims->B == 0)
         return PKV_OK;
-    if (seq_lens == nullptr || kv_indptr == nullptr || free_head == nullptr || num_free < 0 ||
-        (num_free > 0 && free_pages == nullptr) ||
-        (dims->num_indices > 0 && kv_indices == nullptr))
-        return PKV_ERR_INVALID_ARG;
-    if (!aligned(seq_lens, 4) || !aligned(kv_indptr, 4) || !aligned(free_head, 4) ||
-        (kv_indices != nullptr && !aligned(kv_indices, 4)) ||
-        (free_pages != nullptr && !aligned(free_pages, 4)) ||
-        (status != nullptr && !aligned(status, 4)))
-        return PKV_ERR_INVALID_ARG;
-    pkv::AdvanceParams p{};
-    p.seq_lens = seq_lens;
-    p.kv_indptr = kv_indptr;
-    p.kv_indices = kv_indices;
-    p.free_pages = free_pages;
-    p.free_head = free_head;
-    p.status = status;
-    p.B = dims->B;
-    p.page_size = dims->page_size;
-    p.max_seq_len = dims->max_seq_len;
-    p.num_indices = dims->num_indices;
-    p.num_free = num_free;
+    st = check_advance_args(dims, seq_lens, kv_indptr, kv_indices, free_pages, num_free,
+                            free_head, status);
+    if (st != PKV_OK)
+        return st;
+    const pkv::AdvanceParams p = advance_params(dims, seq_lens, kv_indptr, kv_indices,
+                                                free_pages, num_free, free_head, status);
     return launch_status(pkv::launch_advance(p, (cudaStream_t)stream));
 }
 
@@ -565,6 +589,43 @@ pkv_status paged_decode_step(const pkv_dims *dims, const void *q, const void *k_
     if (st != PKV_OK || direct)
         return st;
     return launch_combine_split(dims, num_splits, workspace, out, stream);
+}
+
+pkv_status paged_decode_step_advance(const pkv_dims *dims, const void *q, const void *k_new,
+                                     const void *v_new, void *k_pool, void *v_pool,
+                                     int32_t *kv_indices, const int32_t *kv_indptr,
+                                     int32_t *seq_lens, const float *rope_cos_sin,
+                                     int rope_max_pos, int num_splits, void *workspace,
+                                     size_t ws_bytes, void *out, const int32_t *free_pages,
+                                     int num_free, int32_t *free_head, pkv_stream_t stream)
+{
+    pkv_status st = check_decode_args(dims, q, k_pool, v_pool, kv_indices, kv_indptr,
+                                      seq_lens, num_splits, workspace, ws_bytes, out, true);
+    if (st != PKV_OK || dims->B == 0)
+        return st;
+    uint32_t *status = static_cast<uint32_t *>(workspace);
+    st = check_append_args(dims, q, k_new, v_new, k_pool, v_pool, kv_indices, kv_indptr,
+                           seq_lens, rope_cos_sin, rope_max_pos, 0, status);
+    if (st != PKV_OK)
+        return st;
+    st = check_advance_args(dims, seq_lens, kv_indptr, kv_indices, free_pages, num_free,
+                            free_head, status);
+    if (st != PKV_OK)
+        return st;
+    const pkv::AdvanceParams adv = advance_params(dims, seq_lens, kv_indptr, kv_indices,
+                                                  free_pages, num_free, free_head, status);
+    // The piece combine runs after the decode grid has completed and never
+    // reads the metadata, so one extra block of it can advance that metadata.
+    if (fused_path_ok(dims) && num_splits > 1)
+        return launch_persistent(dims, q, k_pool, v_pool, kv_indices, kv_indptr, seq_lens,
+                                 num_splits, workspace, out, k_new, v_new, rope_cos_sin,
+                                 rope_max_pos, stream, &adv);
+    st = paged_decode_step(dims, q, k_new, v_new, k_pool, v_pool, kv_indices, kv_indptr,
+                           seq_lens, rope_cos_sin, rope_max_pos, num_splits, workspace,
+                           ws_bytes, out, stream);
+    if (st != PKV_OK)
+        return st;
+    return launch_status(pkv::launch_advance(adv, (cudaStream_t)stream));
 }
 
 pkv_status decode_attn_contig(const pkv_dims *dims, const void *q, const void *k_new,

@@ -32,8 +32,7 @@
 //    the piece combine kernel merges each row's consecutive pieces.
 #include <cmath>
 
-#include "pkv_device.cuh"
-#include "pkv_internal.h"
+#include "pkv_advance.cuh"
 
 namespace pkv {
 
@@ -685,6 +684,12 @@ __global__ void __launch_bounds__(WPH > 8 ? 32 * WPH : 256)
     __shared__ float s_m[NWARP], s_den[NWARP];
     __shared__ float s_acc[NWARP][D];
     grid_dependency_wait();
+    // paged_decode_step_advance: the last block advances the metadata for the
+    // next step; the decode grid, the only reader of it, has completed
+    if (p.adv.seq_lens != nullptr && blockIdx.x == gridDim.x - 1) {
+        advance_block(p.adv);
+        return;
+    }
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int grp = warp / WPH, wi = warp % WPH;
@@ -879,7 +884,8 @@ cudaError_t launch_piece_combine(const PieceCombineParams &p, int D, int grid_bl
     const long long pairs = (long long)p.Bv * p.HQV;
     const int warps = wph > 8 ? wph : 8;
     const int groups = warps / wph;
-    const unsigned blocks = (unsigned)((pairs + groups - 1) / groups);
+    const unsigned blocks = (unsigned)((pairs + groups - 1) / groups) +
+                            (p.adv.seq_lens != nullptr ? 1u : 0u);
     cudaError_t e;
 #define PKV_COMBINE_CASE(DD, W)                                                              \
     e = launch_pdl(piece_combine_kernel<DD, W>, dim3(blocks), dim3(warps * 32), 0, stream, p)

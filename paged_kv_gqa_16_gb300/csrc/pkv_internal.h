@@ -114,6 +114,9 @@ struct PieceCombineParams {
     const int32_t *row_info;
     __nv_bfloat16 *out;
     int B, Bv, Hq, HQV;
+    // paged_decode_step_advance: one extra block runs the metadata advance
+    // (adv.seq_lens == nullptr: none)
+    AdvanceParams adv;
 };
 
 struct CombineParams {

@@ -37,7 +37,7 @@ EXPORTS = (
     "pkv_workspace_init", "pkv_rope_table", "paged_kv_append", "paged_decode_attn",
     "paged_decode_step", "paged_decode_partials", "decode_combine", "pkv_status_str",
     "pkv_version", "paged_decode_attn_noalloc", "paged_kv_advance", "decode_attn_contig",
-    "paged_prefill_attn", "paged_kv_extend",
+    "paged_prefill_attn", "paged_kv_extend", "paged_decode_step_advance",
 )
 
 
@@ -90,6 +90,8 @@ def lib():
             "decode_combine": (I, [DP, P, P, I, P, P]),
             "paged_decode_attn_noalloc": (I, [DP, P, P, P, P, P, P, I, P, P, P]),
             "paged_kv_advance": (I, [DP, P, P, P, P, I, P, P, P]),
+            "paged_decode_step_advance": (I, [DP, P, P, P, P, P, P, P, P, P, I, I, P, Z, P,
+                                              P, I, P, P]),
             "decode_attn_contig": (I, [DP, P, P, P, P, P, P, P, P, I, I, P, Z, P, P]),
             "paged_prefill_attn": (I, [DP, P, P, I, I, P, P, P, P, P, P, P, P]),
             "paged_kv_extend": (I, [DP, P, P, P, P, I, P, P, P, P, P, P, I, I, P, P]),
@@ -215,6 +217,22 @@ def paged_kv_advance(d: Dims, seq_lens, kv_indptr, kv_indices, free_pages, free_
     _check("paged_kv_advance", lib().paged_kv_advance(
         ctypes.byref(d), _ptr(seq_lens), _ptr(kv_indptr), _ptr(kv_indices), _ptr(free_pages),
         num_free, _ptr(free_head), _ptr(status), _stream(stream)))
+
+
+def paged_decode_step_advance(d: Dims, q, k_new, v_new, k_pool, v_pool, kv_indices,
+                              kv_indptr, seq_lens, rope_cos_sin, rope_max_pos: int,
+                              num_splits: int, workspace, out, free_pages, free_head,
+                              stream=None) -> None:
+    """paged_decode_step, then paged_kv_advance (its flags in the workspace
+    status word): one decode-loop step that leaves the metadata ready for
+    the next."""
+    ws_bytes = workspace.numel() * workspace.element_size()
+    num_free = 0 if free_pages is None else int(free_pages.numel())
+    _check("paged_decode_step_advance", lib().paged_decode_step_advance(
+        ctypes.byref(d), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_pool), _ptr(v_pool),
+        _ptr(kv_indices), _ptr(kv_indptr), _ptr(seq_lens), _ptr(rope_cos_sin), rope_max_pos,
+        num_splits, _ptr(workspace), ws_bytes, _ptr(out), _ptr(free_pages), num_free,
+        _ptr(free_head), _stream(stream)))
 
 
 def decode_attn_contig(d: Dims, q, k_cache, v_cache, seq_lens, num_splits: int, workspace,

@@ -184,6 +184,32 @@ def test_advance_argument_checks():
                               None) == pkv.PKV_OK
 
 
+def test_step_advance_argument_checks():
+    """The advance's arguments are checked before anything is launched."""
+    L = pkv.lib()
+    byref = pkv.ctypes.byref
+    fake = 1 << 32
+    d = _d(B=4)
+    S = 2
+    wsb = pkv.workspace_bytes(d, S)
+
+    def call(d=d, **kw):
+        a = dict(q=fake, kn=fake, vn=fake, k=fake, v=fake, ind=fake, ptr=fake, sl=fake,
+                 rope=None, ws=fake, out=fake, free=fake, n_free=8, head=fake)
+        a.update(kw)
+        return L.paged_decode_step_advance(
+            byref(d), a["q"], a["kn"], a["vn"], a["k"], a["v"], a["ind"], a["ptr"], a["sl"],
+            a["rope"], 0, S, a["ws"], wsb, a["out"], a["free"], a["n_free"], a["head"], None)
+
+    assert call(head=None) == pkv.PKV_ERR_INVALID_ARG
+    assert call(n_free=-1) == pkv.PKV_ERR_INVALID_ARG
+    assert call(free=None) == pkv.PKV_ERR_INVALID_ARG            # num_free > 0 needs a list
+    assert call(head=fake + 2) == pkv.PKV_ERR_INVALID_ARG        # misaligned
+    assert call(kn=None) == pkv.PKV_ERR_INVALID_ARG              # the step's own checks
+    assert call(ws=fake + 16) == pkv.PKV_ERR_INVALID_ARG
+    assert call(d=_d(B=0), head=None, free=None, n_free=0) == pkv.PKV_OK
+
+
 def test_prefill_argument_checks():
     L = pkv.lib()
     byref = pkv.ctypes.byref
