@@ -40,6 +40,8 @@ namespace {
 
 constexpr float kLn2f = 0.693147180559945309f;
 constexpr float kLog2ef = 1.4426950408889634f;
+// the piece combine splits D until it has about this many items
+constexpr long long kCombineMinItems = 128;
 constexpr int kSmemLimit = 232448;        // opt-in shared memory per block, sm_100 family
 constexpr unsigned kFull = 0xffffffffu;
 
@@ -271,6 +273,9 @@ __global__ void __launch_bounds__(FusedCfg<D, HPC>::kThreads, 1)
         const int my_t = lane & 15;
         const bool my_v = lane >= 16;
         const __nv_bfloat16 *pool = my_v ? p.v_pool : p.k_pool;
+        // K/V are read once per call: first out of L2, so the page table,
+        // q and the partials stay
+        const uint64_t stream_policy = policy_evict_first();
         int it = 0, pc = 0;
         bool aborted = false;
         auto page_of_tok = [&](int t) {
@@ -402,7 +407,7 @@ __global__ void __launch_bounds__(FusedCfg<D, HPC>::kThreads, 1)
                     }
                     const __nv_bfloat16 *src =
                         pool + ((size_t)page * p.page_size + sl) * (size_t)p.Hkv * D + head_off;
-                    bulk_copy_g2s(row, src, C::kRowBytes, &full[st]);
+                    bulk_copy_g2s_hint(row, src, C::kRowBytes, &full[st], stream_policy);
                 }
             }
         }
@@ -669,20 +674,24 @@ __global__ void __launch_bounds__(FusedCfg<D, HPC>::kThreads, 1)
 }
 
 // ---- merge the pieces of every row that has more than one ------------------
-// A group of WPH warps merges one (virtual row, query head): warp w takes
-// pieces w, w + WPH, ... and keeps a running (M, den, acc) that it rescales
-// whenever a larger max arrives, so the loads of U pieces can be in flight
-// at once; the group then merges its warps' states in shared memory.
-template <int D, int WPH>
+// An item is one (virtual row, query head, column slice of D / DS): a group
+// of WPH warps merges it.  Warp w takes pieces w, w + WPH, ... in rounds of
+// U, loaded together; each round rescales the running (M, den, acc) once to
+// the round's max and adds the round's weights, which are independent of one
+// another.  The group then merges its warps' states in shared memory.  A
+// column split (DS > 1) spreads rows with many pieces over more blocks.
+template <int D, int WPH, int DS>
 __global__ void __launch_bounds__(WPH > 8 ? 32 * WPH : 256)
     piece_combine_kernel(const PieceCombineParams p)
 {
-    constexpr int V = D / 32;                          // floats per lane
+    constexpr int DW = D / DS;                         // columns of one item
+    constexpr int V = DW / 32;                         // floats per lane
+    static_assert(V == 1 || V == 2 || V == 4, "slice width");
     constexpr int U = WPH >= 16 ? 16 : 8;              // pieces loaded ahead per warp
     constexpr int NWARP = WPH > 8 ? WPH : 8;
-    constexpr int GROUPS = NWARP / WPH;                // (row, head) pairs per block
+    constexpr int GROUPS = NWARP / WPH;                // items per block
     __shared__ float s_m[NWARP], s_den[NWARP];
-    __shared__ float s_acc[NWARP][D];
+    __shared__ __align__(16) float s_acc[NWARP][DW];
     grid_dependency_wait();
     // paged_decode_step_advance: the last block advances the metadata for the
     // next step; the decode grid, the only reader of it, has completed
@@ -693,12 +702,14 @@ __global__ void __launch_bounds__(WPH > 8 ? 32 * WPH : 256)
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int grp = warp / WPH, wi = warp % WPH;
-    const long long pair = (long long)blockIdx.x * GROUPS + grp;
-    const bool live = pair < (long long)p.Bv * p.HQV;
-    int n = 0, first = 0, r = 0, j = 0;
+    const long long item = (long long)blockIdx.x * GROUPS + grp;
+    const bool live = item < (long long)p.Bv * p.HQV * DS;
+    int n = 0, first = 0, r = 0, j = 0, col = lane * V;
     if (live) {
+        const long long pair = item / DS;
         r = (int)(pair / p.HQV);
         j = (int)(pair % p.HQV);
+        col += (int)(item % DS) * DW;
         first = p.row_info[2 * r];
         n = p.row_info[2 * r + 1];
     }
@@ -718,13 +729,15 @@ __global__ void __launch_bounds__(WPH > 8 ? 32 * WPH : 256)
                 if (k < n) {
                     const size_t slot = (size_t)(first + k + r) * p.HQV + j;
                     mlv[u] = __ldcg(ml + slot);
-                    const float *src = p.o_part + slot * D + lane * V;
+                    const float *src = p.o_part + slot * D + col;
                     if constexpr (V == 4) {
                         const float4 x = __ldcg(reinterpret_cast<const float4 *>(src));
                         o[u][0] = x.x; o[u][1] = x.y; o[u][2] = x.z; o[u][3] = x.w;
-                    } else {
+                    } else if constexpr (V == 2) {
                         const float2 x = __ldcg(reinterpret_cast<const float2 *>(src));
                         o[u][0] = x.x; o[u][1] = x.y;
+                    } else {
+                        o[u][0] = __ldcg(src);
                     }
                 } else {
                     mlv[u] = make_float2(-INFINITY, 0.f);
@@ -733,19 +746,32 @@ __global__ void __launch_bounds__(WPH > 8 ? 32 * WPH : 256)
                         o[u][v] = 0.f;
                 }
             }
+            // the round's max over its pieces with a nonzero sum (an empty
+            // piece leaves its o slot unwritten)
+            float mr = -INFINITY;
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+                if (mlv[u].y > 0.f)
+                    mr = fmaxf(mr, mlv[u].x);
+            if (mr == -INFINITY)
+                continue;
+            const float mn = fmaxf(M, mr);
+            const float a = M == -INFINITY ? 0.f : exp2f((M - mn) * kLog2ef);
+            den *= a;
+#pragma unroll
+            for (int v = 0; v < V; ++v)
+                acc[v] *= a;
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 if (!(mlv[u].y > 0.f))
                     continue;
-                const float mn = fmaxf(M, mlv[u].x);
-                const float a = exp2f((M - mn) * kLog2ef);            // 0 when M = -inf
                 const float w = mlv[u].y * exp2f((mlv[u].x - mn) * kLog2ef);
-                den = den * a + w;
+                den += w;
 #pragma unroll
                 for (int v = 0; v < V; ++v)
-                    acc[v] = acc[v] * a + w * o[u][v];
-                M = mn;
+                    acc[v] = fmaf(w, o[u][v], acc[v]);
             }
+            M = mn;
         }
     }
     if constexpr (WPH > 1) {
@@ -753,9 +779,13 @@ __global__ void __launch_bounds__(WPH > 8 ? 32 * WPH : 256)
             s_m[warp] = M;
             s_den[warp] = den;
         }
-#pragma unroll
-        for (int v = 0; v < V; ++v)
-            s_acc[warp][lane * V + v] = acc[v];
+        if constexpr (V == 4)
+            *reinterpret_cast<float4 *>(&s_acc[warp][lane * 4]) =
+                make_float4(acc[0], acc[1], acc[2], acc[3]);
+        else if constexpr (V == 2)
+            *reinterpret_cast<float2 *>(&s_acc[warp][lane * 2]) = make_float2(acc[0], acc[1]);
+        else
+            s_acc[warp][lane] = acc[0];
         __syncthreads();
         if (wi != 0)
             return;
@@ -784,15 +814,16 @@ __global__ void __launch_bounds__(WPH > 8 ? 32 * WPH : 256)
         return;
     const float inv = den > 0.f ? 1.f / den : 0.f;
     const int b = r % p.B, hg = r / p.B;
-    __nv_bfloat16 *dst =
-        p.out + ((size_t)b * p.Hq + (size_t)hg * p.HQV + j) * D + lane * V;
+    __nv_bfloat16 *dst = p.out + ((size_t)b * p.Hq + (size_t)hg * p.HQV + j) * D + col;
     if constexpr (V == 4) {
         uint2 v;
         v.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
         v.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
         *reinterpret_cast<uint2 *>(dst) = v;
-    } else {
+    } else if constexpr (V == 2) {
         *reinterpret_cast<uint32_t *>(dst) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+    } else {
+        *dst = __float2bfloat16_rn(acc[0] * inv);
     }
 }
 
@@ -876,33 +907,43 @@ cudaError_t launch_fused_decode(const FusedParams &p, int D, int grid, cudaStrea
 cudaError_t launch_piece_combine(const PieceCombineParams &p, int D, int grid_blocks,
                                  cudaStream_t stream)
 {
-    // warps per (row, head): enough that each warp loads all its pieces in
-    // one round
-    // rows are uneven: size for three times the average pieces per row
+    // warps per item: enough that each warp loads all its pieces in one
+    // round; rows are uneven, so size for three times the average pieces
+    // per row
     const long long expect = 3 * (grid_blocks / (p.Bv > 0 ? p.Bv : 1)) + 2;
     const int wph = expect <= 8 ? 1 : expect <= 16 ? 2 : expect <= 32 ? 4 : expect <= 64 ? 8 : 16;
     const long long pairs = (long long)p.Bv * p.HQV;
+    // split the columns while there are fewer items than about one per SM
+    // (few rows, many pieces each: long contexts)
+    int ds = 1;
+    while (ds < D / 32 && pairs * ds < kCombineMinItems)
+        ds *= 2;
     const int warps = wph > 8 ? wph : 8;
     const int groups = warps / wph;
-    const unsigned blocks = (unsigned)((pairs + groups - 1) / groups) +
+    const unsigned blocks = (unsigned)((pairs * ds + groups - 1) / groups) +
                             (p.adv.seq_lens != nullptr ? 1u : 0u);
-    cudaError_t e;
-#define PKV_COMBINE_CASE(DD, W)                                                              \
-    e = launch_pdl(piece_combine_kernel<DD, W>, dim3(blocks), dim3(warps * 32), 0, stream, p)
-    if (D == 64) {
-        if (wph == 1) PKV_COMBINE_CASE(64, 1);
-        else if (wph == 2) PKV_COMBINE_CASE(64, 2);
-        else if (wph == 4) PKV_COMBINE_CASE(64, 4);
-        else if (wph == 8) PKV_COMBINE_CASE(64, 8);
-        else PKV_COMBINE_CASE(64, 16);
-    } else {
-        if (wph == 1) PKV_COMBINE_CASE(128, 1);
-        else if (wph == 2) PKV_COMBINE_CASE(128, 2);
-        else if (wph == 4) PKV_COMBINE_CASE(128, 4);
-        else if (wph == 8) PKV_COMBINE_CASE(128, 8);
-        else PKV_COMBINE_CASE(128, 16);
+    cudaError_t e = cudaErrorInvalidValue;
+#define PKV_COMBINE_WPH(DD, S)                                                               \
+    switch (wph) {                                                                           \
+    case 1: e = launch_pdl(piece_combine_kernel<DD, 1, S>, dim3(blocks), dim3(warps * 32), 0, \
+                           stream, p); break;                                                \
+    case 2: e = launch_pdl(piece_combine_kernel<DD, 2, S>, dim3(blocks), dim3(warps * 32), 0, \
+                           stream, p); break;                                                \
+    case 4: e = launch_pdl(piece_combine_kernel<DD, 4, S>, dim3(blocks), dim3(warps * 32), 0, \
+                           stream, p); break;                                                \
+    case 8: e = launch_pdl(piece_combine_kernel<DD, 8, S>, dim3(blocks), dim3(warps * 32), 0, \
+                           stream, p); break;                                                \
+    default: e = launch_pdl(piece_combine_kernel<DD, 16, S>, dim3(blocks), dim3(warps * 32), \
+                            0, stream, p); break;                                            \
     }
-#undef PKV_COMBINE_CASE
+    if (D == 64) {
+        if (ds == 1) { PKV_COMBINE_WPH(64, 1) } else { PKV_COMBINE_WPH(64, 2) }
+    } else {
+        if (ds == 1) { PKV_COMBINE_WPH(128, 1) }
+        else if (ds == 2) { PKV_COMBINE_WPH(128, 2) }
+        else { PKV_COMBINE_WPH(128, 4) }
+    }
+#undef PKV_COMBINE_WPH
     if (e != cudaSuccess)
         return e;
     return cudaGetLastError();
