@@ -215,14 +215,17 @@ __global__ void __launch_bounds__(FusedCfg<D, HPC>::kThreads, 1)
 
     // T: the rows' total weight.  Token t of row r sits at position
     // prefix[r] + row_cost + t; block c owns positions [T c / G, T (c+1) / G).
-    const long long T = prefix[Bv];
+    // T < 2^31 (the launch bounds rows x (max length + row cost)) and
+    // G <= 65536, so 32-bit divisions give these bounds exactly:
+    // T c / G = (T / G) c + ((T % G) c) / G.
+    const unsigned T = (unsigned)prefix[Bv];
     // fewer blocks when there is little work: at least kFusedMinTokens each
-    long long Ge = (T + kFusedMinTokens - 1) / kFusedMinTokens;
-    if (Ge > gridDim.x)
-        Ge = gridDim.x;
-    if (Ge < 1)
-        Ge = 1;
-    const int G = (int)Ge;
+    unsigned Gu = (T + kFusedMinTokens - 1) / kFusedMinTokens;
+    if (Gu > gridDim.x)
+        Gu = gridDim.x;
+    if (Gu < 1)
+        Gu = 1;
+    const int G = (int)Gu;
 
     // rows with no tokens: zero output, no pieces (owner: block r mod grid)
     for (int r = cta; r < Bv; r += gridDim.x) {
@@ -240,8 +243,9 @@ __global__ void __launch_bounds__(FusedCfg<D, HPC>::kThreads, 1)
     }
     if (cta >= G)
         return;
-    const long long start = T * cta / G;
-    const long long end = T * (cta + 1) / G;
+    const unsigned t_q = T / Gu, t_r = T % Gu;
+    const long long start = (long long)t_q * cta + t_r * (unsigned)cta / Gu;
+    const long long end = (long long)t_q * (cta + 1) + t_r * (unsigned)(cta + 1) / Gu;
     if (start >= end)
         return;
 
