@@ -696,6 +696,10 @@ __global__ void __launch_bounds__(WPH > 8 ? 32 * WPH : 256)
     constexpr int GROUPS = NWARP / WPH;                // items per block
     __shared__ float s_m[NWARP], s_den[NWARP];
     __shared__ __align__(16) float s_acc[NWARP][DW];
+    // the next kernel (the next step's decode) may be scheduled once every
+    // block of this grid has started; it waits for this grid's completion
+    // before it reads anything this grid writes
+    grid_launch_dependents();
     grid_dependency_wait();
     // paged_decode_step_advance: the last block advances the metadata for the
     // next step; the decode grid, the only reader of it, has completed
