@@ -10,27 +10,36 @@
 // 0 .. that position: out = softmax(scale q K^T) V with K/V of kv head
 // h / n_rep gathered through the page table.
 //
-// Layout of the work.  One block of 128 threads takes one (query tile, row,
-// kv head): 128 query rows = the tile's 128 / n_rep tokens x the kv head's
-// n_rep query heads (token-major).  Thread t owns query row t, which is lane t
-// of tensor memory.  Per key tile of 64 tokens:
-//  - every thread gathers 16-byte chunks of the tile's K and V rows through
-//    the page table with cp.async, straight into the no-swizzle canonical
-//    layout the MMA reads (8-row x 16-byte core matrices; consecutive threads
-//    fill consecutive 16 bytes), two stages;
-//  - one thread issues S = Q K^T (M 128, N 64, K = D in steps of 16; Q and K
-//    K-major) into 64 TMEM columns and commits it to an mbarrier;
-//  - each thread loads its row of S from TMEM, masks keys past its position,
-//    updates its own fp32 online softmax (log2 domain, the scale folded into
-//    one FFMA per exponent), writes P (bf16) into shared memory as the K-major
-//    A operand, and rescales its row of O in TMEM only when its max has grown
-//    by more than 2^8 (P stays below 2^8 otherwise); l sums the fp32 terms;
-//  - one thread issues O += P V (M 128, N = D, K = 64; V read MN-major, its
-//    rows as they are) into D TMEM columns, then the next tile's S.
+// A query tile is 128 query rows = 128 / n_rep tokens x the kv head's n_rep
+// query heads (token-major) of one (row, kv head); the thread that owns query
+// row t of a tile owns lane t of tensor memory.  Per K/V tile of 64 keys:
+// K and V rows are gathered through the page table with 16-byte cp.async,
+// straight into the no-swizzle canonical layout the MMA reads (8-row x
+// 16-byte core matrices); S = Q K^T (M 128, N 64, K = D in steps of 16; Q
+// and K K-major) goes to tensor memory; each row's thread reads its row of
+// S, masks keys past its position, updates its own fp32 online softmax (log2
+// domain, the scale folded into one FFMA per exponent, l from the fp32
+// terms), rescales its row of O in tensor memory only when its max has grown
+// by more than 2^8, and writes P (bf16) to shared memory as the K-major A
+// operand; O += P V (M 128, N = D, K = 64; V read MN-major, its rows as they
+// are) accumulates in tensor memory.  Two block layouts, chosen by D:
+//
+//  - D = 64, prefill_row_kernel: one tile per block of 128 threads, three
+//    blocks per SM.  All threads gather (two stages) and run the softmax; one
+//    thread issues the MMAs, and the steps alternate within a block while
+//    the SM's blocks overlap one another.
+//  - D = 128, prefill_pair_kernel: two consecutive tiles (A, B) per block,
+//    sharing every K/V tile, with warp roles handing work over through
+//    mbarriers: warps 9-12 gather three K/V stages ahead, warp 8 owns tensor
+//    memory and issues S_A and S_B of K/V tile kt (two S buffers per tile),
+//    then O_A and O_B of tile kt - 1, and warps 0-3 / 4-7 run the softmax of
+//    tiles A / B.  While one tile's rows run their softmax, the tensor cores
+//    work on the other tile's S and on both tiles' P V.
+//
 // Descriptors: version 1, no swizzle; leading byte offset = stride between
 // core matrices along K, stride byte offset = along M/N, for both K-major and
 // MN-major operands.  Every mbarrier wait is time-bounded; tensor memory is
-// allocated by warp 0 at the start and released on every path.
+// allocated at the start and released on every path.
 #include <cmath>
 
 #include "pkv_device.cuh"
@@ -43,7 +52,7 @@ namespace {
 constexpr unsigned kAllTc = 0xffffffffu;
 
 template <int D>
-struct TcCfg {
+struct RowCfg {
     static constexpr int kRows = 128;
     static constexpr int kKeys = 64;
     static constexpr int kThreads = 128;
@@ -199,9 +208,9 @@ __device__ __forceinline__ void cp_async_wait_all()
 }
 
 template <int D>
-__global__ void __launch_bounds__(TcCfg<D>::kThreads, 2) prefill_tc_kernel(const PrefillParams p)
+__global__ void __launch_bounds__(RowCfg<D>::kThreads, 2) prefill_row_kernel(const PrefillParams p)
 {
-    using C = TcCfg<D>;
+    using C = RowCfg<D>;
     constexpr int CH = D / 8;                      // 16-byte chunks per row
     extern __shared__ __align__(1024) unsigned char smem[];
     uint64_t *bar_s = reinterpret_cast<uint64_t *>(smem + C::kBarOff);
@@ -494,12 +503,12 @@ __global__ void __launch_bounds__(TcCfg<D>::kThreads, 2) prefill_tc_kernel(const
 }
 
 template <int D>
-cudaError_t launch_tc_d(const PrefillParams &p, int max_q_len, cudaStream_t stream)
+cudaError_t launch_row(const PrefillParams &p, int max_q_len, cudaStream_t stream)
 {
-    using C = TcCfg<D>;
+    using C = RowCfg<D>;
     static bool attr_done = false;
     if (!attr_done) {
-        cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<D>,
+        cudaError_t e = cudaFuncSetAttribute(prefill_row_kernel<D>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              C::kSmemBytes);
         if (e != cudaSuccess)
@@ -522,7 +531,416 @@ cudaError_t launch_tc_d(const PrefillParams &p, int max_q_len, cudaStream_t stre
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, prefill_tc_kernel<D>, p);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, prefill_row_kernel<D>, p);
+    if (e != cudaSuccess)
+        return e;
+    return cudaGetLastError();
+}
+
+template <int D>
+struct PairCfg {
+    static constexpr int kRows = 128;                      // query rows of one tile
+    static constexpr int kKeys = 64;                       // keys of one K/V tile
+    static constexpr int kStages = 3;                      // K/V tiles in flight
+    static constexpr int kMmaWarp = 8;                     // warp 8: tensor-memory owner, MMA issue
+    static constexpr int kLoadThreads = 128;               // warps 9-12: K/V gathers
+    static constexpr int kLoadTid0 = (kMmaWarp + 1) * 32;
+    static constexpr int kThreads = kLoadTid0 + kLoadThreads;
+    static constexpr int kGroup = D * 16;                  // 8 rows x D bf16, canonical
+    static constexpr int kQBytes = kRows / 8 * kGroup;     // one query tile
+    static constexpr int kKVBytes = kKeys / 8 * kGroup;    // one K or V tile
+    static constexpr int kPGroup = kKeys * 16;             // 8 rows x 64 keys
+    static constexpr int kPBytes = kRows / 8 * kPGroup;    // one P tile
+    static constexpr int kKVOff = 2 * kQBytes;             // stage s: K, then V
+    static constexpr int kPOff = kKVOff + kStages * 2 * kKVBytes;
+    static constexpr int kBarOff = kPOff + 2 * kPBytes;
+    // mbarriers: kv_full[3], kv_empty[3], s_full[tile][buffer], p_full[2],
+    // o_done[2], drain
+    static constexpr int kNumBars = 2 * kStages + 9;
+    static constexpr int kTmemSlot = kBarOff + kNumBars * 8;
+    static constexpr int kAbortOff = kTmemSlot + 4;
+    static constexpr int kSmemBytes = kAbortOff + 12;
+    static_assert(kSmemBytes <= 232448, "shared memory per block");
+    // tensor memory: S of tile X in two buffers at 128 X + 64 j, O of tile X
+    // at 256 + D X
+    static constexpr uint32_t kTmemCols = 512;
+    static constexpr uint32_t kOCol = 256;
+};
+
+// cp.async completion of this thread's earlier copies arrives on bar (the
+// barrier's count includes one arrival per loading thread).
+__device__ __forceinline__ void cp_async_arrive(uint64_t *bar)
+{
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar))
+                 : "memory");
+}
+
+template <int D>
+__global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
+    prefill_pair_kernel(const PrefillParams p)
+{
+    using C = PairCfg<D>;
+    constexpr int CH = D / 8;                      // 16-byte chunks per row
+    constexpr int NS = C::kStages;
+    extern __shared__ __align__(1024) unsigned char smem[];
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kBarOff);
+    uint64_t *kv_full = bars, *kv_empty = bars + NS;
+    // s_full has one barrier per S buffer, so it never runs two phases ahead
+    // of the softmax that waits on it
+    uint64_t *s_full = bars + 2 * NS, *p_full = s_full + 4, *o_done = p_full + 2;
+    uint64_t *drain = o_done + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kTmemSlot);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kAbortOff);
+    const uint32_t sbase = smem_addr(smem);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    const int b = blockIdx.y / p.Hkv, g = blockIdx.y % p.Hkv;
+    const int n_rep = p.n_rep, tq = p.tq;
+
+    grid_dependency_wait();
+    // the row's chunk, checked (a bad row is flagged once, by its block 0)
+    const int q0 = p.qo_indptr[b], q1 = p.qo_indptr[b + 1];
+    const int L = p.seq_lens[b];
+    const int q_len = q1 - q0;
+    const bool row_ok = q_len >= 0 && q0 >= 0 && q1 <= p.total_q && L >= 0 &&
+                        L <= p.max_seq_len && q_len <= L;
+    if (!row_ok) {
+        if (blockIdx.x == 0 && g == 0 && tid == 0)
+            tc_flag(p.status, kFlagBadLen);
+        return;
+    }
+    const int n_tiles = (q_len + tq - 1) / tq;
+    if ((n_tiles + 1) / 2 > (int)gridDim.x && blockIdx.x == 0 && g == 0 && tid == 0)
+        tc_flag(p.status, kFlagBadLen);                // chunk longer than max_q_len
+    // tiles B = n_tiles - 1 - 2x (the most keys first) and A = B - 1
+    const int tB = n_tiles - 1 - 2 * (int)blockIdx.x;
+    if (tB < 0)
+        return;
+    const int tA = tB - 1;                             // -1: tile A is idle
+    const int kv_end = L - q_len + min(q_len, (tB + 1) * tq);
+    const int n_kt = (kv_end + C::kKeys - 1) / C::kKeys;
+    const int pg0 = p.kv_indptr[b];
+    const int npg = p.kv_indptr[b + 1] - pg0;
+    const bool table_ok = pg0 >= 0 && npg >= 0 && p.kv_indptr[b + 1] <= p.num_indices &&
+                          (long long)npg * p.page_size >= (long long)L;
+    if (!table_ok && tid == 0)
+        tc_flag(p.status, kFlagBadPage);
+
+    if (tid == 0) {
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(&kv_full[s], C::kLoadThreads);
+            mbar_init(&kv_empty[s], 1);
+        }
+        for (int x = 0; x < 2; ++x) {
+            mbar_init(&s_full[2 * x], 1);
+            mbar_init(&s_full[2 * x + 1], 1);
+            mbar_init(&p_full[x], C::kRows);
+            mbar_init(&o_done[x], 1);
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == C::kMmaWarp) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_addr(tmem_slot)),
+                     "r"(C::kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    // Q of both tiles: row m of tile x = token m / n_rep, head m % n_rep
+    const int rows_used = tq * n_rep;
+    for (int e = tid; e < 2 * C::kRows * CH; e += C::kThreads) {
+        const int x = e / (C::kRows * CH), ee = e % (C::kRows * CH);
+        const int r8 = ee & 7, c = (ee >> 3) % CH, grp = (ee >> 3) / CH;
+        const int m = grp * 8 + r8;
+        const int t = x == 0 ? tA : tB;
+        const int tok = m / n_rep, hh = m - tok * n_rep;
+        const bool live = t >= 0 && m < rows_used && tok < q_len - t * tq;
+        const __nv_bfloat16 *src =
+            live ? p.q + ((size_t)(q0 + t * tq + tok) * p.Hq + (size_t)g * n_rep + hh) * D + c * 8
+                 : p.q;
+        cp_async16(sbase + e * 16, src, live ? 16u : 0u);
+    }
+    cp_async_commit();
+    cp_async_wait_all();
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (tid >= C::kLoadTid0) {
+        // ====================== K/V gathers =================================
+        // thread: key lt / 2 of the tile, chunks [CH/2 (lt & 1), CH/2 (lt & 1) + CH/2)
+        const int lt = tid - C::kLoadTid0;
+        const int key = lt >> 1, c0 = (lt & 1) * (CH / 2);
+        const uint32_t row_off = (uint32_t)((key >> 3) * C::kGroup + (key & 7) * 16);
+        for (int kt = 0; kt < n_kt; ++kt) {
+            const int st = kt % NS;
+            if (kt >= NS) {
+                const bool ok = mbar_wait_bounded(&kv_empty[st], (uint32_t)(((kt / NS) - 1) & 1));
+                if (!ok) {
+                    *abort_flag = 1;
+                    tc_flag(p.status, kFlagTimeout);
+                }
+                if (*abort_flag)
+                    break;
+            }
+            const int tok = kt * C::kKeys + key;
+            bool live = tok < kv_end;
+            size_t off = 0;
+            if (live) {
+                const int pi = p.ps_shift >= 0 ? (tok >> p.ps_shift) : (tok / p.page_size);
+                const int sl = tok - pi * p.page_size;
+                int page = table_ok ? __ldg(p.kv_indices + pg0 + pi) : 0;
+                if (page < 0 || page >= p.num_pages) {
+                    tc_flag(p.status, kFlagBadPage);
+                    page = 0;
+                }
+                off = (((size_t)page * p.page_size + sl) * p.Hkv + g) * D;
+            }
+            const uint32_t kdst = sbase + C::kKVOff + st * 2 * C::kKVBytes + row_off;
+            const uint32_t vdst = kdst + C::kKVBytes;
+#pragma unroll
+            for (int c = c0; c < c0 + CH / 2; ++c) {
+                cp_async16(kdst + c * 128, p.k_pool + off + c * 8, live ? 16u : 0u);
+                cp_async16(vdst + c * 128, p.v_pool + off + c * 8, live ? 16u : 0u);
+            }
+            cp_async_arrive(&kv_full[st]);
+        }
+        cp_async_wait_all();
+    } else if (warp == C::kMmaWarp) {
+        // ====================== tensor-core issue ===========================
+        constexpr uint32_t kIdescS = instr_desc(128, C::kKeys, 0);
+        constexpr uint32_t kIdescO = instr_desc(128, D, 1);
+        if (lane == 0) {
+            auto fail = [&]() {
+                *abort_flag = 1;
+                tc_flag(p.status, kFlagTimeout);
+            };
+            bool ok = true;
+            for (int kt = 0; kt <= n_kt && ok; ++kt) {
+                if (kt < n_kt) {
+                    const int st = kt % NS;
+                    ok = mbar_wait_bounded(&kv_full[st], (uint32_t)((kt / NS) & 1)) && !*abort_flag;
+                    if (!ok)
+                        break;
+                    tc_fence_after();
+                    const uint32_t k_s = sbase + C::kKVOff + st * 2 * C::kKVBytes;
+                    for (int x = 0; x < 2; ++x) {
+                        const uint32_t q_s = sbase + x * C::kQBytes;
+                        const uint32_t t_s = tmem + 128 * x + 64 * (kt & 1);
+#pragma unroll
+                        for (int s = 0; s < D / 16; ++s)
+                            umma(t_s, smem_desc(q_s + s * 256, 128, C::kGroup),
+                                 smem_desc(k_s + s * 256, 128, C::kGroup), kIdescS, s > 0);
+                        umma_commit(&s_full[2 * x + (kt & 1)]);
+                    }
+                }
+                if (kt > 0) {
+                    const int j = kt - 1, sj = j % NS;
+                    const uint32_t v_s = sbase + C::kKVOff + sj * 2 * C::kKVBytes + C::kKVBytes;
+                    for (int x = 0; x < 2 && ok; ++x) {
+                        ok = mbar_wait_bounded(&p_full[x], (uint32_t)(j & 1)) && !*abort_flag;
+                        if (!ok)
+                            break;
+                        tc_fence_after();
+                        const uint32_t p_s = sbase + C::kPOff + x * C::kPBytes;
+                        const uint32_t t_o = tmem + C::kOCol + D * x;
+#pragma unroll
+                        for (int s = 0; s < C::kKeys / 16; ++s)
+                            umma(t_o, smem_desc(p_s + s * 256, 128, C::kPGroup),
+                                 smem_desc(v_s + s * 2 * C::kGroup, C::kGroup, 128), kIdescO,
+                                 (j == 0 && s == 0) ? 0u : 1u);
+                        umma_commit(&o_done[x]);
+                    }
+                    if (ok)
+                        umma_commit(&kv_empty[sj]);
+                }
+            }
+            if (!ok)
+                fail();
+        }
+        __syncwarp();
+    } else {
+        // ====================== softmax of tile x, row m ====================
+        const int x = warp >> 2;
+        const int m = tid & (C::kRows - 1);
+        const int t = x == 0 ? tA : tB;
+        const int tok_m = m / n_rep;
+        const int ntok = t >= 0 ? min(tq, q_len - t * tq) : 0;
+        const int pos_first = L - q_len + (t >= 0 ? t * tq : 0);
+        const int pos = (t >= 0 && m < rows_used && tok_m < ntok) ? pos_first + tok_m : -1;
+        const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+        const uint32_t t_o = tmem + C::kOCol + D * x;
+        unsigned char *p_row =
+            smem + C::kPOff + x * C::kPBytes + (m >> 3) * C::kPGroup + (m & 7) * 16;
+        float m_run = -INFINITY, l_run = 0.f;
+        bool ok = true;
+        for (int kt = 0; kt < n_kt; ++kt) {
+            ok = mbar_wait_bounded(&s_full[2 * x + (kt & 1)], (uint32_t)((kt >> 1) & 1)) &&
+                 !*abort_flag;
+            if (!__all_sync(kAllTc, ok)) {
+                ok = false;
+                if (lane == 0) {
+                    *abort_flag = 1;
+                    tc_flag(p.status, kFlagTimeout);
+                }
+                break;
+            }
+            tc_fence_after();
+            const int key0 = kt * C::kKeys;
+            const bool need_mask = key0 + C::kKeys - 1 > pos_first;
+            float sv[C::kKeys];
+            static_assert(C::kKeys == 64, "one 64-column load per tile");
+            tmem_ld64(tmem + 128 * x + 64 * (kt & 1) + lane_off, sv);
+            if (need_mask) {
+#pragma unroll
+                for (int i = 0; i < C::kKeys; ++i)
+                    sv[i] = key0 + i > pos ? -INFINITY : sv[i];
+            }
+            float mraw = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < C::kKeys; ++i)
+                mraw = fmaxf(mraw, sv[i]);
+            const float mx = mraw * p.scale_log2;
+            // a new base only when the max grows by more than 2^8 (or first)
+            const bool rebase = mx > m_run + 8.f;
+            float alpha = 1.f;
+            if (rebase) {
+                alpha = exp2f(m_run - mx);             // 0 while m_run is -inf
+                m_run = mx;
+                l_run *= alpha;
+            }
+            // O and P of this tile are free once the previous P V is done
+            if (kt > 0) {
+                ok = mbar_wait_bounded(&o_done[x], (uint32_t)((kt - 1) & 1)) && !*abort_flag;
+                if (!__all_sync(kAllTc, ok)) {
+                    ok = false;
+                    if (lane == 0) {
+                        *abort_flag = 1;
+                        tc_flag(p.status, kFlagTimeout);
+                    }
+                    break;
+                }
+                tc_fence_after();
+            }
+            if (__any_sync(kAllTc, rebase && kt > 0)) {
+#pragma unroll
+                for (int c0 = 0; c0 < D; c0 += 16) {
+                    float v[16];
+                    tmem_ld16(t_o + lane_off + c0, v);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        v[i] *= alpha;
+                    tmem_st16(t_o + lane_off + c0, v);
+                }
+                tmem_st_wait();
+            }
+            const float nbase = m_run == -INFINITY ? 0.f : -m_run;
+            const float sl2 = p.scale_log2;
+            float lsum = 0.f;
+#pragma unroll
+            for (int c = 0; c < C::kKeys / 8; ++c) {
+                uint32_t w[4];
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) {
+                    const float e0 = exp2f(fmaf(sv[c * 8 + 2 * jj], sl2, nbase));
+                    const float e1 = exp2f(fmaf(sv[c * 8 + 2 * jj + 1], sl2, nbase));
+                    w[jj] = pack_bf16x2(e0, e1);
+                    lsum += e0 + e1;                  // l from the fp32 terms
+                }
+                *reinterpret_cast<uint4 *>(p_row + c * 128) = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+            l_run += lsum;
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(&p_full[x]);
+        }
+        // ---- normalise and store this row ----------------------------------
+        if (ok) {
+            ok = mbar_wait_bounded(&o_done[x], (uint32_t)((n_kt - 1) & 1)) && !*abort_flag;
+            if (!__all_sync(kAllTc, ok) && lane == 0) {
+                *abort_flag = 1;
+                tc_flag(p.status, kFlagTimeout);
+            }
+        }
+        tc_fence_after();
+        if (__all_sync(kAllTc, ok)) {
+            const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+            __nv_bfloat16 *orow = nullptr;
+            if (pos >= 0) {
+                const int hh = m - tok_m * n_rep;
+                orow = p.out + ((size_t)(q0 + t * tq + tok_m) * p.Hq + (size_t)g * n_rep + hh) * D;
+            }
+#pragma unroll
+            for (int c0 = 0; c0 < D; c0 += 16) {
+                float v[16];
+                tmem_ld16(t_o + lane_off + c0, v);
+                if (orow != nullptr) {
+                    uint4 lo = make_uint4(pack_bf16x2(v[0] * inv, v[1] * inv),
+                                          pack_bf16x2(v[2] * inv, v[3] * inv),
+                                          pack_bf16x2(v[4] * inv, v[5] * inv),
+                                          pack_bf16x2(v[6] * inv, v[7] * inv));
+                    uint4 hi = make_uint4(pack_bf16x2(v[8] * inv, v[9] * inv),
+                                          pack_bf16x2(v[10] * inv, v[11] * inv),
+                                          pack_bf16x2(v[12] * inv, v[13] * inv),
+                                          pack_bf16x2(v[14] * inv, v[15] * inv));
+                    *reinterpret_cast<uint4 *>(orow + c0) = lo;
+                    *reinterpret_cast<uint4 *>(orow + c0 + 8) = hi;
+                }
+            }
+        }
+    }
+    // every role is done; on an abort the MMA warp waits (bounded) for the
+    // tensor cores to drain before tensor memory is released
+    tc_fence_before();
+    __syncthreads();
+    if (warp == C::kMmaWarp) {
+        if (*abort_flag && lane == 0) {
+            umma_commit(drain);
+            (void)mbar_wait_bounded(drain, 0u);
+        }
+        __syncwarp();
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(C::kTmemCols)
+                     : "memory");
+    }
+}
+
+template <int D>
+cudaError_t launch_pair(const PrefillParams &p, int max_q_len, cudaStream_t stream)
+{
+    using C = PairCfg<D>;
+    static bool attr_done = false;
+    if (!attr_done) {
+        cudaError_t e = cudaFuncSetAttribute(prefill_pair_kernel<D>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             C::kSmemBytes);
+        if (e != cudaSuccess)
+            return e;
+        attr_done = true;
+    }
+    const long long tiles = ((long long)max_q_len + p.tq - 1) / p.tq;
+    const long long pairs = (tiles + 1) / 2;
+    const long long rows = (long long)p.B * p.Hkv;
+    if (pairs <= 0 || rows <= 0)
+        return cudaSuccess;
+    if (pairs > 0x7fffffffLL || rows > 65535)
+        return cudaErrorInvalidValue;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)pairs, (unsigned)rows);
+    cfg.blockDim = dim3(C::kThreads);
+    cfg.dynamicSmemBytes = C::kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, prefill_pair_kernel<D>, p);
     if (e != cudaSuccess)
         return e;
     return cudaGetLastError();
@@ -532,9 +950,11 @@ cudaError_t launch_tc_d(const PrefillParams &p, int max_q_len, cudaStream_t stre
 
 cudaError_t launch_prefill(const PrefillParams &p, int D, int max_q_len, cudaStream_t stream)
 {
+    // the paired, warp-specialised layout is 27-31% faster at D = 128; at
+    // D = 64 the single-tile blocks, three to an SM, are 16% faster
     if (D == 64)
-        return launch_tc_d<64>(p, max_q_len, stream);
-    return launch_tc_d<128>(p, max_q_len, stream);
+        return launch_row<64>(p, max_q_len, stream);
+    return launch_pair<128>(p, max_q_len, stream);
 }
 
 } // namespace pkv
