@@ -714,6 +714,13 @@ __global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
         // ====================== tensor-core issue ===========================
         constexpr uint32_t kIdescS = instr_desc(128, C::kKeys, 0);
         constexpr uint32_t kIdescO = instr_desc(128, D, 1);
+        // Every shared-memory address is below 256 KB, so moving an operand by
+        // d bytes adds d / 16 to its descriptor's address field with no carry:
+        // the descriptors are built once and offset per stage and k-step.
+        const uint64_t dq = smem_desc(sbase, 128, C::kGroup);
+        const uint64_t dk = smem_desc(sbase + C::kKVOff, 128, C::kGroup);
+        const uint64_t dv = smem_desc(sbase + C::kKVOff + C::kKVBytes, C::kGroup, 128);
+        const uint64_t dp = smem_desc(sbase + C::kPOff, 128, C::kPGroup);
         if (lane == 0) {
             auto fail = [&]() {
                 *abort_flag = 1;
@@ -727,32 +734,30 @@ __global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
                     if (!ok)
                         break;
                     tc_fence_after();
-                    const uint32_t k_s = sbase + C::kKVOff + st * 2 * C::kKVBytes;
+                    const uint64_t dk_st = dk + (uint64_t)((st * 2 * C::kKVBytes) >> 4);
                     for (int x = 0; x < 2; ++x) {
-                        const uint32_t q_s = sbase + x * C::kQBytes;
+                        const uint64_t dq_x = dq + (uint64_t)((x * C::kQBytes) >> 4);
                         const uint32_t t_s = tmem + 128 * x + 64 * (kt & 1);
 #pragma unroll
                         for (int s = 0; s < D / 16; ++s)
-                            umma(t_s, smem_desc(q_s + s * 256, 128, C::kGroup),
-                                 smem_desc(k_s + s * 256, 128, C::kGroup), kIdescS, s > 0);
+                            umma(t_s, dq_x + 16 * s, dk_st + 16 * s, kIdescS, s > 0);
                         umma_commit(&s_full[2 * x + (kt & 1)]);
                     }
                 }
                 if (kt > 0) {
                     const int j = kt - 1, sj = j % NS;
-                    const uint32_t v_s = sbase + C::kKVOff + sj * 2 * C::kKVBytes + C::kKVBytes;
+                    const uint64_t dv_st = dv + (uint64_t)((sj * 2 * C::kKVBytes) >> 4);
                     for (int x = 0; x < 2 && ok; ++x) {
                         ok = mbar_wait_bounded(&p_full[x], (uint32_t)(j & 1)) && !*abort_flag;
                         if (!ok)
                             break;
                         tc_fence_after();
-                        const uint32_t p_s = sbase + C::kPOff + x * C::kPBytes;
+                        const uint64_t dp_x = dp + (uint64_t)((x * C::kPBytes) >> 4);
                         const uint32_t t_o = tmem + C::kOCol + D * x;
 #pragma unroll
                         for (int s = 0; s < C::kKeys / 16; ++s)
-                            umma(t_o, smem_desc(p_s + s * 256, 128, C::kPGroup),
-                                 smem_desc(v_s + s * 2 * C::kGroup, C::kGroup, 128), kIdescO,
-                                 (j == 0 && s == 0) ? 0u : 1u);
+                            umma(t_o, dp_x + 16 * s, dv_st + (uint64_t)((s * 2 * C::kGroup) >> 4),
+                                 kIdescO, (j == 0 && s == 0) ? 0u : 1u);
                         umma_commit(&o_done[x]);
                     }
                     if (ok)
