@@ -53,23 +53,26 @@ def test_prefill_shapes(Hq, Hkv, D):
     compare_out(out, _want(c))
 
 
-@pytest.mark.parametrize("ps", [1, 5, 32])
-def test_prefill_page_sizes(ps):
+@pytest.mark.parametrize("ps,D", [(1, 64), (5, 64), (32, 64), (1, 128), (5, 128), (32, 128)])
+def test_prefill_page_sizes(ps, D):
     lens = [100, 7, 250]
     qls = [37, 7, 129]
-    c = wl.prefill("pfp", B=3, Hq=16, Hkv=4, D=64, page_size=ps, seq_lens=lens, q_lens=qls,
-                   seed=ps)
+    c = wl.prefill("pfp", B=3, Hq=16, Hkv=4, D=D, page_size=ps, seq_lens=lens, q_lens=qls,
+                   seed=ps + D)
     out, st, _ = _run(c)
     assert st == 0
     compare_out(out, _want(c))
 
 
-def test_prefill_many_tiles():
-    """Chunks of several query tiles against several key tiles each."""
+@pytest.mark.parametrize("Hq,Hkv,D", [(16, 4, 64), (16, 4, 128), (8, 8, 128)])
+def test_prefill_many_tiles(Hq, Hkv, D):
+    """Chunks of several query tiles against several key tiles each (at
+    D = 128: pairs of tiles, an odd tile count leaving one tile of a pair
+    idle, and the three K/V stages reused many times)."""
     lens = [1000, 700, 513, 129]
     qls = [700, 700, 200, 129]
-    c = wl.prefill("pfm", B=4, Hq=16, Hkv=4, D=64, page_size=16, seq_lens=lens, q_lens=qls,
-                   seed=21)
+    c = wl.prefill("pfm", B=4, Hq=Hq, Hkv=Hkv, D=D, page_size=16, seq_lens=lens, q_lens=qls,
+                   seed=21 + D + Hq)
     out, st, _ = _run(c)
     assert st == 0
     compare_out(out, _want(c))
