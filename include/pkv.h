@@ -233,7 +233,9 @@ pkv_status decode_combine(const pkv_dims *dims, const float *o_part,
  * PKV_FLAG_BAD_PAGE (page 0 is read instead).  B * Hkv <= 65535 (else
  * PKV_ERR_UNSUPPORTED).  status (device, nullable) receives the flags.  No
  * workspace; graph-capturable.  Runs on the 5th-generation tensor cores
- * (tcgen05.mma, accumulators in tensor memory). */
+ * (tcgen05.mma, accumulators in tensor memory); at D = 128 each block holds
+ * all 512 tensor-memory columns of its SM while it runs, so kernels of other
+ * streams that allocate tensor memory wait for it on that SM. */
 pkv_status paged_prefill_attn(const pkv_dims *dims, const void *q, const int32_t *qo_indptr,
                               int total_q, int max_q_len, const void *k_pool, const void *v_pool,
                               const int32_t *kv_indices, const int32_t *kv_indptr,
