@@ -148,6 +148,30 @@ def cached_traffic(workload: str, splits: int):
         return None
 
 
+def measure_read_peak(dev, stream, reps=10):
+    """GB/s of a plain streaming read on this GPU: torch.sum over a 4 GiB
+    float32 buffer (32x L2), median of `reps` timed with events."""
+    import torch
+    buf = torch.ones(1 << 30, dtype=torch.float32, device=dev)
+    sink = torch.empty((), dtype=torch.float32, device=dev)
+    for _ in range(3):
+        torch.sum(buf, dim=0, out=sink)
+    ms = []
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        torch.sum(buf, dim=0, out=sink)
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        ms.append(a.elapsed_time(b))
+    del buf
+    return buf_bytes_gbs(1 << 32, statistics.median(ms))
+
+
+def buf_bytes_gbs(nbytes, ms):
+    return nbytes / (ms * 1e-3) / 1e9
+
+
 class ClockSampler:
     """nvidia-smi sampling of SM clock and throttle reasons while running."""
 
@@ -733,6 +757,7 @@ def run_pkv(args):
     dec_bytes = kv_bytes + w.B * w.Hq * w.D * 2 * 2 + 4 * n_idx + 8 * w.B
     peak, peak_kind = load_peaks()
     achieved = alg_bytes / (ms_step * 1e-3) / 1e9
+    read_peak = measure_read_peak(dev, stream)
     traffic = cached_traffic(w.name, S) if args.layout == "paged" else None
     clocks = clk.summary(wall0, wall0 + wall)
 
@@ -768,7 +793,11 @@ def run_pkv(args):
                      "frac": round(achieved / peak, 4), "traffic": traffic,
                      "peak_source": f"{peak_kind} (copy bandwidth)",
                      "us_per_launch": round(1e3 * ms_step, 2),
-                     "alg_bytes_per_launch": alg_bytes},
+                     "alg_bytes_per_launch": alg_bytes,
+                     "read_peak": {"gbs": round(read_peak, 1),
+                                   "frac": round(achieved / read_peak, 4),
+                                   "how": "torch.sum over a 4 GiB float32 buffer on this GPU, "
+                                          "median of 10 (a plain streaming read)"}},
         "cold_single_step": {"us": round(1e3 * ms_cold_max, 2),
                              "kv_read_gbs": round(total_bytes / (ms_cold_max * 1e-3) / 1e9, 1),
                              "note": "one step per replay, L2 flushed before it; includes the "
