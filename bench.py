@@ -1,19 +1,31 @@
 #!/usr/bin/env python3
-"""Benchmark of one decode step of paged GQA attention on GB300.
+"""Benchmark of paged GQA split-KV decode attention on GB300.
 
-A step is the whole hot path over one batch: fused RoPE + K/V append, the
-split-KV decode kernel and the combine (the split count comes from the
-library's planner).  The default workload is the batched ragged decode
-(B=32, Hq=32, Hkv=8, D=128, page_size=16, seq_lens uniform in [512, 4096],
-pages scattered over a 65536-page pool).
+A step is the whole hot path over one batch: the new token's RoPE + K/V
+append, the split-KV decode and the merge of the split partials, as one
+paged_decode_step call (split count from the library's planner).
 
-Printed: one JSON line.  ``value`` is the KV-read throughput of the step:
-the bytes of K and V the attention must read (every token of every row,
-every kv head) divided by the step time, summed over ranks.  The L2 is
-flushed (a 2x-L2 write) between timed steps, outside the timed events.
+Headline workload: the largest single-GPU configuration, the serving mix at
+B=128 (Hq=64, Hkv=8, D=128, page_size=16, lognormal lengths, a quarter of the
+rows padding at seq_len 0).  Its K+V (598 MB) is several times the L2, so its
+steps run back to back inside CUDA-graph replays with no flush: a step finds
+none of the previous step's K/V in L2.  The timed region holds exactly
+--steps steps, in at least 10 replays of `inner` steps; the line reports the
+region's mean per step and the replays' median, min and max.
+
+``value`` is the KV-read throughput: the bytes of K and V the attention must
+read (every token of every row, every kv head) divided by the step time,
+summed over ranks.
+
+Every other seeded configuration is measured in the same run (``configs``):
+tiny, gqa_1b, ragged_b32, long_32k and the serving mix at B=1..64.  Inputs of
+at least twice the L2 run back to back as above; smaller ones are timed two
+ways: "rotation" (consecutive steps each read their own copy of the pools, as
+consecutive layers of a model do, the copies holding at least 3x L2) and
+"flushed" (one step per replay, the L2 flushed before it, outside the events).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
-                  [--splits S] [--pool-pages P] [--impl pkv|reference]
+                  [--configs all|none|NAME,...] [--impl pkv|reference]
 
 ``--impl reference`` times the fp64 CPU oracle on the host cores instead (a
 bounded sample of the same workload each step).  Under torchrun (N > 1)
@@ -40,19 +52,28 @@ if ROOT not in sys.path:
 
 METRIC = "paged GQA decode attn: µs/call and KV-read GB/s (% of GB300 HBM peak)"
 FALLBACK_HBM_GBS = 6800.0
+HEADLINE = "serving_b128"
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "fused_decode_traffic.json")
 DECODE_SRC = os.path.join(ROOT, "paged_kv_gqa_16_gb300", "csrc", "pkv_fused.cu")
+
+
+def config_names():
+    from paged_kv_gqa_16_gb300 import workloads as wl
+    return ["tiny", "gqa_1b", "ragged_b32", "long_32k"] + [f"serving_b{B}"
+                                                          for B in wl.SERVING_BATCHES]
 
 
 def parse_args(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=5000)
-    ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--workload", default="ragged_b32")
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=HEADLINE)
+    ap.add_argument("--configs", default="all",
+                    help="the per-configuration map: all, none, or a comma list of names")
     ap.add_argument("--splits", type=int, default=0, help="override the planner's split count")
     ap.add_argument("--pool-pages", type=int, default=0,
-                    help="pool size of the ragged workload (smaller pools for profiling)")
+                    help="pool size of the headline workload (smaller pools for profiling)")
     ap.add_argument("--impl", choices=["pkv", "reference"], default="pkv")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -67,11 +88,29 @@ def parse_args(argv=None):
     ap.add_argument("--no-loop", action="store_true",
                     help="skip the decode-loop leg (paged_kv_advance + step per graph)")
     ap.add_argument("--no-flush", action="store_true", help="skip the L2 flush (not for reporting)")
-    ap.add_argument("--flush-always", action="store_true",
-                    help="flush the L2 before every step even when the inputs exceed it")
-    ap.add_argument("--cpu-seconds", type=float, default=15.0,
-                    help="target CPU time of the oracle baseline sample")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="target CPU time of the all-core oracle baseline sample")
+    ap.add_argument("--cpu-seconds-1t", type=float, default=6.0,
+                    help="target CPU time of the one-thread oracle baseline sample")
     return ap.parse_args(argv)
+
+
+def config_of(w, gpus: int, layout: str = "paged") -> dict:
+    """The workload as the JSON line names it (the same for both arms)."""
+    return {"workload": w.name + ("" if layout == "paged" else " (contiguous cache)"),
+            "layout": layout, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D,
+            "page_size": w.page_size, "num_pages": w.num_pages, "tokens": w.total_tokens,
+            "live_rows": int((w.seq_lens > 0).sum()), "kv_bytes": w.kv_bytes(),
+            "max_seq_len": w.max_seq_len, "parallelism": f"replicas x{gpus}"}
+
+
+def alg_bytes_of(w) -> int:
+    """Algorithmic bytes of one step: K and V of every token, q in and the
+    output, the new token's K/V read and written to its slot, and the page
+    tables (kv_indices, kv_indptr, seq_lens)."""
+    n_idx = int(w.kv_indices.numel())
+    return (w.kv_bytes() + w.B * w.Hq * w.D * 2 * 2 + w.B * w.Hkv * w.D * 2 * 2 * 2
+            + 4 * n_idx + 8 * w.B)
 
 
 # --------------------------------------------------------------------------
@@ -245,15 +284,14 @@ def cpu_cores():
         return os.cpu_count() or 1
 
 
-def oracle_sample(w, target_s: float, max_reps: int = 1000):
+def oracle_sample(w, target_s: float, max_reps: int = 1000, threads: int | None = None):
     """Time the fp64 oracle's step (append + decode) on the host cores over a
     bounded sample of the workload: whole rows, taken in order until their
     estimated cost reaches the target, repeated while time remains."""
     import numpy as np
     import oracle
-    from paged_kv_gqa_16_gb300 import workloads as wl
 
-    cores = cpu_cores()
+    cores = cpu_cores() if threads is None else threads
     oracle.set_threads(cores)
     kp, vp, idx = w.compact_host()
     lens = w.seq_lens.numpy()
@@ -323,9 +361,7 @@ def run_reference(args):
         "n_gpus": args.gpus, "steps": steps, "warmup": warm,
         "ms_per_step": round(1e3 * tot_s / steps, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name + ("" if args.layout == "paged" else " (contiguous cache)"),
-                   "layout": args.layout, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D,
-                   "page_size": w.page_size, "num_pages": w.num_pages},
+        "config": config_of(w, args.gpus, args.layout),
         "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": res["cores"],
                          "kind": "oracle",
                          "sample": f"fp64 oracle append+decode on rows 0..{res['rows'] - 1} of "
@@ -337,22 +373,6 @@ def run_reference(args):
     return 0
 
 
-
-# Prefill / extend shapes: the pages' 512-token prompts at the 1B-class head
-# shape, a long prefill, and an extend of 256 new tokens on 2,048-token rows.
-PREFILL_SHAPES = {
-    "prefill_b32_512": ("prefill B=32 x 512 (Hq 32, Hkv 8, D 64)",
-                        dict(B=32, Hq=32, Hkv=8, D=64, page_size=16, seq_lens=[512] * 32,
-                             q_lens=[512] * 32)),
-    "prefill_b4_4096": ("prefill B=4 x 4096 (Hq 32, Hkv 8, D 128)",
-                        dict(B=4, Hq=32, Hkv=8, D=128, page_size=16, seq_lens=[4096] * 4,
-                             q_lens=[4096] * 4)),
-    "extend_b16": ("extend B=16, 256 new of 2048 (Hq 32, Hkv 8, D 128)",
-                   dict(B=16, Hq=32, Hkv=8, D=128, page_size=16, seq_lens=[2048] * 16,
-                        q_lens=[256] * 16)),
-}
-
-
 def prefill_leg(pkv, wl, dev, stream, flush_l2, rank, names, reps=20):
     """paged_prefill_attn on each named shape: one call per graph replay, the
     L2 flushed before each, median of `reps`; tensor roofline against the
@@ -361,8 +381,8 @@ def prefill_leg(pkv, wl, dev, stream, flush_l2, rank, names, reps=20):
     tf_peak = load_bf16_peak()
     out_rows = []
     for name in names:
-        label, kw = PREFILL_SHAPES[name]
-        c = wl.prefill("prefill", seed=rank, **kw)
+        label, kw = wl.PREFILL_SHAPES[name]
+        c = wl.prefill_shape(name, seed=rank)
         pt = c.w.to_device(dev)
         pd = pkv.dims(c.w.B, c.w.Hq, c.w.Hkv, c.w.D, c.w.page_size, pt["k_pool"].shape[0],
                       int(c.w.kv_indices.numel()), c.w.max_seq_len, c.w.scale)
@@ -424,12 +444,164 @@ def run_prefill_only(args):
         flush_w.zero_()
         torch.sum(flush_r, dim=0, out=sink)
 
-    names = list(PREFILL_SHAPES) if args.only_prefill == "all" else [args.only_prefill]
+    names = list(wl.PREFILL_SHAPES) if args.only_prefill == "all" else [args.only_prefill]
     rows = prefill_leg(pkv, wl, dev, torch.cuda.current_stream(dev), flush_l2, 0, names,
                        reps=max(1, args.steps))
     print(json.dumps({"metric": "paged prefill / extend attention TFLOP/s", "unit": "TFLOP/s",
                       "n_gpus": 1, "prefill": rows}), flush=True)
     return 0
+
+
+# --------------------------------------------------------------------------
+class StepState:
+    """Device state of one workload for timing paged_decode_step: the pools
+    (``copies`` copies of every referenced page, copy i at page ids
+    i * P + id), one page table per copy, the shared q / new K/V / lengths,
+    the workspace, the RoPE table and the output."""
+
+    def __init__(self, pkv, w, dev, copies: int = 1, pool_pages: int = 0, splits: int = 0):
+        import torch
+        P = pool_pages or w.num_pages
+        self.w, self.dev, self.copies, self.P = w, dev, copies, P
+        shape = (copies * P, w.page_size, w.Hkv, w.D)
+        self.k_pool = torch.full(shape, float("nan"), dtype=torch.bfloat16, device=dev)
+        self.v_pool = torch.full(shape, float("nan"), dtype=torch.bfloat16, device=dev)
+        idx = w.kv_indices.to(device=dev, dtype=torch.long)
+        if idx.numel():
+            kpg, vpg = w.k_pages.to(dev), w.v_pages.to(dev)
+            for i in range(copies):
+                self.k_pool[i * P + idx] = kpg
+                self.v_pool[i * P + idx] = vpg
+            del kpg, vpg
+        base = w.kv_indices.to(dev)
+        self.tables = [(base + i * P).contiguous() for i in range(copies)]
+        self.q = w.q.to(dev).contiguous()
+        self.k_new = w.k_new.to(dev).contiguous()
+        self.v_new = w.v_new.to(dev).contiguous()
+        self.kv_indptr = w.kv_indptr.to(dev)
+        self.seq_lens = w.seq_lens.to(dev)
+        self.d = pkv.dims(w.B, w.Hq, w.Hkv, w.D, w.page_size, copies * P,
+                          int(w.kv_indices.numel()), w.max_seq_len, w.scale)
+        self.S = splits or pkv.plan(self.d)[0]
+        self.ws = pkv.alloc_workspace(self.d, self.S, dev)
+        self.rope_rows = max(w.max_seq_len, 1)
+        self.rope = torch.empty(self.rope_rows, w.D // 2, 2, dtype=torch.float32, device=dev)
+        pkv.rope_table(self.rope, self.rope_rows, w.D, w.rope_base or 10000.0)
+        self.out = torch.empty(w.B, w.Hq, w.D, dtype=torch.bfloat16, device=dev)
+        self.pkv = pkv
+
+    def step(self, i: int = 0, args=None):
+        """paged_decode_step on copy i (or on the given device inputs)."""
+        q, k_new, v_new, kv_indices, kv_indptr, seq_lens = args or (
+            self.q, self.k_new, self.v_new, self.tables[i], self.kv_indptr, self.seq_lens)
+        self.pkv.paged_decode_step(self.d, q, k_new, v_new, self.k_pool, self.v_pool,
+                                   kv_indices, kv_indptr, seq_lens, self.rope, self.rope_rows,
+                                   self.S, self.ws, self.out)
+
+    def decode(self, i: int = 0):
+        self.pkv.paged_decode_attn(self.d, self.q, self.k_pool, self.v_pool, self.tables[i],
+                                   self.kv_indptr, self.seq_lens, self.S, self.ws, self.out)
+
+    def check_status(self, what: str):
+        s = self.pkv.status_word(self.ws)
+        if s != 0:
+            raise SystemExit(f"device status {s:#x} {what}")
+
+
+def capture(fn, n: int):
+    """One CUDA graph holding n calls of fn(k), k = 0..n-1."""
+    import torch
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for k in range(n):
+            fn(k)
+    return g
+
+
+def replay_times(graph, reps: int, stream, dev, flush=None):
+    """Milliseconds of each of `reps` replays (events on the replay stream),
+    with `flush` run before each replay, outside the events."""
+    import torch
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(reps)]
+    for a, b in evs:
+        if flush is not None:
+            flush()
+        a.record(stream)
+        graph.replay()
+        b.record(stream)
+    torch.cuda.synchronize(dev)
+    return [a.elapsed_time(b) for a, b in evs]
+
+
+def rotation_copies(kv_bytes: int, l2: int) -> int:
+    """Copies of the pools whose K+V together hold at least 3x L2 (2..64)."""
+    return max(2, min(64, -(-3 * l2 // max(kv_bytes, 1))))
+
+
+def measure_config(pkv, w, dev, stream, l2, flush_l2, peak, splits=0):
+    """µs per paged_decode_step of one workload, with KV GB/s and the
+    fraction of the HBM peak, timed as the module docstring describes."""
+    import torch
+    kv = w.kv_bytes()
+    alg = alg_bytes_of(w)
+    b2b = kv >= 2 * l2
+    copies = 1 if b2b else rotation_copies(kv, l2)
+    st = StepState(pkv, w, dev, copies=copies, splits=splits)
+    for i in range(copies):
+        st.step(i)
+    torch.cuda.synchronize(dev)
+    st.check_status(f"after warm-up of {w.name}")
+
+    def line(ms, mode, extra=None):
+        r = {"us_per_call": round(1e3 * ms, 2),
+             "kv_gbs": round(kv / (ms * 1e-3) / 1e9, 1),
+             "pct_hbm": round(100.0 * kv / (ms * 1e-3) / 1e9 / peak, 1),
+             "roofline_frac": round(alg / (ms * 1e-3) / 1e9 / peak, 4),
+             "l2": mode}
+        r.update(extra or {})
+        return r
+
+    out = {"splits": st.S, "kv_bytes": kv, "alg_bytes": alg, "tokens": w.total_tokens}
+    if b2b:
+        inner = 20
+        g = capture(lambda k: st.step(0), inner)
+        replay_times(g, 3, stream, dev)
+        ms = [t / inner for t in replay_times(g, 15, stream, dev)]
+        out.update(line(statistics.median(ms), f"back to back, {inner} steps per replay, "
+                                               f"K+V = {kv / l2:.1f} x L2, no flush",
+                        {"replays": 15}))
+    else:
+        n = max(copies, 20 // copies * copies)
+        g = capture(lambda k: st.step(k % copies), n)
+        replay_times(g, 3, stream, dev)
+        ms = [t / n for t in replay_times(g, 15, stream, dev)]
+        out.update(line(statistics.median(ms),
+                        f"rotation over {copies} copies of the pools "
+                        f"({copies * kv / l2:.1f} x L2 of K+V), {n} steps per replay",
+                        {"replays": 15}))
+        g1 = capture(lambda k: st.step(0), 1)
+        replay_times(g1, 3, stream, dev, flush_l2)
+        ms1 = replay_times(g1, 30, stream, dev, flush_l2)
+        out["flushed"] = line(statistics.median(ms1),
+                              "one step per replay, L2 flushed before it (outside the events)",
+                              {"replays": 30})
+        del g1
+    torch.cuda.synchronize(dev)
+    st.check_status(f"after timing {w.name}")
+    del g, st
+    torch.cuda.empty_cache()
+    return out
+
+
+def pick_inner(K: int) -> int:
+    """Steps per timed replay: the largest divisor of K that is at most
+    min(20, K // 10), so the K timed steps form at least 10 replays."""
+    cap = max(1, min(20, K // 10))
+    for d in range(cap, 0, -1):
+        if K % d == 0:
+            return d
+    return 1
 
 
 def run_pkv(args):
@@ -449,20 +621,9 @@ def run_pkv(args):
         pkv_build.build()
     barrier(world, dev)
     pkv.lib()
+    stream = torch.cuda.current_stream(dev)
+    peak, peak_kind = load_peaks()
 
-    # each rank: an independent replica of the workload (own seed)
-    kw = {"num_pages": args.pool_pages} if args.pool_pages else {}
-    w = wl.make(args.workload, seed=rank, **kw)
-    t = w.to_device(dev)
-    P = t["k_pool"].shape[0]
-    d = pkv.dims(w.B, w.Hq, w.Hkv, w.D, w.page_size, P, int(w.kv_indices.numel()),
-                 w.max_seq_len, w.scale)
-    S = args.splits or pkv.plan(d)[0]
-    ws = pkv.alloc_workspace(d, S, dev)
-    rope_rows = max(w.max_seq_len, 1)
-    rope = torch.empty(rope_rows, w.D // 2, 2, dtype=torch.float32, device=dev)
-    pkv.rope_table(rope, rope_rows, w.D, w.rope_base or 10000.0)
-    out = torch.empty(w.B, w.Hq, w.D, dtype=torch.bfloat16, device=dev)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush_w = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
     flush_r = torch.zeros(max(2 * l2, 256 << 20) // 4, dtype=torch.int32, device=dev)
@@ -475,16 +636,13 @@ def run_pkv(args):
         flush_w.zero_()
         torch.sum(flush_r, dim=0, out=flush_sink)
 
-    def step(q, k_new, v_new, kv_indices, kv_indptr, seq_lens):
-        """One pass of the hot path on the current stream: the new token's
-        RoPE + append, the split decode and the combine (paged_decode_step)."""
-        pkv.paged_decode_step(d, q, k_new, v_new, t["k_pool"], t["v_pool"], kv_indices,
-                              kv_indptr, seq_lens, rope, rope_rows, S, ws, out)
-
-    def decode(q, kv_indices, kv_indptr, seq_lens):
-        pkv.paged_decode_attn(d, q, t["k_pool"], t["v_pool"], kv_indices, kv_indptr,
-                              seq_lens, S, ws, out)
-
+    # ---- the headline workload: each rank an independent replica (own seed)
+    kw = {"num_pages": args.pool_pages} if args.pool_pages else {}
+    w = wl.make(args.workload, seed=rank, **kw)
+    st = StepState(pkv, w, dev, copies=1, splits=args.splits)
+    d, S = st.d, st.S
+    step = st.step
+    decode = st.decode
     if args.layout == "contig":
         # the same rows in a contiguous cache: slot b holds row b's tokens in
         # order (gathered from its pages), NaN past them
@@ -497,95 +655,99 @@ def run_pkv(args):
             L = int(w.seq_lens[b])
             if L == 0:
                 continue
-            pages = t["kv_indices"][ptr_h[b]:ptr_h[b + 1]].long()
-            ck[b, :L] = t["k_pool"][pages].reshape(-1, w.Hkv, w.D)[:L]
-            cv[b, :L] = t["v_pool"][pages].reshape(-1, w.Hkv, w.D)[:L]
-        del t["k_pool"], t["v_pool"]
+            pages = st.tables[0][ptr_h[b]:ptr_h[b + 1]].long()
+            ck[b, :L] = st.k_pool[pages].reshape(-1, w.Hkv, w.D)[:L]
+            cv[b, :L] = st.v_pool[pages].reshape(-1, w.Hkv, w.D)[:L]
+        del st.k_pool, st.v_pool
         torch.cuda.empty_cache()
-        d = pkv.dims(w.B, w.Hq, w.Hkv, w.D, cache_len, w.B, w.B, cache_len, w.scale)
-        ws = pkv.alloc_workspace(d, S, dev)
+        cd = pkv.dims(w.B, w.Hq, w.Hkv, w.D, cache_len, w.B, w.B, cache_len, w.scale)
+        cws = pkv.alloc_workspace(cd, S, dev)
+        st.ws = cws
 
-        def step(q, k_new, v_new, kv_indices, kv_indptr, seq_lens):
-            pkv.decode_attn_contig(d, q, ck, cv, seq_lens, S, ws, out, k_new=k_new, v_new=v_new,
-                                   rope_cos_sin=rope, rope_max_pos=rope_rows)
+        def step(i=0, a=None):
+            pkv.decode_attn_contig(cd, st.q, ck, cv, st.seq_lens, S, cws, st.out,
+                                   k_new=st.k_new, v_new=st.v_new, rope_cos_sin=st.rope,
+                                   rope_max_pos=st.rope_rows)
 
-        def decode(q, kv_indices, kv_indptr, seq_lens):
-            pkv.decode_attn_contig(d, q, ck, cv, seq_lens, S, ws, out)
+        def decode(i=0):
+            pkv.decode_attn_contig(cd, st.q, ck, cv, st.seq_lens, S, cws, st.out)
 
         args.no_e2e = True
         args.no_loop = True
+        args.configs = "none"
 
     launches_per_step = (1 if S == 1 else 2) + (1 if args.layout == "contig" else 0)
-    dev_args = (t["q"], t["k_new"], t["v_new"], t["kv_indices"], t["kv_indptr"], t["seq_lens"])
-
     for _ in range(max(3, args.warmup)):
-        step(*dev_args)
+        step()
     torch.cuda.synchronize(dev)
-    if pkv.status_word(ws) != 0:
-        raise SystemExit(f"device status {pkv.status_word(ws):#x} after warm-up")
+    st.check_status("after warm-up")
 
-    # Timing.  Inputs at least twice the L2 size are streamed back to back:
-    # INNER consecutive steps are captured in one CUDA graph (each step's
-    # kernels chained to the previous ones, as in a decode loop) and replayed
-    # between one pair of events; a step's K/V are evicted by the time the
-    # next step reads them.  Smaller inputs: one step per graph, the L2
-    # flushed before every step outside the events.
     kv_bytes = w.kv_bytes()
-    back_to_back = kv_bytes >= 2 * l2 and not args.flush_always
-    inner = 20 if back_to_back else 1
+    alg_bytes = alg_bytes_of(w)
+    back_to_back = kv_bytes >= 2 * l2
+    K = max(1, args.steps)
+    inner = pick_inner(K)
+    reps = K // inner
+    g_step = capture(lambda k: step(), inner)
+    replay_times(g_step, 3, stream, dev)
+    est_ms = statistics.median(replay_times(g_step, 3, stream, dev))
+    flush = None if (back_to_back or args.no_flush) else flush_l2
 
-    def capture(fn):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            for _ in range(inner):
-                fn()
-        return g
-
-    g_step = capture(lambda: step(*dev_args))
-    g_dec = capture(lambda: decode(t["q"], t["kv_indices"], t["kv_indptr"], t["seq_lens"]))
-    g_one = torch.cuda.CUDAGraph()                  # one flushed step, for the cold figure
-    with torch.cuda.graph(g_one):
-        step(*dev_args)
-    for _ in range(3):
-        g_step.replay()
-        g_dec.replay()
-        g_one.replay()
-    stream = torch.cuda.current_stream(dev)
-
-    def timed(graph, K, flush_each):
-        """Per-step milliseconds: events around each replay / steps per replay."""
-        reps = max(1, -(-K // inner)) if not flush_each else K
+    # Timed region: exactly K steps in `reps` replays.  The clock sampler
+    # runs across an untimed burst of the same replays just before it (the
+    # region itself can be a few milliseconds, shorter than the sampling
+    # period) and across the region.
+    with ClockSampler(dev.index) as clk:
+        time.sleep(0.3)              # let the sampler start
+        t_clk0 = time.perf_counter()
+        n_burst = max(1, int(0.8 / max(est_ms * 1e-3, 1e-6)))
+        for _ in range(n_burst):
+            if flush is not None:
+                flush()
+            g_step.replay()
+        barrier(world, dev)
+        torch.cuda.synchronize(dev)
+        e_start = torch.cuda.Event(enable_timing=True)
+        e_end = torch.cuda.Event(enable_timing=True)
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(reps)]
-        for k in range(reps):
-            if flush_each and not args.no_flush:
-                flush_l2()
-            evs[k][0].record(stream)
-            graph.replay()
-            evs[k][1].record(stream)
-        torch.cuda.synchronize(dev)
-        per = 1 if flush_each else inner
-        return [a.elapsed_time(b) / per for a, b in evs]
-
-    K = args.steps
-    barrier(world, dev)
-    torch.cuda.synchronize(dev)
-    with ClockSampler(dev.index) as clk:
-        time.sleep(0.4)              # let the sampler start before the timed region
         wall0 = time.perf_counter()
-        step_ms = timed(g_step, K, not back_to_back)
+        e_start.record(stream)
+        for a, b in evs:
+            if flush is not None:
+                flush()
+            a.record(stream)
+            g_step.replay()
+            b.record(stream)
+        e_end.record(stream)
+        torch.cuda.synchronize(dev)
         wall = time.perf_counter() - wall0
-    barrier(world, dev)
-    dec_ms = timed(g_dec, max(50, min(K, 2000)), not back_to_back)
-    cold_ms = timed(g_one, max(20, min(K // 10, 500)), True)
-    ms_step = statistics.mean(step_ms)
-    ms_dec = statistics.mean(dec_ms)
-    ms_step_max = reduce_max(ms_step, world, dev)
-    ms_dec_max = reduce_max(ms_dec, world, dev)
-    ms_cold_max = reduce_max(statistics.mean(cold_ms), world, dev)
+        barrier(world, dev)
+        t_clk1 = time.perf_counter()
+        time.sleep(0.1)
+    per_step = [a.elapsed_time(b) / inner for a, b in evs]
+    # with flushes inside the region, its span includes them: use the replays
+    ms_region = (e_start.elapsed_time(e_end) / K) if flush is None else statistics.mean(per_step)
+    ms_step_max = reduce_max(ms_region, world, dev)
+    st.check_status("after the timed run")
+    clocks = clk.summary(t_clk0, t_clk1)
+    clocks["window"] = (f"{n_burst} untimed replays just before the timed region, "
+                        "then the timed region")
 
     total_bytes = kv_bytes * world
     value = total_bytes / (ms_step_max * 1e-3) / 1e9
+
+    # decode-only and a cold single step (L2 flushed before it) on the same rows
+    g_dec = capture(lambda k: decode(), inner)
+    replay_times(g_dec, 3, stream, dev)
+    ms_dec = statistics.median(t / inner for t in replay_times(g_dec, max(10, reps), stream,
+                                                              dev, flush))
+    g_one = capture(lambda k: step(), 1)
+    replay_times(g_one, 3, stream, dev, flush_l2)
+    ms_cold = statistics.median(replay_times(g_one, 30, stream, dev, flush_l2))
+    ms_dec_max = reduce_max(ms_dec, world, dev)
+    ms_cold_max = reduce_max(ms_cold, world, dev)
+    del g_dec, g_one
 
     # e2e: host (pinned) inputs copied in, the step, the output copied back.
     # The step's inputs sit in one pinned host block (each at a 256-byte
@@ -610,28 +772,17 @@ def run_pkv(args):
             blk_view(host_blk, k).copy_(srcs[k])
         dev_blk = torch.empty(blk_bytes, dtype=torch.uint8, device=dev)
         e_args = tuple(blk_view(dev_blk, k) for k in names)
-        out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        out_host = torch.empty(st.out.shape, dtype=st.out.dtype).pin_memory()
         h2d = blk_bytes
         d2h = out_host.numel() * out_host.element_size()
         g_e2e = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g_e2e):
             dev_blk.copy_(host_blk, non_blocking=True)
-            step(*e_args)
-            out_host.copy_(out, non_blocking=True)
-        for _ in range(3):
-            g_e2e.replay()
+            step(0, e_args)
+            out_host.copy_(st.out, non_blocking=True)
+        replay_times(g_e2e, 3, stream, dev)
         Ke = max(10, min(K, 500))
-        e_evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                 for _ in range(Ke)]
-        torch.cuda.synchronize(dev)
-        for k in range(Ke):
-            if not args.no_flush and not back_to_back:
-                flush_l2()
-            e_evs[k][0].record(stream)
-            g_e2e.replay()
-            e_evs[k][1].record(stream)
-        torch.cuda.synchronize(dev)
-        e_ms = statistics.mean(a.elapsed_time(b) for a, b in e_evs)
+        e_ms = statistics.mean(replay_times(g_e2e, Ke, stream, dev, flush))
         e_ms = reduce_max(e_ms, world, dev)
         e2e = {"value": round(total_bytes / (e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                "ms_per_step": round(e_ms, 5), "h2d_bytes_per_step": h2d,
@@ -639,59 +790,88 @@ def run_pkv(args):
                "path": "pinned host block -> one H2D copy, the step, one D2H copy of the "
                        "output, captured in one CUDA graph per step"}
         del g_e2e, dev_blk
+        st.check_status("after the e2e leg")
 
-    status = pkv.status_word(ws)
-    if status != 0:
-        raise SystemExit(f"device status {status:#x} after the timed run")
+    achieved = alg_bytes / (ms_region * 1e-3) / 1e9
+    read_peak = measure_read_peak(dev, stream)
+    traffic = cached_traffic(w.name, S) if args.layout == "paged" else None
+    del g_step
+    st_config = config_of(w, world, args.layout)
+    headline_entry = {"splits": S, "kv_bytes": kv_bytes, "alg_bytes": alg_bytes,
+                      "tokens": w.total_tokens, "us_per_call": round(1e3 * ms_region, 2),
+                      "kv_gbs": round(kv_bytes / (ms_region * 1e-3) / 1e9, 1),
+                      "pct_hbm": round(100.0 * kv_bytes / (ms_region * 1e-3) / 1e9 / peak, 1),
+                      "roofline_frac": round(achieved / peak, 4),
+                      "l2": "the headline's timed region (see config)"}
+    if args.layout != "paged":
+        headline_entry = None
+    del st
+    torch.cuda.empty_cache()
 
-    # decode loop: the same rows as a loop whose table grows on the device.
+    # ---- every seeded configuration -------------------------------------
+    configs = {}
+    ragged = None
+    if args.configs != "none":
+        names_c = config_names() if args.configs == "all" else args.configs.split(",")
+        for name in names_c:
+            if name == w.name and headline_entry is not None:
+                configs[name] = headline_entry
+                continue
+            wc = wl.make(name, seed=rank)
+            configs[name] = measure_config(pkv, wc, dev, stream, l2, flush_l2, peak)
+            if name == "ragged_b32":
+                ragged = wc
+            del wc
+
+    # decode loop: the ragged rows as a loop whose table grows on the device.
     # LOOP steps per graph, each paged_kv_advance + paged_decode_step (the
     # step's new token at the advanced length), against the same graph
     # without the advance; the small state is reset between replays, outside
     # the events, and nothing is flushed (consecutive steps, as in serving).
     loop = None
     if not args.no_loop:
-        LOOP, reps = 20, 20
-        before = (w.seq_lens - 1).clamp(min=0).tolist()     # cached tokens before a step
-        held_max = max(-(-L // w.page_size) for L in before)
-        cap = held_max + -(-LOOP // w.page_size) + 2
-        need = sum(-(-L // w.page_size) for L in before) + w.B * (-(-LOOP // w.page_size) + 1)
-        ls = wl.decode_loop(B=w.B, Hq=w.Hq, Hkv=w.Hkv, D=w.D, page_size=w.page_size,
+        wr = ragged if ragged is not None else wl.make("ragged_b32", seed=rank)
+        LOOP, lreps = 20, 20
+        before = (wr.seq_lens - 1).clamp(min=0).tolist()     # cached tokens before a step
+        held_max = max(-(-L // wr.page_size) for L in before)
+        cap = held_max + -(-LOOP // wr.page_size) + 2
+        need = sum(-(-L // wr.page_size) for L in before) + wr.B * (-(-LOOP // wr.page_size) + 1)
+        ls = wl.decode_loop(B=wr.B, Hq=wr.Hq, Hkv=wr.Hkv, D=wr.D, page_size=wr.page_size,
                             seq_lens=before, steps=LOOP, cap=cap, num_pages=need + 64,
                             seed=1000 + rank)
 
         def t16(a):
             return torch.from_numpy(a.view(np.int16).copy()).view(torch.bfloat16).to(dev)
 
-        ld = pkv.dims(w.B, w.Hq, w.Hkv, w.D, w.page_size, ls.num_pages, len(ls.kv_indices),
-                      ls.max_seq_len, w.scale)
+        ld = pkv.dims(wr.B, wr.Hq, wr.Hkv, wr.D, wr.page_size, ls.num_pages, len(ls.kv_indices),
+                      ls.max_seq_len, wr.scale)
         lS = args.splits or pkv.plan(ld)[0]
         lws = pkv.alloc_workspace(ld, lS, dev)
         lq, lkn, lvn = t16(ls.q), t16(ls.k_new), t16(ls.v_new)
         lkp, lvp = t16(ls.k_pool), t16(ls.v_pool)
-        lrope = torch.empty(ls.max_seq_len, w.D // 2, 2, dtype=torch.float32, device=dev)
-        pkv.rope_table(lrope, ls.max_seq_len, w.D, w.rope_base or 10000.0)
+        lrope = torch.empty(ls.max_seq_len, wr.D // 2, 2, dtype=torch.float32, device=dev)
+        pkv.rope_table(lrope, ls.max_seq_len, wr.D, wr.rope_base or 10000.0)
         lsl0 = torch.from_numpy(ls.seq_lens).to(dev)
         lind0 = torch.from_numpy(ls.kv_indices).to(dev)
         lsl, lind = lsl0.clone(), lind0.clone()
         lptr = torch.from_numpy(ls.kv_indptr).to(dev)
         lfree = torch.from_numpy(ls.free_pages).to(dev)
         lhead = torch.zeros(1, dtype=torch.int32, device=dev)
-        lout = torch.empty(w.B, w.Hq, w.D, dtype=torch.bfloat16, device=dev)
+        lout = torch.empty(wr.B, wr.Hq, wr.D, dtype=torch.bfloat16, device=dev)
 
-        def one(st, adv):
+        def one(stp, adv):
             if adv == "fused":
                 # the loop opens with one advance; each step then advances
                 # for the next inside its own combine launch
-                if st == 0:
+                if stp == 0:
                     pkv.paged_kv_advance(ld, lsl, lptr, lind, lfree, lhead, status=lws)
-                pkv.paged_decode_step_advance(ld, lq, lkn[st], lvn[st], lkp, lvp, lind, lptr,
+                pkv.paged_decode_step_advance(ld, lq, lkn[stp], lvn[stp], lkp, lvp, lind, lptr,
                                               lsl, lrope, ls.max_seq_len, lS, lws, lout,
                                               lfree, lhead)
                 return
             if adv:
                 pkv.paged_kv_advance(ld, lsl, lptr, lind, lfree, lhead, status=lws)
-            pkv.paged_decode_step(ld, lq, lkn[st], lvn[st], lkp, lvp, lind, lptr, lsl, lrope,
+            pkv.paged_decode_step(ld, lq, lkn[stp], lvn[stp], lkp, lvp, lind, lptr, lsl, lrope,
                                   ls.max_seq_len, lS, lws, lout)
 
         def reset():
@@ -701,24 +881,19 @@ def run_pkv(args):
 
         def loop_graph(adv):
             reset()
-            for st in range(LOOP):
-                one(st, adv)
+            for stp in range(LOOP):
+                one(stp, adv)
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g):
-                for st in range(LOOP):
-                    one(st, adv)
+                for stp in range(LOOP):
+                    one(stp, adv)
             return g
 
         def loop_timed(g):
             ms = []
-            for _ in range(reps + 3):
+            for _ in range(lreps + 3):
                 reset()
-                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                a.record(stream)
-                g.replay()
-                b.record(stream)
-                torch.cuda.synchronize(dev)
-                ms.append(a.elapsed_time(b) / LOOP)
+                ms.append(replay_times(g, 1, stream, dev)[0] / LOOP)
             return statistics.median(ms[3:])
 
         g_adv, g_noadv, g_fused = loop_graph(True), loop_graph(False), loop_graph("fused")
@@ -728,7 +903,7 @@ def run_pkv(args):
         ms_noadv = loop_timed(g_noadv)
         if pkv.status_word(lws) != 0:
             raise SystemExit(f"device status {pkv.status_word(lws):#x} after the loop leg")
-        loop = {"steps_per_graph": LOOP, "replays": reps,
+        loop = {"workload": wr.name, "steps_per_graph": LOOP, "replays": lreps,
                 "us_per_step": round(1e3 * ms_adv, 2),
                 "us_per_step_without_advance": round(1e3 * ms_noadv, 2),
                 "advance_us": round(1e3 * (ms_adv - ms_noadv), 2),
@@ -743,71 +918,64 @@ def run_pkv(args):
     # prefill / extend: paged_prefill_attn on three shapes (see prefill_leg)
     prefill = None
     if not args.no_prefill and args.layout == "paged":
-        prefill = prefill_leg(pkv, wl, dev, stream, flush_l2, rank, list(PREFILL_SHAPES))
-
-    # roofline of the dominant kernel, the fused step kernel (its launch is
-    # timed as the step call, so the small piece combine is included).
-    # Algorithmic bytes per call: K and V of every token, q, the new token's
-    # K/V read and written to its slot, the output, and the page tables.
-    n_idx = int(w.kv_indices.numel())
-    io_bytes = (w.B * w.Hq * w.D * 2 * 2            # q in, out
-                + w.B * w.Hkv * w.D * 2 * 2 * 2     # k_new/v_new in, slot writes
-                + 4 * n_idx + 8 * w.B)              # kv_indices, kv_indptr, seq_lens
-    alg_bytes = kv_bytes + io_bytes
-    dec_bytes = kv_bytes + w.B * w.Hq * w.D * 2 * 2 + 4 * n_idx + 8 * w.B
-    peak, peak_kind = load_peaks()
-    achieved = alg_bytes / (ms_step * 1e-3) / 1e9
-    read_peak = measure_read_peak(dev, stream)
-    traffic = cached_traffic(w.name, S) if args.layout == "paged" else None
-    clocks = clk.summary(wall0, wall0 + wall)
+        prefill = prefill_leg(pkv, wl, dev, stream, flush_l2, rank, list(wl.PREFILL_SHAPES))
 
     if rank != 0:
         return 0
     cpu = None
     if not args.no_cpu_baseline:
         res = oracle_sample(w, args.cpu_seconds)
+        one_t = oracle_sample(w, args.cpu_seconds_1t, threads=1)
         cpu = {"value": round(res["gbs"], 4), "unit": "GB/s", "cores": res["cores"],
                "kind": "oracle",
                "sample": f"fp64 oracle append+decode, rows 0..{res['rows'] - 1} of {w.name} "
-                         f"x{res['reps']} ({res['seconds']:.1f} s)"}
+                         f"x{res['reps']} ({res['seconds']:.1f} s, OpenMP over (row, head))",
+               "single_thread": {"value": round(one_t["gbs"], 4), "unit": "GB/s", "cores": 1,
+                                 "sample": f"rows 0..{one_t['rows'] - 1} of {w.name} "
+                                           f"x{one_t['reps']} ({one_t['seconds']:.1f} s)"}}
+    spread = {"replays": reps, "steps_per_replay": inner,
+              "median_us": round(1e3 * statistics.median(per_step), 2),
+              "min_us": round(1e3 * min(per_step), 2),
+              "max_us": round(1e3 * max(per_step), 2)}
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": K, "warmup": max(3, args.warmup), "ms_per_step": round(ms_step_max, 5),
-        "timing": "CUDA graph replay; events on the replay stream around each replay",
+        "timing": (f"CUDA graph replay, {inner} steps per replay x {reps} replays = the K "
+                   "timed steps; events on the replay stream around the region and each "
+                   "replay; ms_per_step = region / K"),
+        "spread": spread,
         "us_per_call": round(1e3 * ms_step_max, 2),
         "pct_hbm_peak": round(100.0 * value / world / peak, 1),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D,
-                   "page_size": w.page_size, "num_pages": P, "tokens": w.total_tokens,
-                   "kv_bytes": kv_bytes, "num_splits": S, "chunk": pkv.split_chunk(d, S),
-                   "l2": (f"inputs larger than L2 (K+V = {kv_bytes / l2:.1f} x L2): {inner} steps "
-                         "back to back per graph replay, no flush" if back_to_back else
-                         "flushed between steps (2x L2 written, then 2x L2 read), outside "
-                         "the timed events") if not args.no_flush else "warm",
-                   "parallelism": f"replicas x{world}"},
+        "config": st_config,
+        "plan": {"num_splits": S, "chunk": pkv.split_chunk(d, S)},
+        "l2": (f"inputs larger than L2 (K+V = {kv_bytes / l2:.1f} x L2): steps back to back "
+               "inside each replay, no flush" if back_to_back else
+               "flushed before every replay (2x L2 written, then 2x L2 read), outside the "
+               "events") if not args.no_flush else "warm",
         "roofline": {"bound": "hbm",
                      "kernel": "fused_decode_kernel (paged_decode_step; its piece combine "
                                "is inside the timed call)",
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
                      "peak_source": f"{peak_kind} (copy bandwidth)",
-                     "us_per_launch": round(1e3 * ms_step, 2),
+                     "us_per_launch": round(1e3 * ms_region, 2),
                      "alg_bytes_per_launch": alg_bytes,
                      "read_peak": {"gbs": round(read_peak, 1),
                                    "frac": round(achieved / read_peak, 4),
                                    "how": "torch.sum over a 4 GiB float32 buffer on this GPU, "
                                           "median of 10 (a plain streaming read)"}},
+        "configs": configs or None,
         "cold_single_step": {"us": round(1e3 * ms_cold_max, 2),
                              "kv_read_gbs": round(total_bytes / (ms_cold_max * 1e-3) / 1e9, 1),
                              "note": "one step per replay, L2 flushed before it; includes the "
-                                     "~6 us event/launch floor of an isolated call"},
+                                     "event/launch floor of an isolated call"},
         "decode_only": {"call": "paged_decode_attn", "us": round(1e3 * ms_dec_max, 2),
-                        "kv_read_gbs": round(kv_bytes / (ms_dec_max * 1e-3) / 1e9, 1),
-                        "alg_gbs": round(dec_bytes / (ms_dec_max * 1e-3) / 1e9, 1)},
-        "gpu_launches": len(step_ms) * (1 if not back_to_back else inner) * launches_per_step,
+                        "kv_read_gbs": round(kv_bytes / (ms_dec_max * 1e-3) / 1e9, 1)},
+        "gpu_launches": K * launches_per_step,
         "clocks": clocks,
-        "wall_s_timed": round(wall, 3),
+        "wall_s_timed": round(wall, 4),
         "e2e": e2e,
         "decode_loop": loop,
         "prefill": prefill,

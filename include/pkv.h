@@ -374,6 +374,19 @@ pkv_status paged_decode_attn_noalloc(const pkv_dims *dims, const void *q,
                                      const int32_t *seq_lens, int num_splits, void *out,
                                      uint32_t *status, pkv_stream_t stream);
 
+/* ---- testing -------------------------------------------------------------- */
+
+/* Test-only: the time limit, in nanoseconds, of the waits that hand a stage
+ * or a q block between the decode kernel's copy warp and its compute warps
+ * (default and maximum: 2,000,000,000).  A shorter limit makes those waits
+ * give up while data is still in flight, so tests can drive the timeout path:
+ * the kernel then sets PKV_FLAG_TIMEOUT in the status word, lets every copy
+ * it has issued land (those waits keep the full limit), and returns; the
+ * call's output is undefined.  Applies to launches made after the call, from
+ * any thread; not for production use.  Returns PKV_ERR_INVALID_ARG above the
+ * default. */
+pkv_status pkv_testing_set_handoff_wait_ns(unsigned long long ns);
+
 const char *pkv_status_str(pkv_status s);
 
 /* ABI version: (major << 16) | minor. */

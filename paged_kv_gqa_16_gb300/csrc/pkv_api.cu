@@ -7,28 +7,8 @@
 #include "pkv.h"
 #include "pkv_internal.h"
 
-namespace {
+namespace pkv {
 
-constexpr size_t kHeaderBytes = 256;
-constexpr int kMaxSplits = 65536;
-constexpr int kMinChunkTokens = 256;   // per-split path: never split finer than this
-
-size_t round_up(size_t x, size_t a)
-{
-    return (x + a - 1) / a * a;
-}
-
-bool aligned(const void *p, uintptr_t a)
-{
-    return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0;
-}
-
-pkv_status launch_status(cudaError_t e)
-{
-    return e == cudaSuccess ? PKV_OK : PKV_ERR_LAUNCH;
-}
-
-// Shape checks common to every entry point.
 pkv_status check_dims(const pkv_dims *d)
 {
     if (d == nullptr)
@@ -47,6 +27,31 @@ pkv_status check_dims(const pkv_dims *d)
     if ((double)d->num_pages * d->page_size * d->Hkv * d->D > 9.0e18)
         return PKV_ERR_INVALID_ARG;
     return PKV_OK;
+}
+
+} // namespace pkv
+
+namespace {
+
+using pkv::check_dims;
+using pkv::kMaxSplits;
+
+constexpr size_t kHeaderBytes = 256;
+constexpr int kMinChunkTokens = 256;   // per-split path: never split finer than this
+
+size_t round_up(size_t x, size_t a)
+{
+    return (x + a - 1) / a * a;
+}
+
+bool aligned(const void *p, uintptr_t a)
+{
+    return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0;
+}
+
+pkv_status launch_status(cudaError_t e)
+{
+    return e == cudaSuccess ? PKV_OK : PKV_ERR_LAUNCH;
 }
 
 int chunk_for(const pkv_dims *d, int num_splits)

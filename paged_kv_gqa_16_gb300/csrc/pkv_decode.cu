@@ -445,20 +445,19 @@ template <int D, int NW, int NSTAGE>
 cudaError_t launch_split_cfg(const DecodeParams &p, cudaStream_t stream)
 {
     using C = SplitCfg<D, NW, NSTAGE>;
-    static bool attr_done = false;   // raising the smem limit is per function
-    if (!attr_done) {
-        cudaError_t e = cudaFuncSetAttribute(split_decode_kernel<D, NW, NSTAGE>,
+    static DeviceOnce attrs;       // raising the smem limit is per function and device
+    const cudaError_t e = attrs.run([] {
+        cudaError_t r = cudaFuncSetAttribute(split_decode_kernel<D, NW, NSTAGE>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              C::kSmemBytes);
-        if (e != cudaSuccess)
-            return e;
-        e = cudaFuncSetAttribute(split_decode_kernel<D, NW, NSTAGE>,
-                                 cudaFuncAttributePreferredSharedMemoryCarveout,
-                                 cudaSharedmemCarveoutMaxShared);
-        if (e != cudaSuccess)
-            return e;
-        attr_done = true;
-    }
+        if (r != cudaSuccess)
+            return r;
+        return cudaFuncSetAttribute(split_decode_kernel<D, NW, NSTAGE>,
+                                    cudaFuncAttributePreferredSharedMemoryCarveout,
+                                    cudaSharedmemCarveoutMaxShared);
+    });
+    if (e != cudaSuccess)
+        return e;
     dim3 grid(p.num_splits, p.Hkv, p.B);
     split_decode_kernel<D, NW, NSTAGE><<<grid, C::kThreads, C::kSmemBytes, stream>>>(p);
     return cudaGetLastError();

@@ -331,7 +331,8 @@ __global__ void __launch_bounds__(FusedCfg<D, HPC>::kThreads, 1)
             // stage the row's q block (and RoPE row) for the consumers
             if (q_staged) {
                 if (pc > 0) {
-                    const bool ok = mbar_wait_bounded(&qbar[1], (uint32_t)((pc - 1) & 1));
+                    const bool ok = mbar_wait_bounded(&qbar[1], (uint32_t)((pc - 1) & 1),
+                                                      p.handoff_wait_ns);
                     if (!__all_sync(kFull, ok) || scratch[0]) {
                         aborted = true;
                         if (lane == 0) {
@@ -358,7 +359,8 @@ __global__ void __launch_bounds__(FusedCfg<D, HPC>::kThreads, 1)
             for (int tok = t0; tok < t1; tok += C::kTok, ++it) {
                 const int st = it % NST;
                 if (it >= NST) {
-                    const bool ok = mbar_wait_bounded(&empty[st], (uint32_t)(((it / NST) - 1) & 1));
+                    const bool ok = mbar_wait_bounded(&empty[st], (uint32_t)(((it / NST) - 1) & 1),
+                                                      p.handoff_wait_ns);
                     if (!__all_sync(kFull, ok) || scratch[0]) {
                         aborted = true;
                         if (lane == 0) {
@@ -415,13 +417,15 @@ __global__ void __launch_bounds__(FusedCfg<D, HPC>::kThreads, 1)
                 }
             }
         }
-        if (aborted) {
-            // let the copies already issued land before the block exits
-            for (int k = (it > NST ? it - NST : 0); k < it; ++k)
-                (void)mbar_wait_bounded(&full[k % NST], (uint32_t)((k / NST) & 1));
-            if (pc > 0)
-                (void)mbar_wait_bounded(&qbar[0], (uint32_t)((pc - 1) & 1));
-        }
+        // Let the copies already issued land before this warp exits, with the
+        // full time limit.  Always, not only when this warp gave up: a
+        // consumer that gave up waiting skips its stages, and the block must
+        // not exit while a copy into its shared memory is in flight.  In a
+        // run without timeouts these phases have completed or are about to.
+        for (int k = (it > NST ? it - NST : 0); k < it; ++k)
+            (void)mbar_wait_bounded(&full[k % NST], (uint32_t)((k / NST) & 1));
+        if (pc > 0)
+            (void)mbar_wait_bounded(&qbar[0], (uint32_t)((pc - 1) & 1));
         // the piece combine may be scheduled once every block has signalled;
         // signalling at the end (not the start) keeps its blocks from piling
         // onto the first SMs to free up
@@ -470,7 +474,8 @@ __global__ void __launch_bounds__(FusedCfg<D, HPC>::kThreads, 1)
             if (q_staged) {
                 // staged by the producer when it started this row
                 if (!aborted) {
-                    const bool ok = mbar_wait_bounded(&qbar[0], (uint32_t)(pc & 1));
+                    const bool ok = mbar_wait_bounded(&qbar[0], (uint32_t)(pc & 1),
+                                                      p.handoff_wait_ns);
                     if (!__all_sync(kFull, ok) || scratch[0]) {
                         aborted = true;
                         if (lane == 0) {
@@ -551,7 +556,8 @@ __global__ void __launch_bounds__(FusedCfg<D, HPC>::kThreads, 1)
         for (int tok = t0; tok < t1; tok += C::kTok, ++it) {
             const int st = it % NST;
             if (!aborted) {
-                const bool ok = mbar_wait_bounded(&full[st], (uint32_t)((it / NST) & 1));
+                const bool ok = mbar_wait_bounded(&full[st], (uint32_t)((it / NST) & 1),
+                                                  p.handoff_wait_ns);
                 if (!__all_sync(kFull, ok) || scratch[0]) {
                     aborted = true;
                     if (lane == 0) {
@@ -856,21 +862,20 @@ template <int D, int HPC>
 cudaError_t launch_fused_cfg(const FusedParams &p, int grid, cudaStream_t stream)
 {
     using C = FusedCfg<D, HPC>;
-    static bool attr_done = false;
-    if (!attr_done) {
-        cudaError_t e = cudaFuncSetAttribute(fused_decode_kernel<D, HPC>,
+    static DeviceOnce attrs;
+    cudaError_t e = attrs.run([] {
+        cudaError_t r = cudaFuncSetAttribute(fused_decode_kernel<D, HPC>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              C::kSmemBytes);
-        if (e != cudaSuccess)
-            return e;
-        e = cudaFuncSetAttribute(fused_decode_kernel<D, HPC>,
-                                 cudaFuncAttributePreferredSharedMemoryCarveout,
-                                 cudaSharedmemCarveoutMaxShared);
-        if (e != cudaSuccess)
-            return e;
-        attr_done = true;
-    }
-    cudaError_t e = launch_pdl(fused_decode_kernel<D, HPC>, dim3(grid), dim3(C::kThreads),
+        if (r != cudaSuccess)
+            return r;
+        return cudaFuncSetAttribute(fused_decode_kernel<D, HPC>,
+                                    cudaFuncAttributePreferredSharedMemoryCarveout,
+                                    cudaSharedmemCarveoutMaxShared);
+    });
+    if (e != cudaSuccess)
+        return e;
+    e = launch_pdl(fused_decode_kernel<D, HPC>, dim3(grid), dim3(C::kThreads),
                                C::kSmemBytes, stream, p);
     if (e != cudaSuccess)
         return e;
@@ -905,12 +910,36 @@ int fused_heads_per_block(int Hkv)
     return 1;
 }
 
-cudaError_t launch_fused_decode(const FusedParams &p, int D, int grid, cudaStream_t stream)
+namespace {
+std::atomic<unsigned long long> g_handoff_wait_ns{kWaitLimitNs};
+} // namespace
+
+unsigned long long handoff_wait_ns()
 {
+    return g_handoff_wait_ns.load(std::memory_order_relaxed);
+}
+
+cudaError_t launch_fused_decode(const FusedParams &params, int D, int grid,
+                                cudaStream_t stream)
+{
+    FusedParams p = params;
+    p.handoff_wait_ns = handoff_wait_ns();
     if (D == 64)
         return launch_fused_d<64>(p, grid, stream);
     return launch_fused_d<128>(p, grid, stream);
 }
+
+} // namespace pkv
+
+extern "C" pkv_status pkv_testing_set_handoff_wait_ns(unsigned long long ns)
+{
+    if (ns > pkv::kWaitLimitNs)
+        return PKV_ERR_INVALID_ARG;
+    pkv::g_handoff_wait_ns.store(ns, std::memory_order_relaxed);
+    return PKV_OK;
+}
+
+namespace pkv {
 
 cudaError_t launch_piece_combine(const PieceCombineParams &p, int D, int grid_blocks,
                                  cudaStream_t stream)

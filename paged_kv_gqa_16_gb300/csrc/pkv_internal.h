@@ -2,12 +2,55 @@
 // libpkv (not part of the public ABI; see include/pkv.h for that).
 #pragma once
 
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
+#include <mutex>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include "pkv.h"
+
 namespace pkv {
+
+// Largest split count any entry point accepts.
+constexpr int kMaxSplits = 65536;
+
+// Shape checks common to every entry point (pkv_api.cu).
+pkv_status check_dims(const pkv_dims *d);
+
+// One-time set-up of a kernel's function attributes (the opt-in shared
+// memory size, the carveout).  Those attributes belong to the current
+// device's context, so a process that launches on several devices sets them
+// once on each; host threads may launch concurrently, hence the lock.
+constexpr int kMaxDevices = 64;
+
+class DeviceOnce {
+public:
+    template <typename F>
+    cudaError_t run(F &&setup)
+    {
+        int dev = -1;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess)
+            return e;
+        if (dev < 0 || dev >= kMaxDevices)
+            return cudaErrorInvalidDevice;
+        if (done_[dev].load(std::memory_order_acquire))
+            return cudaSuccess;
+        std::lock_guard<std::mutex> lock(mu_);
+        if (done_[dev].load(std::memory_order_relaxed))
+            return cudaSuccess;
+        e = setup();
+        if (e == cudaSuccess)
+            done_[dev].store(true, std::memory_order_release);
+        return e;
+    }
+
+private:
+    std::mutex mu_;
+    std::atomic<bool> done_[kMaxDevices]{};
+};
 
 struct AppendParams {
     __nv_bfloat16 *q;
@@ -106,7 +149,14 @@ struct FusedParams {
     const __nv_bfloat16 *v_new;
     const float *rope;                // [rope_max_pos, D/2, 2] or nullptr
     int rope_max_pos;
+    // limit of the waits that hand a stage or the q block between the
+    // producer and the consumers (normally the full ~2 s; shortened only by
+    // the testing call).  Waits for copies already issued keep the full limit.
+    unsigned long long handoff_wait_ns;
 };
+
+// The hand-off wait limit launches use (pkv_testing_set_handoff_wait_ns).
+unsigned long long handoff_wait_ns();
 
 struct PieceCombineParams {
     const float *o_part;

@@ -51,15 +51,24 @@ extern "C" pkv_status paged_decode_attn_noalloc(const pkv_dims *dims, const void
                                                 void *out, uint32_t *status,
                                                 pkv_stream_t stream)
 {
-    const size_t need = pkv_workspace_bytes(dims, num_splits);
-    if (need == 0)
-        return dims == nullptr || num_splits < 1 ? PKV_ERR_INVALID_ARG : PKV_ERR_UNSUPPORTED;
-    if (need > PKV_NOALLOC_SCRATCH_BYTES)
+    // the shape checks of paged_decode_attn, with its status codes
+    const pkv_status dst = pkv::check_dims(dims);
+    if (dst != PKV_OK)
+        return dst;
+    if (num_splits < 1 || num_splits > pkv::kMaxSplits)
+        return PKV_ERR_INVALID_ARG;
+    if (pkv_workspace_bytes(dims, num_splits) > PKV_NOALLOC_SCRATCH_BYTES)
         return PKV_ERR_WORKSPACE_TOO_SMALL;
     if (status != nullptr && (reinterpret_cast<uintptr_t>(status) & 3) != 0)
         return PKV_ERR_INVALID_ARG;
-    if (dims->B == 0)
+    if (dims->B == 0) {
+        // nothing to compute, but the caller's status word still starts this
+        // call at zero
+        if (status != nullptr &&
+            cudaMemsetAsync(status, 0, sizeof(uint32_t), (cudaStream_t)stream) != cudaSuccess)
+            return PKV_ERR_LAUNCH;
         return PKV_OK;
+    }
     void *scratch = nullptr;
     pkv_status st = scratch_for_current_device(&scratch);
     if (st != PKV_OK)

@@ -506,15 +506,13 @@ template <int D>
 cudaError_t launch_row(const PrefillParams &p, int max_q_len, cudaStream_t stream)
 {
     using C = RowCfg<D>;
-    static bool attr_done = false;
-    if (!attr_done) {
-        cudaError_t e = cudaFuncSetAttribute(prefill_row_kernel<D>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             C::kSmemBytes);
-        if (e != cudaSuccess)
-            return e;
-        attr_done = true;
-    }
+    static DeviceOnce attrs;
+    const cudaError_t attr_err = attrs.run([] {
+        return cudaFuncSetAttribute(prefill_row_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    C::kSmemBytes);
+    });
+    if (attr_err != cudaSuccess)
+        return attr_err;
     const long long tiles = ((long long)max_q_len + p.tq - 1) / p.tq;
     const long long rows = (long long)p.B * p.Hkv;
     if (tiles <= 0 || rows <= 0)
@@ -919,15 +917,13 @@ template <int D>
 cudaError_t launch_pair(const PrefillParams &p, int max_q_len, cudaStream_t stream)
 {
     using C = PairCfg<D>;
-    static bool attr_done = false;
-    if (!attr_done) {
-        cudaError_t e = cudaFuncSetAttribute(prefill_pair_kernel<D>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             C::kSmemBytes);
-        if (e != cudaSuccess)
-            return e;
-        attr_done = true;
-    }
+    static DeviceOnce attrs;
+    const cudaError_t attr_err = attrs.run([] {
+        return cudaFuncSetAttribute(prefill_pair_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    C::kSmemBytes);
+    });
+    if (attr_err != cudaSuccess)
+        return attr_err;
     const long long tiles = ((long long)max_q_len + p.tq - 1) / p.tq;
     const long long pairs = (tiles + 1) / 2;
     const long long rows = (long long)p.B * p.Hkv;

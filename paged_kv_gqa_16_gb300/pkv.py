@@ -38,6 +38,7 @@ EXPORTS = (
     "paged_decode_step", "paged_decode_partials", "decode_combine", "pkv_status_str",
     "pkv_version", "paged_decode_attn_noalloc", "paged_kv_advance", "decode_attn_contig",
     "paged_prefill_attn", "paged_kv_extend", "paged_decode_step_advance",
+    "pkv_testing_set_handoff_wait_ns",
 )
 
 
@@ -95,6 +96,7 @@ def lib():
             "decode_attn_contig": (I, [DP, P, P, P, P, P, P, P, P, I, I, P, Z, P, P]),
             "paged_prefill_attn": (I, [DP, P, P, I, I, P, P, P, P, P, P, P, P]),
             "paged_kv_extend": (I, [DP, P, P, P, P, I, P, P, P, P, P, P, I, I, P, P]),
+            "pkv_testing_set_handoff_wait_ns": (I, [ctypes.c_ulonglong]),
             "pkv_status_str": (ctypes.c_char_p, [I]),
             "pkv_version": (I, []),
         }
@@ -330,3 +332,12 @@ def status_word(workspace) -> int:
     """Read the device status word (synchronises through the copy)."""
     import torch
     return int(workspace[:4].view(torch.int32).item()) & 0xFFFFFFFF
+
+
+DEFAULT_HANDOFF_WAIT_NS = 2_000_000_000
+
+
+def testing_set_handoff_wait_ns(ns: int) -> None:
+    """Test-only: the time limit of the decode kernel's producer/consumer
+    hand-off waits (default DEFAULT_HANDOFF_WAIT_NS)."""
+    _check("pkv_testing_set_handoff_wait_ns", lib().pkv_testing_set_handoff_wait_ns(int(ns)))

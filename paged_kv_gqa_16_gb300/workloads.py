@@ -445,3 +445,25 @@ def prefill(name: str, *, B: int, Hq: int, Hkv: int, D: int, page_size: int, seq
     indptr[1:] = np.cumsum(ql)
     q = _randn_bf16((int(indptr[-1]), Hq, D), gen)
     return PrefillCase(w=w, q=q, qo_indptr=torch.from_numpy(indptr))
+
+
+# Prefill / extend shapes the benchmark times: the pages' 512-token prompts at
+# the 1B-class head shape, a long prefill, and an extend of 256 new tokens on
+# 2,048-token rows.  name -> (label, arguments of prefill()).
+PREFILL_SHAPES = {
+    "prefill_b32_512": ("prefill B=32 x 512 (Hq 32, Hkv 8, D 64)",
+                        dict(B=32, Hq=32, Hkv=8, D=64, page_size=16, seq_lens=[512] * 32,
+                             q_lens=[512] * 32)),
+    "prefill_b4_4096": ("prefill B=4 x 4096 (Hq 32, Hkv 8, D 128)",
+                        dict(B=4, Hq=32, Hkv=8, D=128, page_size=16, seq_lens=[4096] * 4,
+                             q_lens=[4096] * 4)),
+    "extend_b16": ("extend B=16, 256 new of 2048 (Hq 32, Hkv 8, D 128)",
+                   dict(B=16, Hq=32, Hkv=8, D=128, page_size=16, seq_lens=[2048] * 16,
+                        q_lens=[256] * 16)),
+}
+
+
+def prefill_shape(name: str, seed: int = 0) -> PrefillCase:
+    """The named benchmark prefill shape, seeded."""
+    return prefill(name, seed=seed, **PREFILL_SHAPES[name][1])
+

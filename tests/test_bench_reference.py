@@ -31,7 +31,12 @@ def test_reference_arm_json_line():
     assert j["value"] > 0 and j["ms_per_step"] > 0
     assert j["steps"] == 1 and j["warmup"] == 3 and j["n_gpus"] == 1
     assert j["vs_baseline"] is None
-    assert j["config"]["workload"] == "ragged_b32"
+    assert j["config"]["workload"] == "serving_b128"
+    # the same config object as the GPU arm's line (bench.config_of)
+    sys.path.insert(0, ROOT)
+    import bench
+    from paged_kv_gqa_16_gb300 import workloads as wl
+    assert j["config"] == bench.config_of(wl.make("serving_b128"), 1)
     cb = j["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["sample"]
     assert cb["value"] == j["value"] and cb["unit"] == j["unit"]

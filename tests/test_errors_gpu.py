@@ -62,3 +62,30 @@ def test_context_usable_after_flags():
     c2.append()
     compare_out(c2.decode(), oracle_step(w2)["out"])
     assert c2.status() == 0
+
+
+def test_handoff_timeout_sets_flag_and_context_survives():
+    """The bounded waits' own path: with the hand-off limit at zero, the
+    decode kernel's producer and consumer warps give up waiting on each other
+    while copies are in flight.  The call still returns, the status word
+    carries PKV_FLAG_TIMEOUT, and once the limit is back a normal call on the
+    same context matches the oracle."""
+    w = wl.make("gqa_1b")
+    c = GpuCase(w)
+    c.append()
+    try:
+        pkv.testing_set_handoff_wait_ns(0)
+        for _ in range(3):
+            pkv.workspace_init(c.ws)
+            c.decode()
+            assert c.status() & pkv.FLAG_TIMEOUT
+    finally:
+        pkv.testing_set_handoff_wait_ns(pkv.DEFAULT_HANDOFF_WAIT_NS)
+    pkv.workspace_init(c.ws)
+    compare_out(c.decode(), oracle_step(w)["out"])
+    assert c.status() == 0
+
+
+def test_handoff_limit_above_default_refused():
+    with pytest.raises(pkv.PkvError):
+        pkv.testing_set_handoff_wait_ns(pkv.DEFAULT_HANDOFF_WAIT_NS + 1)

@@ -130,3 +130,87 @@ def test_prefill_max_q_len():
                            t["seq_lens"], out, status=st2, max_q_len=64)
     torch.cuda.synchronize()
     assert int(st2.item()) & pkv.FLAG_BAD_LEN
+
+
+# ---- the shapes the benchmark times, in its launch configuration ----------
+def _sampled_want(c, picks):
+    """The oracle's output for the picked queries only.  Query j of row b's
+    chunk sits at position p = seq_len - q_len + j and attends to keys 0..p:
+    that is the prefill of a row of p + 1 tokens (the same pages) whose chunk
+    is its last token, so each pick becomes a one-query row of its own."""
+    w = c.w
+    kp, vp, idx = w.compact_host()
+    ptr = w.kv_indptr.numpy()
+    lens = w.seq_lens.numpy()
+    qo = c.qo_indptr.numpy()
+    sub_idx, sub_ptr, sub_len, rows = [], [0], [], []
+    for b, j in picks:
+        p = int(lens[b]) - int(qo[b + 1] - qo[b]) + j
+        need = -(-(p + 1) // w.page_size)
+        sub_idx.extend(idx[ptr[b]:ptr[b] + need].tolist())
+        sub_ptr.append(len(sub_idx))
+        sub_len.append(p + 1)
+        rows.append(int(qo[b]) + j)
+    want = oracle.prefill(_bits(c.q)[rows], np.arange(len(picks) + 1, dtype=np.int32), kp, vp,
+                          np.array(sub_idx, dtype=np.int32), np.array(sub_ptr, dtype=np.int32),
+                          np.array(sub_len, dtype=np.int32), w.scale)
+    return rows, want
+
+
+def _picks(c, runs, n_random, seed):
+    """Per row: the query runs given (first and last queries, runs across
+    tile and tile-pair boundaries) plus n_random random queries."""
+    g = np.random.default_rng(seed)
+    qo = c.qo_indptr.numpy()
+    out = []
+    for b in range(c.w.B):
+        n = int(qo[b + 1] - qo[b])
+        js = set()
+        for a, e in runs:
+            js.update(j for j in range(a if a >= 0 else n + a, e if e > 0 else n + e)
+                      if 0 <= j < n)
+        js.update(g.integers(0, n, n_random).tolist())
+        out += [(b, j) for j in sorted(js)]
+    return out
+
+
+def test_prefill_bench_shape_b32_512_full():
+    """32 prompts of 512 at D = 64, every query against the oracle."""
+    c = wl.prefill_shape("prefill_b32_512")
+    out, st, _ = _run_bench_config(c)
+    assert st == 0
+    compare_out(out, _want(c))
+
+
+@pytest.mark.parametrize("name,runs,n_random", [
+    # 4 rows of 4096: tiles of 32 tokens (n_rep 4), pairs of 64
+    ("prefill_b4_4096", [(0, 8), (28, 37), (60, 69), (2040, 2057), (-8, 0)], 24),
+    # 16 extends of 256 new tokens on rows of 2048
+    ("extend_b16", [(0, 4), (30, 34), (62, 66), (126, 130), (-4, 0)], 4),
+])
+def test_prefill_bench_shape_sampled(name, runs, n_random):
+    """The large bench shapes: the GPU computes every query; the oracle
+    checks a sample of them, each as a one-query row of its own."""
+    c = wl.prefill_shape(name)
+    out, st, _ = _run_bench_config(c)
+    assert st == 0
+    assert torch.isfinite(out.float()).all()
+    rows, want = _sampled_want(c, _picks(c, runs, n_random, seed=len(name)))
+    compare_out(out[rows], want)
+
+
+def _run_bench_config(c):
+    """One call as the benchmark makes it: max_q_len is the longest chunk."""
+    w = c.w
+    t = w.to_device("cuda")
+    P = t["k_pool"].shape[0]
+    d = pkv.dims(w.B, w.Hq, w.Hkv, w.D, w.page_size, P, int(w.kv_indices.numel()),
+                 w.max_seq_len, w.scale)
+    out = torch.full((c.total_q, w.Hq, w.D), float("nan"), dtype=torch.bfloat16, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ql = (c.qo_indptr[1:] - c.qo_indptr[:-1]).tolist()
+    pkv.paged_prefill_attn(d, c.q.cuda(), c.qo_indptr.cuda(), t["k_pool"], t["v_pool"],
+                           t["kv_indices"], t["kv_indptr"], t["seq_lens"], out, status=st,
+                           max_q_len=max(ql))
+    torch.cuda.synchronize()
+    return out.cpu(), int(st.item()) & 0xFFFFFFFF, (d, t)

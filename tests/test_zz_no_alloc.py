@@ -57,3 +57,43 @@ def test_noalloc_rejects_oversized_shape():
     code = pkv.lib().paged_decode_attn_noalloc(ctypes.byref(d), fake, fake, fake, fake, fake,
                                                fake, 152, fake, None, None)
     assert code == pkv.PKV_ERR_WORKSPACE_TOO_SMALL
+
+
+def test_noalloc_empty_batch_clears_status():
+    # B = 0 computes nothing, but the caller's status word still starts the
+    # call at zero, as every other call leaves it
+    status = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    d = pkv.dims(0, 32, 8, 128, 16, 64, 0, 1024)
+    code = pkv.lib().paged_decode_attn_noalloc(ctypes.byref(d), None, None, None, None, None,
+                                               None, 4, None, status.data_ptr(),
+                                               torch.cuda.current_stream().cuda_stream)
+    assert code == pkv.PKV_OK
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+
+
+@pytest.mark.parametrize("case,want", [
+    ("splits_zero", pkv.PKV_ERR_INVALID_ARG),
+    ("splits_above_max", pkv.PKV_ERR_INVALID_ARG),
+    ("hq_not_multiple", pkv.PKV_ERR_INVALID_ARG),
+    ("bad_head_dim", pkv.PKV_ERR_UNSUPPORTED),
+])
+def test_noalloc_rejects_like_workspace_call(case, want):
+    # bad arguments get the codes paged_decode_attn gives them
+    d = pkv.dims(4, 32, 8, 128, 16, 64, 64, 1024)
+    S = 4
+    if case == "splits_zero":
+        S = 0
+    elif case == "splits_above_max":
+        S = 65537
+    elif case == "hq_not_multiple":
+        d.Hq = 30
+    elif case == "bad_head_dim":
+        d.D = 96
+    fake = 1 << 32
+    ref = pkv.lib().paged_decode_attn(ctypes.byref(d), fake, fake, fake, fake, fake, fake, S,
+                                      fake, 1 << 30, fake, None)
+    code = pkv.lib().paged_decode_attn_noalloc(ctypes.byref(d), fake, fake, fake, fake, fake,
+                                               fake, S, fake, None, None)
+    assert code == ref == want
+
