@@ -88,6 +88,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-loop", action="store_true",
                     help="skip the decode-loop leg (paged_kv_advance + step per graph)")
     ap.add_argument("--no-flush", action="store_true", help="skip the L2 flush (not for reporting)")
+    ap.add_argument("--no-plan", action="store_true",
+                    help="the unplanned calls (each computes the partition itself)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target CPU time of the all-core oracle baseline sample")
     ap.add_argument("--cpu-seconds-1t", type=float, default=6.0,
@@ -454,34 +456,42 @@ def run_prefill_only(args):
 
 # --------------------------------------------------------------------------
 class StepState:
-    """Device state of one workload for timing paged_decode_step: the pools
-    (``copies`` copies of every referenced page, copy i at page ids
-    i * P + id), one page table per copy, the shared q / new K/V / lengths,
-    the workspace, the RoPE table and the output."""
+    """Device state of one workload for timing paged_decode_step: ``copies``
+    pairs of K/V pools (the layers of one decode step: each its own pools,
+    all named by one page table), the shared q / new K/V / lengths / table,
+    the workspace (which holds the step's plan), the RoPE table and the
+    output.  A decode step's first call computes the block partition and
+    leaves it in the workspace as the plan; with ``planned`` the step's later
+    calls (its other layers) run on that plan."""
 
-    def __init__(self, pkv, w, dev, copies: int = 1, pool_pages: int = 0, splits: int = 0):
+    def __init__(self, pkv, w, dev, copies: int = 1, pool_pages: int = 0, splits: int = 0,
+                 planned: bool = True):
         import torch
         P = pool_pages or w.num_pages
-        self.w, self.dev, self.copies, self.P = w, dev, copies, P
-        shape = (copies * P, w.page_size, w.Hkv, w.D)
-        self.k_pool = torch.full(shape, float("nan"), dtype=torch.bfloat16, device=dev)
-        self.v_pool = torch.full(shape, float("nan"), dtype=torch.bfloat16, device=dev)
+        self.w, self.dev, self.copies, self.P, self.planned = w, dev, copies, P, planned
+        shape = (P, w.page_size, w.Hkv, w.D)
         idx = w.kv_indices.to(device=dev, dtype=torch.long)
-        if idx.numel():
-            kpg, vpg = w.k_pages.to(dev), w.v_pages.to(dev)
-            for i in range(copies):
-                self.k_pool[i * P + idx] = kpg
-                self.v_pool[i * P + idx] = vpg
-            del kpg, vpg
-        base = w.kv_indices.to(dev)
-        self.tables = [(base + i * P).contiguous() for i in range(copies)]
+        self.k_pools, self.v_pools = [], []
+        kpg = w.k_pages.to(dev) if idx.numel() else None
+        vpg = w.v_pages.to(dev) if idx.numel() else None
+        for _ in range(copies):
+            kp = torch.full(shape, float("nan"), dtype=torch.bfloat16, device=dev)
+            vp = torch.full(shape, float("nan"), dtype=torch.bfloat16, device=dev)
+            if idx.numel():
+                kp[idx] = kpg
+                vp[idx] = vpg
+            self.k_pools.append(kp)
+            self.v_pools.append(vp)
+        del kpg, vpg
+        self.k_pool, self.v_pool = self.k_pools[0], self.v_pools[0]
+        self.kv_indices = w.kv_indices.to(dev)
         self.q = w.q.to(dev).contiguous()
         self.k_new = w.k_new.to(dev).contiguous()
         self.v_new = w.v_new.to(dev).contiguous()
         self.kv_indptr = w.kv_indptr.to(dev)
         self.seq_lens = w.seq_lens.to(dev)
-        self.d = pkv.dims(w.B, w.Hq, w.Hkv, w.D, w.page_size, copies * P,
-                          int(w.kv_indices.numel()), w.max_seq_len, w.scale)
+        self.d = pkv.dims(w.B, w.Hq, w.Hkv, w.D, w.page_size, P, int(w.kv_indices.numel()),
+                          w.max_seq_len, w.scale)
         self.S = splits or pkv.plan(self.d)[0]
         self.ws = pkv.alloc_workspace(self.d, self.S, dev)
         self.rope_rows = max(w.max_seq_len, 1)
@@ -490,17 +500,29 @@ class StepState:
         self.out = torch.empty(w.B, w.Hq, w.D, dtype=torch.bfloat16, device=dev)
         self.pkv = pkv
 
-    def step(self, i: int = 0, args=None):
-        """paged_decode_step on copy i (or on the given device inputs)."""
-        q, k_new, v_new, kv_indices, kv_indptr, seq_lens = args or (
-            self.q, self.k_new, self.v_new, self.tables[i], self.kv_indptr, self.seq_lens)
-        self.pkv.paged_decode_step(self.d, q, k_new, v_new, self.k_pool, self.v_pool,
-                                   kv_indices, kv_indptr, seq_lens, self.rope, self.rope_rows,
-                                   self.S, self.ws, self.out)
+    def plan(self, args=None):
+        """The step's plan (once per decode step, for every layer's call)."""
+        if not self.planned:
+            return
+        kv_indices, kv_indptr, seq_lens = args or (self.kv_indices, self.kv_indptr,
+                                                   self.seq_lens)
+        self.pkv.paged_decode_plan(self.d, kv_indices, kv_indptr, seq_lens, self.S, self.ws)
 
-    def decode(self, i: int = 0):
-        self.pkv.paged_decode_attn(self.d, self.q, self.k_pool, self.v_pool, self.tables[i],
-                                   self.kv_indptr, self.seq_lens, self.S, self.ws, self.out)
+    def step(self, i: int = 0, args=None, planned: bool = False):
+        """paged_decode_step on layer i's pools (or on the given device
+        inputs); planned: on the plan the step's first call left behind."""
+        q, k_new, v_new, kv_indices, kv_indptr, seq_lens = args or (
+            self.q, self.k_new, self.v_new, self.kv_indices, self.kv_indptr, self.seq_lens)
+        fn = (self.pkv.paged_decode_step_planned if planned and self.planned
+              else self.pkv.paged_decode_step)
+        fn(self.d, q, k_new, v_new, self.k_pools[i], self.v_pools[i], kv_indices, kv_indptr,
+           seq_lens, self.rope, self.rope_rows, self.S, self.ws, self.out)
+
+    def decode(self, i: int = 0, planned: bool = False):
+        fn = (self.pkv.paged_decode_attn_planned if planned and self.planned
+              else self.pkv.paged_decode_attn)
+        fn(self.d, self.q, self.k_pools[i], self.v_pools[i], self.kv_indices, self.kv_indptr,
+           self.seq_lens, self.S, self.ws, self.out)
 
     def check_status(self, what: str):
         s = self.pkv.status_word(self.ws)
@@ -508,11 +530,14 @@ class StepState:
             raise SystemExit(f"device status {s:#x} {what}")
 
 
-def capture(fn, n: int):
-    """One CUDA graph holding n calls of fn(k), k = 0..n-1."""
+def capture(fn, n: int, first=None):
+    """One CUDA graph holding first() (if given) and then n calls of fn(k),
+    k = 0..n-1."""
     import torch
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g):
+        if first is not None:
+            first()
         for k in range(n):
             fn(k)
     return g
@@ -541,13 +566,17 @@ def rotation_copies(kv_bytes: int, l2: int) -> int:
 
 def measure_config(pkv, w, dev, stream, l2, flush_l2, peak, splits=0):
     """µs per paged_decode_step of one workload, with KV GB/s and the
-    fraction of the HBM peak, timed as the module docstring describes."""
+    fraction of the HBM peak, timed as the module docstring describes: in
+    each replay the first call computes the partition and leaves it as the
+    plan, the later calls (the step's other layers) run on it; every call
+    unplanned is timed the same way for reference."""
     import torch
     kv = w.kv_bytes()
     alg = alg_bytes_of(w)
     b2b = kv >= 2 * l2
     copies = 1 if b2b else rotation_copies(kv, l2)
     st = StepState(pkv, w, dev, copies=copies, splits=splits)
+    st.plan()
     for i in range(copies):
         st.step(i)
     torch.cuda.synchronize(dev)
@@ -562,34 +591,38 @@ def measure_config(pkv, w, dev, stream, l2, flush_l2, peak, splits=0):
         r.update(extra or {})
         return r
 
+    def per_step(n, planned, flush=None, reps=15):
+        # the step's first call writes the plan, its later calls run on it
+        st.planned = planned
+        g = capture(lambda k: st.step(k % copies, planned=k > 0), n)
+        replay_times(g, 3, stream, dev, flush)
+        ms = [t / n for t in replay_times(g, reps, stream, dev, flush)]
+        del g
+        return statistics.median(ms)
+
     out = {"splits": st.S, "kv_bytes": kv, "alg_bytes": alg, "tokens": w.total_tokens}
     if b2b:
-        inner = 20
-        g = capture(lambda k: st.step(0), inner)
-        replay_times(g, 3, stream, dev)
-        ms = [t / inner for t in replay_times(g, 15, stream, dev)]
-        out.update(line(statistics.median(ms), f"back to back, {inner} steps per replay, "
-                                               f"K+V = {kv / l2:.1f} x L2, no flush",
-                        {"replays": 15}))
+        n = 20
+        mode = (f"back to back, {n} steps per replay (the first leaves the plan), "
+                f"K+V = {kv / l2:.1f} x L2, no flush")
     else:
         n = max(copies, 20 // copies * copies)
-        g = capture(lambda k: st.step(k % copies), n)
-        replay_times(g, 3, stream, dev)
-        ms = [t / n for t in replay_times(g, 15, stream, dev)]
-        out.update(line(statistics.median(ms),
-                        f"rotation over {copies} copies of the pools "
-                        f"({copies * kv / l2:.1f} x L2 of K+V), {n} steps per replay",
-                        {"replays": 15}))
-        g1 = capture(lambda k: st.step(0), 1)
-        replay_times(g1, 3, stream, dev, flush_l2)
-        ms1 = replay_times(g1, 30, stream, dev, flush_l2)
-        out["flushed"] = line(statistics.median(ms1),
-                              "one step per replay, L2 flushed before it (outside the events)",
-                              {"replays": 30})
-        del g1
+        mode = (f"rotation over {copies} layers' pools ({copies * kv / l2:.1f} x L2 of K+V), "
+                f"{n} steps per replay (the first leaves the plan)")
+    out.update(line(per_step(n, True), mode, {"replays": 15}))
+    out["unplanned_us"] = round(1e3 * per_step(n, False), 2)
+    if not b2b:
+        out["flushed"] = line(per_step(1, True, flush_l2, 30),
+                              "one (unplanned) step per replay, L2 flushed before it "
+                              "(outside the events)", {"replays": 30})
+    # paged_decode_plan alone (for callers that plan ahead of a step)
+    st.planned = True
+    gp = capture(lambda k: st.plan(), 1)
+    replay_times(gp, 3, stream, dev)
+    out["plan_us"] = round(1e3 * statistics.median(replay_times(gp, 20, stream, dev)), 2)
     torch.cuda.synchronize(dev)
     st.check_status(f"after timing {w.name}")
-    del g, st
+    del gp, st
     torch.cuda.empty_cache()
     return out
 
@@ -639,10 +672,11 @@ def run_pkv(args):
     # ---- the headline workload: each rank an independent replica (own seed)
     kw = {"num_pages": args.pool_pages} if args.pool_pages else {}
     w = wl.make(args.workload, seed=rank, **kw)
-    st = StepState(pkv, w, dev, copies=1, splits=args.splits)
+    st = StepState(pkv, w, dev, copies=1, splits=args.splits, planned=not args.no_plan)
     d, S = st.d, st.S
     step = st.step
     decode = st.decode
+    plan = st.plan
     if args.layout == "contig":
         # the same rows in a contiguous cache: slot b holds row b's tokens in
         # order (gathered from its pages), NaN past them
@@ -655,21 +689,22 @@ def run_pkv(args):
             L = int(w.seq_lens[b])
             if L == 0:
                 continue
-            pages = st.tables[0][ptr_h[b]:ptr_h[b + 1]].long()
+            pages = st.kv_indices[ptr_h[b]:ptr_h[b + 1]].long()
             ck[b, :L] = st.k_pool[pages].reshape(-1, w.Hkv, w.D)[:L]
             cv[b, :L] = st.v_pool[pages].reshape(-1, w.Hkv, w.D)[:L]
-        del st.k_pool, st.v_pool
+        del st.k_pool, st.v_pool, st.k_pools, st.v_pools
+        st.planned = False
         torch.cuda.empty_cache()
         cd = pkv.dims(w.B, w.Hq, w.Hkv, w.D, cache_len, w.B, w.B, cache_len, w.scale)
         cws = pkv.alloc_workspace(cd, S, dev)
         st.ws = cws
 
-        def step(i=0, a=None):
+        def step(i=0, a=None, planned=False):
             pkv.decode_attn_contig(cd, st.q, ck, cv, st.seq_lens, S, cws, st.out,
                                    k_new=st.k_new, v_new=st.v_new, rope_cos_sin=st.rope,
                                    rope_max_pos=st.rope_rows)
 
-        def decode(i=0):
+        def decode(i=0, planned=False):
             pkv.decode_attn_contig(cd, st.q, ck, cv, st.seq_lens, S, cws, st.out)
 
         args.no_e2e = True
@@ -688,7 +723,9 @@ def run_pkv(args):
     K = max(1, args.steps)
     inner = pick_inner(K)
     reps = K // inner
-    g_step = capture(lambda k: step(), inner)
+    # each replay: `inner` steps of one decode step's metadata; the first
+    # leaves the plan, the others run on it (unless --no-plan)
+    g_step = capture(lambda k: step(0, None, k > 0), inner)
     replay_times(g_step, 3, stream, dev)
     est_ms = statistics.median(replay_times(g_step, 3, stream, dev))
     flush = None if (back_to_back or args.no_flush) else flush_l2
@@ -738,7 +775,7 @@ def run_pkv(args):
     value = total_bytes / (ms_step_max * 1e-3) / 1e9
 
     # decode-only and a cold single step (L2 flushed before it) on the same rows
-    g_dec = capture(lambda k: decode(), inner)
+    g_dec = capture(lambda k: decode(0, k > 0), inner)
     replay_times(g_dec, 3, stream, dev)
     ms_dec = statistics.median(t / inner for t in replay_times(g_dec, max(10, reps), stream,
                                                               dev, flush))
@@ -792,10 +829,17 @@ def run_pkv(args):
         del g_e2e, dev_blk
         st.check_status("after the e2e leg")
 
+    plan_us = None
+    if st.planned:
+        gp = capture(lambda k: plan(), 1)
+        replay_times(gp, 3, stream, dev)
+        plan_us = round(1e3 * statistics.median(replay_times(gp, 20, stream, dev)), 2)
+        del gp
     achieved = alg_bytes / (ms_region * 1e-3) / 1e9
     read_peak = measure_read_peak(dev, stream)
     traffic = cached_traffic(w.name, S) if args.layout == "paged" else None
     del g_step
+    planned = st.planned
     st_config = config_of(w, world, args.layout)
     headline_entry = {"splits": S, "kv_bytes": kv_bytes, "alg_bytes": alg_bytes,
                       "tokens": w.total_tokens, "us_per_call": round(1e3 * ms_region, 2),
@@ -949,7 +993,12 @@ def run_pkv(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
         "config": st_config,
-        "plan": {"num_splits": S, "chunk": pkv.split_chunk(d, S)},
+        "plan": {"num_splits": S, "chunk": pkv.split_chunk(d, S), "planned": planned,
+                 "plan_us": plan_us,
+                 "note": "in each replay the first step (paged_decode_step) leaves its "
+                         "partition as the plan; the replay's other steps "
+                         "(paged_decode_step_planned) run on it, as a decode step's later "
+                         "layers would; plan_us: paged_decode_plan alone, for reference"},
         "l2": (f"inputs larger than L2 (K+V = {kv_bytes / l2:.1f} x L2): steps back to back "
                "inside each replay, no flush" if back_to_back else
                "flushed before every replay (2x L2 written, then 2x L2 read), outside the "

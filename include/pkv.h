@@ -106,7 +106,8 @@ typedef struct {
 int pkv_split_chunk(const pkv_dims *dims, int num_splits);
 
 /* Workspace bytes for num_splits: a 256-byte header (status word first),
- * per-row bookkeeping, a [B, Hq, D] bf16 scratch, and room for either
+ * per-row bookkeeping, the per-step plan (paged_decode_plan), a [B, Hq, D]
+ * bf16 scratch, and room for either
  * partial layout (the per-row one [B, Hq, S, 2] + [B, Hq, S, D] fp32, or the
  * persistent path's pieces), each region 256-byte aligned.  Returns 0 for
  * invalid arguments. */
@@ -190,6 +191,56 @@ pkv_status paged_decode_step(const pkv_dims *dims, const void *q, const void *k_
                              const int32_t *seq_lens, const float *rope_cos_sin,
                              int rope_max_pos, int num_splits, void *workspace,
                              size_t ws_bytes, void *out, pkv_stream_t stream);
+
+/* ---- the per-step plan --------------------------------------------------- */
+
+/* The decode metadata built once per step and reused by every layer's call
+ * of that step (commits by author: kv_indptr built once per step instead of
+ * per layer; the per-step metadata precompute of the decode path).  Writes
+ * into the workspace the partition that paged_decode_attn and
+ * paged_decode_step compute at the start of each call on the persistent
+ * path: the rows' prefix sums, each row's first block and piece count, and
+ * for each of the num_splits blocks its first row and that row's 64-entry
+ * page-table window.  A call of paged_decode_attn_planned or
+ * paged_decode_step_planned with the same dims and num_splits on this
+ * workspace then starts streaming after one round trip to memory instead of
+ * three, and its piece combine reads the row ranges while the decode grid
+ * finishes.  One launch of num_splits blocks; graph-capturable; allocates
+ * nothing.  The plan stays valid until seq_lens, kv_indptr, kv_indices, dims
+ * or num_splits change: the caller plans again after any of them changes
+ * (once per decode step).  paged_decode_attn and paged_decode_step on the
+ * persistent path leave the partition they compute in the workspace as the
+ * same plan, so a step whose first layer calls them needs no separate
+ * paged_decode_plan before its later layers' planned calls.  A planned call on a plan made for another grid or
+ * shape falls back to computing the partition itself; on a plan made for
+ * other lengths or tables it reads no memory out of bounds but its output is
+ * undefined.  Length and table checks run in the plan and set PKV_FLAG_*
+ * bits of the workspace status word.  Shapes off the persistent path need
+ * no plan: the call returns PKV_OK and writes nothing.  Arguments as in
+ * paged_decode_attn. */
+pkv_status paged_decode_plan(const pkv_dims *dims, const int32_t *kv_indices,
+                             const int32_t *kv_indptr, const int32_t *seq_lens,
+                             int num_splits, void *workspace, size_t ws_bytes,
+                             pkv_stream_t stream);
+
+/* paged_decode_attn on the workspace's plan (paged_decode_plan).  Arguments
+ * and results are those of paged_decode_attn, bit for bit. */
+pkv_status paged_decode_attn_planned(const pkv_dims *dims, const void *q,
+                                     const void *k_pool, const void *v_pool,
+                                     const int32_t *kv_indices, const int32_t *kv_indptr,
+                                     const int32_t *seq_lens, int num_splits,
+                                     void *workspace, size_t ws_bytes, void *out,
+                                     pkv_stream_t stream);
+
+/* paged_decode_step on the workspace's plan (paged_decode_plan).  Arguments
+ * and results are those of paged_decode_step, bit for bit; the step's new
+ * token does not change the plan (its length is already counted). */
+pkv_status paged_decode_step_planned(const pkv_dims *dims, const void *q, const void *k_new,
+                                     const void *v_new, void *k_pool, void *v_pool,
+                                     const int32_t *kv_indices, const int32_t *kv_indptr,
+                                     const int32_t *seq_lens, const float *rope_cos_sin,
+                                     int rope_max_pos, int num_splits, void *workspace,
+                                     size_t ws_bytes, void *out, pkv_stream_t stream);
 
 /* The split kernel alone: always writes the partials (never out), for any
  * num_splits >= 1.  Partial (b, h, s): o_part = the split's softmax-weighted

@@ -74,15 +74,16 @@ int log2_exact(int x)
 }
 
 // Workspace: [header 256 B | row info, persistent path: Bv x 2 int32 |
-//             rotated-q scratch [B, Hq, D] bf16 | one-page-per-row table of
+//             the per-step plan, persistent path | rotated-q scratch
+//             [B, Hq, D] bf16 | one-page-per-row table of
 //             the contiguous-cache call, (2B + 1) int32 | partials].
 // The partial region holds either layout: the per-split one [B,Hq,S,(2|D)]
 // of paged_decode_partials, or the piece one [(S+Bv)*HQV, (2|D)] of the
 // persistent path.  Every region starts on a 256-byte boundary.
 struct Layout {
     int hpc, Bv, HQV;
-    size_t rowinfo_off, qscratch_off, table_off, split_ml_off, split_o_off, piece_ml_off,
-        piece_o_off, total;
+    size_t rowinfo_off, plan_off, qscratch_off, table_off, split_ml_off, split_o_off,
+        piece_ml_off, piece_o_off, total;
 };
 
 Layout layout_for(const pkv_dims *d, int num_splits)
@@ -92,7 +93,11 @@ Layout layout_for(const pkv_dims *d, int num_splits)
     L.Bv = d->B * (d->Hkv / L.hpc);
     L.HQV = L.hpc * (d->Hq / d->Hkv);
     L.rowinfo_off = kHeaderBytes;
-    L.qscratch_off = L.rowinfo_off + round_up((size_t)L.Bv * 2 * sizeof(int32_t), 256);
+    L.plan_off = L.rowinfo_off + round_up((size_t)L.Bv * 2 * sizeof(int32_t), 256);
+    // the per-step plan, for shapes the persistent path serves
+    const size_t plan = L.Bv <= pkv::kFusedMaxRows
+                            ? pkv::plan_words(L.Bv, num_splits) * sizeof(int32_t) : 0;
+    L.qscratch_off = L.plan_off + round_up(plan, 256);
     L.table_off = L.qscratch_off + round_up((size_t)d->B * d->Hq * d->D * 2, 256);
     const size_t part = L.table_off + round_up(((size_t)2 * d->B + 1) * sizeof(int32_t), 256);
     const size_t rows = (size_t)d->B * d->Hq * num_splits;
@@ -199,25 +204,15 @@ pkv_status launch_combine_split(const pkv_dims *dims, int num_splits, void *work
 
 // Persistent path: the token-balanced kernel, then the piece combine.  With
 // k_new != nullptr the kernel also appends the step's new token (fused step).
-pkv_status launch_persistent(const pkv_dims *dims, const void *q, const void *k_pool,
-                             const void *v_pool, const int32_t *kv_indices,
-                             const int32_t *kv_indptr, const int32_t *seq_lens,
-                             int num_splits, void *workspace, void *out, const void *k_new,
-                             const void *v_new, const float *rope, int rope_max_pos,
-                             pkv_stream_t stream, const pkv::AdvanceParams *adv = nullptr)
+// The persistent path's parameters (shape, tables, workspace regions).
+pkv::FusedParams persistent_params(const pkv_dims *dims, const Layout &L, char *ws,
+                                   const int32_t *kv_indices, const int32_t *kv_indptr,
+                                   const int32_t *seq_lens)
 {
-    const Layout L = layout_for(dims, num_splits);
-    char *ws = static_cast<char *>(workspace);
     pkv::FusedParams p{};
-    p.q = static_cast<const __nv_bfloat16 *>(q);
-    p.k_pool = static_cast<const __nv_bfloat16 *>(k_pool);
-    p.v_pool = static_cast<const __nv_bfloat16 *>(v_pool);
     p.kv_indices = kv_indices;
     p.kv_indptr = kv_indptr;
     p.seq_lens = seq_lens;
-    p.out = static_cast<__nv_bfloat16 *>(out);
-    p.o_part = reinterpret_cast<float *>(ws + L.piece_o_off);
-    p.ml_part = reinterpret_cast<float *>(ws + L.piece_ml_off);
     p.row_info = reinterpret_cast<int32_t *>(ws + L.rowinfo_off);
     p.status = reinterpret_cast<uint32_t *>(ws);
     p.B = dims->B;
@@ -232,6 +227,29 @@ pkv_status launch_persistent(const pkv_dims *dims, const void *q, const void *k_
     p.Bv = L.Bv;
     p.row_cost = pkv::kFusedRowCost;
     p.hpc = L.hpc;
+    return p;
+}
+
+pkv_status launch_persistent(const pkv_dims *dims, const void *q, const void *k_pool,
+                             const void *v_pool, const int32_t *kv_indices,
+                             const int32_t *kv_indptr, const int32_t *seq_lens,
+                             int num_splits, void *workspace, void *out, const void *k_new,
+                             const void *v_new, const float *rope, int rope_max_pos,
+                             pkv_stream_t stream, const pkv::AdvanceParams *adv = nullptr,
+                             bool planned = false)
+{
+    const Layout L = layout_for(dims, num_splits);
+    char *ws = static_cast<char *>(workspace);
+    pkv::FusedParams p = persistent_params(dims, L, ws, kv_indices, kv_indptr, seq_lens);
+    p.q = static_cast<const __nv_bfloat16 *>(q);
+    p.k_pool = static_cast<const __nv_bfloat16 *>(k_pool);
+    p.v_pool = static_cast<const __nv_bfloat16 *>(v_pool);
+    p.out = static_cast<__nv_bfloat16 *>(out);
+    p.o_part = reinterpret_cast<float *>(ws + L.piece_o_off);
+    p.ml_part = reinterpret_cast<float *>(ws + L.piece_ml_off);
+    int32_t *plan_region = reinterpret_cast<int32_t *>(ws + L.plan_off);
+    p.plan = planned ? plan_region : nullptr;
+    p.plan_out = planned ? nullptr : plan_region;
     p.scale_log2 = (float)((double)dims->scale * 1.4426950408889634);
     p.step = k_new != nullptr ? 1 : 0;
     p.k_pool_w = const_cast<__nv_bfloat16 *>(p.k_pool);
@@ -253,6 +271,7 @@ pkv_status launch_persistent(const pkv_dims *dims, const void *q, const void *k_
     c.Bv = L.Bv;
     c.Hq = dims->Hq;
     c.HQV = L.HQV;
+    c.planned = planned ? 1 : 0;
     if (adv != nullptr)
         c.adv = *adv;
     return launch_status(
@@ -535,10 +554,11 @@ pkv_status paged_kv_advance(const pkv_dims *dims, int32_t *seq_lens, const int32
     return launch_status(pkv::launch_advance(p, (cudaStream_t)stream));
 }
 
-pkv_status paged_decode_attn(const pkv_dims *dims, const void *q, const void *k_pool,
-                             const void *v_pool, const int32_t *kv_indices,
-                             const int32_t *kv_indptr, const int32_t *seq_lens, int num_splits,
-                             void *workspace, size_t ws_bytes, void *out, pkv_stream_t stream)
+static pkv_status decode_attn_impl(const pkv_dims *dims, const void *q, const void *k_pool,
+                                   const void *v_pool, const int32_t *kv_indices,
+                                   const int32_t *kv_indptr, const int32_t *seq_lens,
+                                   int num_splits, void *workspace, size_t ws_bytes, void *out,
+                                   pkv_stream_t stream, bool planned)
 {
     pkv_status st = check_decode_args(dims, q, k_pool, v_pool, kv_indices, kv_indptr,
                                       seq_lens, num_splits, workspace, ws_bytes, out, true);
@@ -547,7 +567,7 @@ pkv_status paged_decode_attn(const pkv_dims *dims, const void *q, const void *k_
     if (fused_path_ok(dims))
         return launch_persistent(dims, q, k_pool, v_pool, kv_indices, kv_indptr, seq_lens,
                                  num_splits, workspace, out, nullptr, nullptr, nullptr, 0,
-                                 stream);
+                                 stream, nullptr, planned);
     const bool direct = num_splits == 1;
     st = launch_split(dims, q, k_pool, v_pool, kv_indices, kv_indptr, seq_lens, num_splits,
                       workspace, out, direct, stream);
@@ -556,12 +576,61 @@ pkv_status paged_decode_attn(const pkv_dims *dims, const void *q, const void *k_
     return launch_combine_split(dims, num_splits, workspace, out, stream);
 }
 
-pkv_status paged_decode_step(const pkv_dims *dims, const void *q, const void *k_new,
-                             const void *v_new, void *k_pool, void *v_pool,
-                             const int32_t *kv_indices, const int32_t *kv_indptr,
-                             const int32_t *seq_lens, const float *rope_cos_sin,
-                             int rope_max_pos, int num_splits, void *workspace,
-                             size_t ws_bytes, void *out, pkv_stream_t stream)
+pkv_status paged_decode_attn(const pkv_dims *dims, const void *q, const void *k_pool,
+                             const void *v_pool, const int32_t *kv_indices,
+                             const int32_t *kv_indptr, const int32_t *seq_lens, int num_splits,
+                             void *workspace, size_t ws_bytes, void *out, pkv_stream_t stream)
+{
+    return decode_attn_impl(dims, q, k_pool, v_pool, kv_indices, kv_indptr, seq_lens,
+                            num_splits, workspace, ws_bytes, out, stream, false);
+}
+
+pkv_status paged_decode_attn_planned(const pkv_dims *dims, const void *q, const void *k_pool,
+                                     const void *v_pool, const int32_t *kv_indices,
+                                     const int32_t *kv_indptr, const int32_t *seq_lens,
+                                     int num_splits, void *workspace, size_t ws_bytes,
+                                     void *out, pkv_stream_t stream)
+{
+    return decode_attn_impl(dims, q, k_pool, v_pool, kv_indices, kv_indptr, seq_lens,
+                            num_splits, workspace, ws_bytes, out, stream, true);
+}
+
+pkv_status paged_decode_plan(const pkv_dims *dims, const int32_t *kv_indices,
+                             const int32_t *kv_indptr, const int32_t *seq_lens, int num_splits,
+                             void *workspace, size_t ws_bytes, pkv_stream_t stream)
+{
+    pkv_status st = check_dims(dims);
+    if (st != PKV_OK)
+        return st;
+    if (num_splits < 1 || num_splits > kMaxSplits)
+        return PKV_ERR_INVALID_ARG;
+    if (dims->B == 0)
+        return PKV_OK;
+    if (kv_indptr == nullptr || seq_lens == nullptr || workspace == nullptr ||
+        (dims->num_indices > 0 && kv_indices == nullptr) || !aligned(workspace, 256) ||
+        !aligned(kv_indptr, 4) || !aligned(seq_lens, 4) ||
+        (kv_indices != nullptr && !aligned(kv_indices, 4)))
+        return PKV_ERR_INVALID_ARG;
+    const size_t need = pkv_workspace_bytes(dims, num_splits);
+    if (need == 0)
+        return PKV_ERR_INVALID_ARG;
+    if (ws_bytes < need)
+        return PKV_ERR_WORKSPACE_TOO_SMALL;
+    if (!fused_path_ok(dims))
+        return PKV_OK;                     // other shapes compute their split per call
+    const Layout L = layout_for(dims, num_splits);
+    char *ws = static_cast<char *>(workspace);
+    const pkv::FusedParams p = persistent_params(dims, L, ws, kv_indices, kv_indptr, seq_lens);
+    return launch_status(pkv::launch_decode_plan(
+        p, num_splits, reinterpret_cast<int32_t *>(ws + L.plan_off), (cudaStream_t)stream));
+}
+
+static pkv_status decode_step_impl(const pkv_dims *dims, const void *q, const void *k_new,
+                                   const void *v_new, void *k_pool, void *v_pool,
+                                   const int32_t *kv_indices, const int32_t *kv_indptr,
+                                   const int32_t *seq_lens, const float *rope_cos_sin,
+                                   int rope_max_pos, int num_splits, void *workspace,
+                                   size_t ws_bytes, void *out, pkv_stream_t stream, bool planned)
 {
     pkv_status st = check_decode_args(dims, q, k_pool, v_pool, kv_indices, kv_indptr,
                                       seq_lens, num_splits, workspace, ws_bytes, out, true);
@@ -575,7 +644,7 @@ pkv_status paged_decode_step(const pkv_dims *dims, const void *q, const void *k_
     if (fused_path_ok(dims))
         return launch_persistent(dims, q, k_pool, v_pool, kv_indices, kv_indptr, seq_lens,
                                  num_splits, workspace, out, k_new, v_new, rope_cos_sin,
-                                 rope_max_pos, stream);
+                                 rope_max_pos, stream, nullptr, planned);
     // other shapes: rotate a copy of q in the workspace, append, then decode
     const Layout L = layout_for(dims, num_splits);
     void *qs = static_cast<char *>(workspace) + L.qscratch_off;
@@ -594,6 +663,30 @@ pkv_status paged_decode_step(const pkv_dims *dims, const void *q, const void *k_
     if (st != PKV_OK || direct)
         return st;
     return launch_combine_split(dims, num_splits, workspace, out, stream);
+}
+
+pkv_status paged_decode_step(const pkv_dims *dims, const void *q, const void *k_new,
+                             const void *v_new, void *k_pool, void *v_pool,
+                             const int32_t *kv_indices, const int32_t *kv_indptr,
+                             const int32_t *seq_lens, const float *rope_cos_sin,
+                             int rope_max_pos, int num_splits, void *workspace,
+                             size_t ws_bytes, void *out, pkv_stream_t stream)
+{
+    return decode_step_impl(dims, q, k_new, v_new, k_pool, v_pool, kv_indices, kv_indptr,
+                            seq_lens, rope_cos_sin, rope_max_pos, num_splits, workspace,
+                            ws_bytes, out, stream, false);
+}
+
+pkv_status paged_decode_step_planned(const pkv_dims *dims, const void *q, const void *k_new,
+                                     const void *v_new, void *k_pool, void *v_pool,
+                                     const int32_t *kv_indices, const int32_t *kv_indptr,
+                                     const int32_t *seq_lens, const float *rope_cos_sin,
+                                     int rope_max_pos, int num_splits, void *workspace,
+                                     size_t ws_bytes, void *out, pkv_stream_t stream)
+{
+    return decode_step_impl(dims, q, k_new, v_new, k_pool, v_pool, kv_indices, kv_indptr,
+                            seq_lens, rope_cos_sin, rope_max_pos, num_splits, workspace,
+                            ws_bytes, out, stream, true);
 }
 
 pkv_status paged_decode_step_advance(const pkv_dims *dims, const void *q, const void *k_new,

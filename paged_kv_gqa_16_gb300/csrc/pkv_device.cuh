@@ -72,10 +72,28 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
     return done != 0;
 }
 
+// Non-blocking probe: has phase `parity` of `bar` completed?
+__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity)
+{
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
 // Wait for phase `parity` of `bar`; false if the time limit ran out first.
+// try_wait may suspend the thread for a while inside one probe, so a limit
+// of zero is one non-blocking probe instead.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity,
                                                   unsigned long long limit_ns = kWaitLimitNs)
 {
+    if (limit_ns == 0)
+        return mbar_test_wait(bar, parity);
     if (mbar_try_wait(bar, parity))
         return true;
     const unsigned long long t0 = global_timer_ns();

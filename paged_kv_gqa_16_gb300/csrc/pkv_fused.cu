@@ -136,6 +136,108 @@ __device__ __forceinline__ int block_of(long long x, long long T, int G)
     return (int)(((x + 1) * G + T - 1) / T) - 1;
 }
 
+// ---- the partition, shared by the decode kernel and the per-step plan -----
+// Token count of virtual row r after the checks: a negative length counts as
+// zero, one above max_seq_len as max_seq_len, and a row whose table is
+// malformed or does not cover its length is cut to what the table covers.
+// The failed checks' flags go to `bad`.
+__device__ __forceinline__ int checked_row_len(const FusedParams &p, int r, unsigned &bad)
+{
+    const int b = r % p.B;
+    int L = p.seq_lens[b];
+    const int pg0 = p.kv_indptr[b];
+    const int pg1 = p.kv_indptr[b + 1];
+    if (L < 0 || L > p.max_seq_len) {
+        bad |= kFlagBadLen;
+        L = L < 0 ? 0 : p.max_seq_len;
+    }
+    if (pg0 < 0 || pg1 < pg0 || pg1 > p.num_indices) {
+        bad |= kFlagBadPage;
+        L = 0;
+    } else if ((long long)(pg1 - pg0) * p.page_size < (long long)L) {
+        bad |= kFlagBadPage;
+        L = (pg1 - pg0) * p.page_size;
+    }
+    return L;
+}
+
+// prefix[0..Bv] of the rows' partition weights (a non-empty row weighs its
+// tokens plus row_cost), computed by every thread of the block; report: OR
+// the flags of the first B rows into the status word.
+__device__ __forceinline__ void row_prefix(const FusedParams &p, int *prefix, bool report)
+{
+    const int Bv = p.Bv, lane = threadIdx.x & 31;
+    for (int r = threadIdx.x; r < Bv; r += blockDim.x) {
+        unsigned bad = 0;
+        const int L = checked_row_len(p, r, bad);
+        if (bad && report && r < p.B)
+            atomicOr(p.status, bad);
+        prefix[r + 1] = L > 0 ? L + p.row_cost : 0;
+    }
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        int carry = 0;
+        for (int base = 0; base < Bv; base += 32) {
+            const int i = base + lane;
+            int v = i < Bv ? prefix[i + 1] : 0;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int n = __shfl_up_sync(kFull, v, off);
+                if (lane >= off)
+                    v += n;
+            }
+            v += carry;
+            if (i < Bv)
+                prefix[i + 1] = v;
+            carry = __shfl_sync(kFull, v, 31);
+        }
+        if (lane == 0)
+            prefix[0] = 0;
+    }
+    __syncthreads();
+}
+
+// Blocks that get work: at least kFusedMinTokens positions each, at most the
+// grid, at least one.
+__device__ __forceinline__ unsigned active_blocks(unsigned T, unsigned grid)
+{
+    unsigned Gu = (T + kFusedMinTokens - 1) / kFusedMinTokens;
+    if (Gu > grid)
+        Gu = grid;
+    return Gu < 1 ? 1 : Gu;
+}
+
+// First row whose positions reach past `start` (never an empty row).
+__device__ __forceinline__ int first_row(const int *prefix, int Bv, long long start)
+{
+    int lo = 0, hi = Bv - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if ((long long)prefix[mid + 1] > start)
+            hi = mid;
+        else
+            lo = mid + 1;
+    }
+    return lo;
+}
+
+// The per-step plan (int32 words): [0] T, [1] active blocks G, [2] grid,
+// [3] virtual rows Bv, [4] rows B, [5] page_size, [6..15] unused; then
+// prefix[0..Bv] (padded to a multiple of 4 words); then one entry of
+// kPlanEntryInts words per block of the grid: [0] its first row r0 (-1: no
+// work), [1] the base wb of that row's page-table window, [2] the row's
+// first table entry kv_indptr[b], [3] its entry count, [4] and [5] the
+// positions of the row's first and last-plus-one token, [6] and [7] the
+// block's positions [start, end), [8..71] the window (the row's table
+// entries wb .. wb + 63, 0 past the table).
+constexpr int kPlanHeaderInts = 16;
+constexpr int kPlanEntryInts = 72;
+
+__device__ __forceinline__ const int32_t *plan_entry(const int32_t *plan, int Bv, int c)
+{
+    return plan + kPlanHeaderInts + ((Bv + 1 + 3) & ~3) + (size_t)c * kPlanEntryInts;
+}
+
 template <int D, int HPC>
 __global__ void __launch_bounds__(FusedCfg<D, HPC>::kThreads, 1)
     fused_decode_kernel(const FusedParams p)
@@ -169,49 +271,135 @@ __global__ void __launch_bounds__(FusedCfg<D, HPC>::kThreads, 1)
     // inputs may come from the kernel just before (the append): wait for it
     grid_dependency_wait();
 
-    // ---- virtual-row lengths, checked, then their prefix sums -------------
-    for (int r = threadIdx.x; r < Bv; r += blockDim.x) {
-        const int b = r % p.B;
-        int L = p.seq_lens[b];
-        const int pg0 = p.kv_indptr[b];
-        const int pg1 = p.kv_indptr[b + 1];
-        unsigned bad = 0;
-        if (L < 0 || L > p.max_seq_len) {
-            bad |= kFlagBadLen;
-            L = L < 0 ? 0 : p.max_seq_len;
+    // ---- the producer's copy issue, shared by its early start (below) and
+    // its row loop.  Lanes 0-15 copy K rows, 16-31 V rows, of one 16-token
+    // stage; the page ids come from a 64-entry window of the row's table.
+    const int HQVb = HPC * p.n_rep;
+    const bool q_staged = HQVb * D * 2 <= C::kQCapBytes;
+    auto rope_row_needed = [&](long long lo_, long long hi_) {
+        const int pos = (int)(hi_ - lo_) - 1;
+        return p.step && p.rope != nullptr && pos < p.rope_max_pos;
+    };
+    const int my_t = lane & 15;
+    const bool my_v = lane >= 16;
+    auto page_of_tok = [&](int t) {
+        return p.ps_shift >= 0 ? (t >> p.ps_shift) : (t / p.page_size);
+    };
+    // the row's q block (and RoPE row) into shared memory, by lane 0
+    auto stage_q = [&](int b, int hg, long long lo, long long hi) {
+        if (lane == 0) {
+            const bool need_cs = rope_row_needed(lo, hi);
+            const uint32_t qbytes = (uint32_t)(HQVb * D * 2);
+            mbar_arrive_expect_tx(&qbar[0], qbytes + (need_cs ? D * 4 : 0));
+            bulk_copy_g2s(const_cast<__nv_bfloat16 *>(s_q),
+                          p.q + ((size_t)b * p.Hq + (size_t)hg * HQVb) * D, qbytes, &qbar[0]);
+            if (need_cs)
+                bulk_copy_g2s(const_cast<float *>(s_cs), p.rope + (size_t)(hi - lo - 1) * D,
+                              D * 4, &qbar[0]);
         }
-        if (pg0 < 0 || pg1 < pg0 || pg1 > p.num_indices) {
-            bad |= kFlagBadPage;
-            L = 0;
-        } else if ((long long)(pg1 - pg0) * p.page_size < (long long)L) {
-            bad |= kFlagBadPage;
-            L = (pg1 - pg0) * p.page_size;
+    };
+    // one stage: tokens tok .. tok + nvalid - 1 of the row piece ending at t1
+    // (row length Lrow), into ring stage st
+    auto issue_stage = [&](int st, int tok, int t1, int Lrow, int b, size_t head_off, int pg0,
+                           int npg, int &wb, int &idx0, int &idx1, uint64_t policy) {
+        fence_proxy_async_smem();
+        const int nvalid = min(C::kTok, t1 - tok);
+        if (page_of_tok(tok) >= wb + 32) {       // slide the window by 32
+            wb += 32;
+            idx0 = idx1;
+            idx1 = wb + 32 + lane < npg ? __ldg(p.kv_indices + pg0 + wb + 32 + lane) : 0;
         }
-        if (bad && cta == 0 && r < p.B)
-            atomicOr(p.status, bad);
-        prefix[r + 1] = L > 0 ? L + p.row_cost : 0;
-    }
-    __syncthreads();
-    if (warp == 0) {
-        int carry = 0;
-        for (int base = 0; base < Bv; base += 32) {
-            const int i = base + lane;
-            int v = i < Bv ? prefix[i + 1] : 0;
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const int n = __shfl_up_sync(kFull, v, off);
-                if (lane >= off)
-                    v += n;
-            }
-            v += carry;
-            if (i < Bv)
-                prefix[i + 1] = v;
-            carry = __shfl_sync(kFull, v, 31);
+        unsigned char *row = smem + st * C::kStageBytes +
+                             ((my_v ? C::kTok : 0) + my_t) * C::kPitch;
+        if (my_v && my_t >= nvalid) {
+            // V rows past the piece's end must be finite (P is 0 there)
+            uint4 *z = reinterpret_cast<uint4 *>(row);
+            for (int k = 0; k < C::kRowBytes / 16; ++k)
+                z[k] = make_uint4(0u, 0u, 0u, 0u);
         }
+        // every lane joins the shuffles; only lanes with a token use them
+        const int t = tok + (my_t < nvalid ? my_t : 0);
+        const int pi = page_of_tok(t);
+        const int sl = t - pi * p.page_size;
+        const int wofs = pi - wb;                  // in [0, 64)
+        const int e0 = __shfl_sync(kFull, idx0, wofs & 31);
+        const int e1 = __shfl_sync(kFull, idx1, wofs & 31);
+        int page = wofs < 32 ? e0 : e1;
+        // fused step: the row's last token is this step's new token; its
+        // K/V come from k_new / v_new (the consumers rotate K in place)
+        const int jn = (p.step && t1 == Lrow && tok + nvalid == t1) ? nvalid - 1 : -1;
         if (lane == 0)
-            prefix[0] = 0;
+            mbar_arrive_expect_tx(&full[st], (uint32_t)(nvalid * 2 * C::kRowBytes));
+        else
+            mbar_arrive(&full[st]);
+        if (my_t == jn) {
+            const __nv_bfloat16 *src =
+                (my_v ? p.v_new : p.k_new) + (size_t)b * p.Hkv * D + head_off;
+            bulk_copy_g2s(row, src, C::kRowBytes, &full[st]);
+        }
+        if (my_t < nvalid && my_t != jn) {
+            if (page < 0 || page >= p.num_pages) {
+                atomicOr(p.status, kFlagBadPage);
+                page = 0;
+            }
+            const __nv_bfloat16 *src = (my_v ? p.v_pool : p.k_pool) +
+                                       ((size_t)page * p.page_size + sl) * (size_t)p.Hkv * D +
+                                       head_off;
+            bulk_copy_g2s_hint(row, src, C::kRowBytes, &full[st], policy);
+        }
+    };
+
+    // ---- the partition: from the step's plan (one round trip: its prefix
+    // sums, and this block's first row, its bounds and page-table window), or
+    // computed here from the lengths (the plan's absence, or a plan made for
+    // another grid or shape)
+    bool planned = false;
+    bool early = false;               // producer: the first row's q and first stage issued
+    int plan_r0 = 0, plan_wb = 0, plan_w0 = 0, plan_w1 = 0, plan_pg0 = 0, plan_npg = 0;
+    if (p.plan != nullptr) {
+        const int32_t *pe = plan_entry(p.plan, Bv, cta);
+        const int hdr_grid = p.plan[2], hdr_bv = p.plan[3];
+        const int hdr_b = p.plan[4], hdr_ps = p.plan[5];
+        int e_lo = 0, e_hi = 0, e_start = 0, e_end = 0;
+        if (warp == HPC) {
+            const int ew = lane < 8 ? pe[lane] : 0;
+            plan_w0 = pe[8 + lane];
+            plan_w1 = pe[40 + lane];
+            plan_r0 = __shfl_sync(kFull, ew, 0);
+            plan_wb = __shfl_sync(kFull, ew, 1);
+            plan_pg0 = __shfl_sync(kFull, ew, 2);
+            plan_npg = __shfl_sync(kFull, ew, 3);
+            e_lo = __shfl_sync(kFull, ew, 4);
+            e_hi = __shfl_sync(kFull, ew, 5);
+            e_start = __shfl_sync(kFull, ew, 6);
+            e_end = __shfl_sync(kFull, ew, 7);
+        } else {
+            for (int i = threadIdx.x; i <= Bv; i += HPC * 32)
+                prefix[i] = p.plan[kPlanHeaderInts + i];
+            plan_r0 = pe[0];
+        }
+        planned = hdr_grid == (int)gridDim.x && hdr_bv == Bv && hdr_b == p.B &&
+                  hdr_ps == p.page_size;
+        if (planned && warp == HPC && plan_r0 >= 0) {
+            // Early start: the first row's q block and first stage go out now,
+            // from this block's entry alone; the compute warps meanwhile copy
+            // the prefix sums and meet this warp at the barrier below.
+            const int b = plan_r0 % p.B, hg = plan_r0 / p.B;
+            const int t0 = (e_start > e_lo ? e_start : e_lo) - e_lo;
+            const int t1 = (e_end < e_hi ? e_end : e_hi) - e_lo;
+            if (t1 > t0) {
+                if (q_staged)
+                    stage_q(b, hg, e_lo, e_hi);
+                int wb = plan_wb, idx0 = plan_w0, idx1 = plan_w1;
+                issue_stage(0, t0, t1, e_hi - e_lo, b, (size_t)hg * HPC * D, plan_pg0,
+                            plan_npg, wb, idx0, idx1, policy_evict_first());
+                early = true;
+            }
+        }
+        __syncthreads();
     }
-    __syncthreads();
+    if (!planned)
+        row_prefix(p, prefix, cta == 0);
 
     // T: the rows' total weight.  Token t of row r sits at position
     // prefix[r] + row_cost + t; block c owns positions [T c / G, T (c+1) / G).
@@ -220,11 +408,7 @@ __global__ void __launch_bounds__(FusedCfg<D, HPC>::kThreads, 1)
     // T c / G = (T / G) c + ((T % G) c) / G.
     const unsigned T = (unsigned)prefix[Bv];
     // fewer blocks when there is little work: at least kFusedMinTokens each
-    unsigned Gu = (T + kFusedMinTokens - 1) / kFusedMinTokens;
-    if (Gu > gridDim.x)
-        Gu = gridDim.x;
-    if (Gu < 1)
-        Gu = 1;
+    const unsigned Gu = active_blocks(T, gridDim.x);
     const int G = (int)Gu;
 
     // rows with no tokens: zero output, no pieces (owner: block r mod grid)
@@ -235,56 +419,53 @@ __global__ void __launch_bounds__(FusedCfg<D, HPC>::kThreads, 1)
                 p.out + ((size_t)b * p.Hq + (size_t)hg * HPC * p.n_rep) * D);
             for (int i = threadIdx.x; i < HPC * p.n_rep * D / 8; i += blockDim.x)
                 o[i] = make_uint4(0u, 0u, 0u, 0u);
-            if (threadIdx.x == 0) {
+            if (threadIdx.x == 0 && !planned) {
                 p.row_info[2 * r] = 0;
                 p.row_info[2 * r + 1] = 0;
             }
         }
     }
-    if (cta >= G)
+    // An unplanned call leaves its partition behind as the step's plan, for
+    // the planned calls of the same step (header and prefix sums: block 0;
+    // each block its own entry, the producer below for blocks with work).
+    int32_t *plan_e = p.plan_out != nullptr
+                          ? const_cast<int32_t *>(plan_entry(p.plan_out, Bv, cta)) : nullptr;
+    if (p.plan_out != nullptr && cta == 0) {
+        for (int i = threadIdx.x; i <= Bv; i += blockDim.x)
+            p.plan_out[kPlanHeaderInts + i] = prefix[i];
+        if (threadIdx.x == 0) {
+            p.plan_out[0] = (int)T;
+            p.plan_out[1] = G;
+            p.plan_out[2] = (int)gridDim.x;
+            p.plan_out[3] = Bv;
+            p.plan_out[4] = p.B;
+            p.plan_out[5] = p.page_size;
+        }
+    }
+    if (cta >= G) {
+        if (plan_e != nullptr && threadIdx.x == 0)
+            plan_e[0] = -1;
         return;
+    }
     const unsigned t_q = T / Gu, t_r = T % Gu;
     const long long start = (long long)t_q * cta + t_r * (unsigned)cta / Gu;
     const long long end = (long long)t_q * (cta + 1) + t_r * (unsigned)(cta + 1) / Gu;
-    if (start >= end)
+    if (start >= end) {
+        if (plan_e != nullptr && threadIdx.x == 0)
+            plan_e[0] = -1;
         return;
-
-    // first row whose positions reach past start (never an empty row)
-    int r0 = 0;
-    {
-        int lo = 0, hi = Bv - 1;
-        while (lo < hi) {
-            const int mid = (lo + hi) >> 1;
-            if ((long long)prefix[mid + 1] > start)
-                hi = mid;
-            else
-                lo = mid + 1;
-        }
-        r0 = lo;
     }
 
-    // the row's q block (and RoPE row) is staged in shared memory by the
-    // producer when it fits, so consumers never stall on q at a row start
-    const int HQVb = HPC * p.n_rep;
-    const bool q_staged = HQVb * D * 2 <= C::kQCapBytes;
-    auto rope_row_needed = [&](long long lo_, long long hi_) {
-        const int pos = (int)(hi_ - lo_) - 1;
-        return p.step && p.rope != nullptr && pos < p.rope_max_pos;
-    };
+    // first row whose positions reach past start (never an empty row)
+    const int r0 = planned ? plan_r0 : first_row(prefix, Bv, start);
 
     if (warp == HPC) {
         // ======================= producer warp ============================
-        const int my_t = lane & 15;
-        const bool my_v = lane >= 16;
-        const __nv_bfloat16 *pool = my_v ? p.v_pool : p.k_pool;
         // K/V are read once per call: first out of L2, so the page table,
         // q and the partials stay
         const uint64_t stream_policy = policy_evict_first();
-        int it = 0, pc = 0;
+        int it = early ? 1 : 0, pc = early && q_staged ? 1 : 0;
         bool aborted = false;
-        auto page_of_tok = [&](int t) {
-            return p.ps_shift >= 0 ? (t >> p.ps_shift) : (t / p.page_size);
-        };
         // the next row's first page-table window, loaded one row ahead
         int n_r = -1, n_idx0 = 0, n_idx1 = 0;
         auto prefetch_window = [&](int from) {
@@ -296,7 +477,9 @@ __global__ void __launch_bounds__(FusedCfg<D, HPC>::kThreads, 1)
                     continue;
                 const int bb = rr % p.B;
                 const int q0 = p.kv_indptr[bb];
-                const int nq = p.kv_indptr[bb + 1] - q0;
+                int nq = p.kv_indptr[bb + 1] - q0;
+                if (q0 < 0 || nq < 0 || q0 > p.num_indices - nq)
+                    nq = 0;                    // a table changed since the plan
                 n_idx0 = lane < nq ? __ldg(p.kv_indices + q0 + lane) : 0;
                 n_idx1 = 32 + lane < nq ? __ldg(p.kv_indices + q0 + 32 + lane) : 0;
                 n_r = rr;
@@ -310,26 +493,50 @@ __global__ void __launch_bounds__(FusedCfg<D, HPC>::kThreads, 1)
                 break;
             if (hi == prefix[r])
                 continue;
+            const bool first_early = early && r == r0;
             const int t0 = (int)((start > lo ? start : lo) - lo);
             const int t1 = (int)((end < hi ? end : hi) - lo);
             const int b = r % p.B, hg = r / p.B;
-            const int pg0 = p.kv_indptr[b];
-            const int npg = p.kv_indptr[b + 1] - pg0;      // >= pages the row's tokens use
+            int pg0, npg;                                  // npg >= pages the row's tokens use
+            if (planned && r == r0) {
+                pg0 = plan_pg0;                            // checked by the plan
+                npg = plan_npg;
+            } else {
+                pg0 = p.kv_indptr[b];
+                npg = p.kv_indptr[b + 1] - pg0;
+                if (pg0 < 0 || npg < 0 || pg0 > p.num_indices - npg)
+                    npg = 0;                               // a table changed since the plan
+            }
             const size_t head_off = (size_t)hg * HPC * D;
             // page-table window: lane l holds entries wb + l and wb + 32 + l of
             // the row, loaded one window ahead of use; a 16-token tile spans at
             // most 17 consecutive entries, which always lie inside the window
             int wb = (page_of_tok(t0) >> 5) << 5;
             int idx0, idx1;
-            if (n_r == r && wb == 0) {
+            if (planned && r == r0 && wb == plan_wb) {
+                idx0 = plan_w0;
+                idx1 = plan_w1;
+            } else if (n_r == r && wb == 0) {
                 idx0 = n_idx0;
                 idx1 = n_idx1;
             } else {
                 idx0 = wb + lane < npg ? __ldg(p.kv_indices + pg0 + wb + lane) : 0;
                 idx1 = wb + 32 + lane < npg ? __ldg(p.kv_indices + pg0 + wb + 32 + lane) : 0;
             }
+            if (plan_e != nullptr && r == r0) {
+                // this block's plan entry: its first row, that row's bounds and
+                // the page-table window its first stage reads
+                plan_e[8 + lane] = idx0;
+                plan_e[40 + lane] = idx1;
+                if (lane < 8) {
+                    const long long v = lane == 0 ? r0 : lane == 1 ? wb : lane == 2 ? pg0
+                                      : lane == 3 ? npg : lane == 4 ? lo : lane == 5 ? hi
+                                      : lane == 6 ? start : end;
+                    plan_e[lane] = (int)v;
+                }
+            }
             // stage the row's q block (and RoPE row) for the consumers
-            if (q_staged) {
+            if (q_staged && !first_early) {
                 if (pc > 0) {
                     const bool ok = mbar_wait_bounded(&qbar[1], (uint32_t)((pc - 1) & 1),
                                                       p.handoff_wait_ns);
@@ -342,21 +549,12 @@ __global__ void __launch_bounds__(FusedCfg<D, HPC>::kThreads, 1)
                         break;
                     }
                 }
-                if (lane == 0) {
-                    const bool need_cs = rope_row_needed(lo, hi);
-                    const uint32_t qbytes = (uint32_t)(HQVb * D * 2);
-                    mbar_arrive_expect_tx(&qbar[0], qbytes + (need_cs ? D * 4 : 0));
-                    bulk_copy_g2s(const_cast<__nv_bfloat16 *>(s_q),
-                                  p.q + ((size_t)b * p.Hq + (size_t)hg * HQVb) * D, qbytes,
-                                  &qbar[0]);
-                    if (need_cs)
-                        bulk_copy_g2s(const_cast<float *>(s_cs),
-                                      p.rope + (size_t)(hi - lo - 1) * D, D * 4, &qbar[0]);
-                }
+                stage_q(b, hg, lo, hi);
                 ++pc;
             }
             prefetch_window(r + 1);
-            for (int tok = t0; tok < t1; tok += C::kTok, ++it) {
+            // (the early start issued the first row's first stage already)
+            for (int tok = t0 + (first_early ? C::kTok : 0); tok < t1; tok += C::kTok, ++it) {
                 const int st = it % NST;
                 if (it >= NST) {
                     const bool ok = mbar_wait_bounded(&empty[st], (uint32_t)(((it / NST) - 1) & 1),
@@ -370,51 +568,8 @@ __global__ void __launch_bounds__(FusedCfg<D, HPC>::kThreads, 1)
                         break;
                     }
                 }
-                fence_proxy_async_smem();
-                const int nvalid = min(C::kTok, t1 - tok);
-                if (page_of_tok(tok) >= wb + 32) {       // slide the window by 32
-                    wb += 32;
-                    idx0 = idx1;
-                    idx1 = wb + 32 + lane < npg ? __ldg(p.kv_indices + pg0 + wb + 32 + lane) : 0;
-                }
-                unsigned char *row = smem + st * C::kStageBytes +
-                                     ((my_v ? C::kTok : 0) + my_t) * C::kPitch;
-                if (my_v && my_t >= nvalid) {
-                    // V rows past the piece's end must be finite (P is 0 there)
-                    uint4 *z = reinterpret_cast<uint4 *>(row);
-                    for (int k = 0; k < C::kRowBytes / 16; ++k)
-                        z[k] = make_uint4(0u, 0u, 0u, 0u);
-                }
-                // every lane joins the shuffles; only lanes with a token use them
-                const int t = tok + (my_t < nvalid ? my_t : 0);
-                const int pi = page_of_tok(t);
-                const int sl = t - pi * p.page_size;
-                const int wofs = pi - wb;                  // in [0, 64)
-                const int e0 = __shfl_sync(kFull, idx0, wofs & 31);
-                const int e1 = __shfl_sync(kFull, idx1, wofs & 31);
-                int page = wofs < 32 ? e0 : e1;
-                // fused step: the row's last token is this step's new token; its
-                // K/V come from k_new / v_new (the consumers rotate K in place)
-                const int jn = (p.step && t1 == (int)(hi - lo) && tok + nvalid == t1)
-                                   ? nvalid - 1 : -1;
-                if (lane == 0)
-                    mbar_arrive_expect_tx(&full[st], (uint32_t)(nvalid * 2 * C::kRowBytes));
-                else
-                    mbar_arrive(&full[st]);
-                if (my_t == jn) {
-                    const __nv_bfloat16 *src =
-                        (my_v ? p.v_new : p.k_new) + (size_t)b * p.Hkv * D + head_off;
-                    bulk_copy_g2s(row, src, C::kRowBytes, &full[st]);
-                }
-                if (my_t < nvalid && my_t != jn) {
-                    if (page < 0 || page >= p.num_pages) {
-                        atomicOr(p.status, kFlagBadPage);
-                        page = 0;
-                    }
-                    const __nv_bfloat16 *src =
-                        pool + ((size_t)page * p.page_size + sl) * (size_t)p.Hkv * D + head_off;
-                    bulk_copy_g2s_hint(row, src, C::kRowBytes, &full[st], stream_policy);
-                }
+                issue_stage(st, tok, t1, (int)(hi - lo), b, head_off, pg0, npg, wb, idx0, idx1,
+                            stream_policy);
             }
         }
         // Let the copies already issued land before this warp exits, with the
@@ -459,7 +614,7 @@ __global__ void __launch_bounds__(FusedCfg<D, HPC>::kThreads, 1)
         const size_t qrow0 = (size_t)b * p.Hq + (size_t)kvh * p.n_rep;
         const int first = block_of(lo, T, G);
         const int last = block_of(hi - 1, T, G);
-        if (t0 == 0 && warp == 0 && lane == 0) {
+        if (t0 == 0 && warp == 0 && lane == 0 && !planned) {
             p.row_info[2 * r] = first;
             p.row_info[2 * r + 1] = last - first + 1;
         }
@@ -531,7 +686,10 @@ __global__ void __launch_bounds__(FusedCfg<D, HPC>::kThreads, 1)
         if (has_new) {
             const int tn = Lrow - 1;
             const int pin = p.ps_shift >= 0 ? (tn >> p.ps_shift) : (tn / p.page_size);
-            new_page = __ldg(p.kv_indices + p.kv_indptr[b] + pin);
+            const int e0 = p.kv_indptr[b], e1 = p.kv_indptr[b + 1];
+            // (a table changed since the plan: no page, flagged at the write)
+            new_page = e0 >= 0 && pin < e1 - e0 && e1 <= p.num_indices
+                           ? __ldg(p.kv_indices + e0 + pin) : -1;
             if (p.rope != nullptr) {
                 new_rope_ok = tn < p.rope_max_pos;
                 if (new_rope_ok) {
@@ -683,6 +841,77 @@ __global__ void __launch_bounds__(FusedCfg<D, HPC>::kThreads, 1)
     grid_launch_dependents();
 }
 
+// ---- the per-step plan ------------------------------------------------------
+// The partition the decode kernel would compute at its start, written once
+// for every call of a step (commits by author, the decode metadata built
+// once per step and reused by every layer): the prefix sums, each row's
+// first block and piece count (row_info, read by the piece combine), and for
+// every block its first row and that row's page-table window.  A planned
+// decode call then starts its copies after one round trip to memory instead
+// of three.  One block per decode block; dynamic shared memory: Bv + 1 ints.
+__global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(const FusedParams p,
+                                                                   int32_t *plan)
+{
+    extern __shared__ int pl_prefix[];
+    const int Bv = p.Bv, cta = blockIdx.x, tid = threadIdx.x;
+    grid_dependency_wait();
+    row_prefix(p, pl_prefix, cta == 0);
+    const unsigned T = (unsigned)pl_prefix[Bv];
+    const unsigned Gu = active_blocks(T, gridDim.x);
+    const int G = (int)Gu;
+    if (cta == 0) {
+        for (int i = tid; i <= Bv; i += blockDim.x)
+            plan[kPlanHeaderInts + i] = pl_prefix[i];
+        for (int r = tid; r < Bv; r += blockDim.x) {
+            const long long lo = (long long)pl_prefix[r] + p.row_cost, hi = pl_prefix[r + 1];
+            int first = 0, n = 0;
+            if (hi != pl_prefix[r]) {
+                first = block_of(lo, T, G);
+                n = block_of(hi - 1, T, G) - first + 1;
+            }
+            p.row_info[2 * r] = first;
+            p.row_info[2 * r + 1] = n;
+        }
+        if (tid == 0) {
+            plan[0] = (int)T;
+            plan[1] = G;
+            plan[2] = (int)gridDim.x;
+            plan[3] = Bv;
+            plan[4] = p.B;
+            plan[5] = p.page_size;
+        }
+    }
+    int32_t *e = const_cast<int32_t *>(plan_entry(plan, Bv, cta));
+    const unsigned t_q = T / Gu, t_r = T % Gu;
+    const long long start = (long long)t_q * cta + t_r * (unsigned)cta / Gu;
+    const long long end = (long long)t_q * (cta + 1) + t_r * (unsigned)(cta + 1) / Gu;
+    if (cta >= G || start >= end) {
+        if (tid == 0)
+            e[0] = -1;
+        return;
+    }
+    const int r0 = first_row(pl_prefix, Bv, start);
+    const long long lo = (long long)pl_prefix[r0] + p.row_cost;
+    const int t0 = (int)((start > lo ? start : lo) - lo);
+    const int b = r0 % p.B;
+    const int pg0 = p.kv_indptr[b];
+    const int npg = p.kv_indptr[b + 1] - pg0;        // checked by row_prefix
+    const int pi = p.ps_shift >= 0 ? (t0 >> p.ps_shift) : (t0 / p.page_size);
+    const int wb = (pi >> 5) << 5;
+    if (tid < 64)
+        e[8 + tid] = wb + tid < npg ? __ldg(p.kv_indices + pg0 + wb + tid) : 0;
+    if (tid == 0) {
+        e[0] = r0;
+        e[1] = wb;
+        e[2] = pg0;
+        e[3] = npg;
+        e[4] = (int)lo;
+        e[5] = pl_prefix[r0 + 1];
+        e[6] = (int)start;
+        e[7] = (int)end;
+    }
+}
+
 // ---- merge the pieces of every row that has more than one ------------------
 // An item is one (virtual row, query head, column slice of D / DS): a group
 // of WPH warps merges it.  Warp w takes pieces w, w + WPH, ... in rounds of
@@ -706,6 +935,27 @@ __global__ void __launch_bounds__(WPH > 8 ? 32 * WPH : 256)
     // block of this grid has started; it waits for this grid's completion
     // before it reads anything this grid writes
     grid_launch_dependents();
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int grp = warp / WPH, wi = warp % WPH;
+    const long long item = (long long)blockIdx.x * GROUPS + grp;
+    const bool live = item < (long long)p.Bv * p.HQV * DS && !(p.adv.seq_lens != nullptr &&
+                                                               blockIdx.x == gridDim.x - 1);
+    int n = 0, first = 0, r = 0, j = 0, col = lane * V;
+    if (live) {
+        const long long pair = item / DS;
+        r = (int)(pair / p.HQV);
+        j = (int)(pair % p.HQV);
+        col += (int)(item % DS) * DW;
+    }
+    // With a plan, each row's first block and piece count were written by the
+    // plan kernel, which completed before the decode grid passed its own
+    // wait: read them while the decode grid finishes.  Without one the decode
+    // grid writes them: read them after the wait.
+    if (p.planned && live) {
+        first = p.row_info[2 * r];
+        n = p.row_info[2 * r + 1];
+    }
     grid_dependency_wait();
     // paged_decode_step_advance: the last block advances the metadata for the
     // next step; the decode grid, the only reader of it, has completed
@@ -713,17 +963,7 @@ __global__ void __launch_bounds__(WPH > 8 ? 32 * WPH : 256)
         advance_block(p.adv);
         return;
     }
-    const int lane = threadIdx.x & 31;
-    const int warp = threadIdx.x >> 5;
-    const int grp = warp / WPH, wi = warp % WPH;
-    const long long item = (long long)blockIdx.x * GROUPS + grp;
-    const bool live = item < (long long)p.Bv * p.HQV * DS;
-    int n = 0, first = 0, r = 0, j = 0, col = lane * V;
-    if (live) {
-        const long long pair = item / DS;
-        r = (int)(pair / p.HQV);
-        j = (int)(pair % p.HQV);
-        col += (int)(item % DS) * DW;
+    if (!p.planned && live) {
         first = p.row_info[2 * r];
         n = p.row_info[2 * r + 1];
     }
@@ -841,9 +1081,9 @@ __global__ void __launch_bounds__(WPH > 8 ? 32 * WPH : 256)
     }
 }
 
-template <typename Kernel, typename Params>
+template <typename Kernel, typename... Params>
 cudaError_t launch_pdl(Kernel k, dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
-                       const Params &p)
+                       const Params &...p)
 {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
@@ -855,7 +1095,7 @@ cudaError_t launch_pdl(Kernel k, dim3 grid, dim3 block, size_t smem, cudaStream_
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, k, p);
+    return cudaLaunchKernelEx(&cfg, k, p...);
 }
 
 template <int D, int HPC>
@@ -940,6 +1180,17 @@ extern "C" pkv_status pkv_testing_set_handoff_wait_ns(unsigned long long ns)
 }
 
 namespace pkv {
+
+cudaError_t launch_decode_plan(const FusedParams &p, int grid, int32_t *plan,
+                               cudaStream_t stream)
+{
+    const size_t smem = ((size_t)p.Bv + 1) * sizeof(int);
+    cudaError_t e = launch_pdl(decode_plan_kernel, dim3(grid), dim3(kPlanThreads), smem, stream,
+                               p, plan);
+    if (e != cudaSuccess)
+        return e;
+    return cudaGetLastError();
+}
 
 cudaError_t launch_piece_combine(const PieceCombineParams &p, int D, int grid_blocks,
                                  cudaStream_t stream)

@@ -153,7 +153,21 @@ struct FusedParams {
     // producer and the consumers (normally the full ~2 s; shortened only by
     // the testing call).  Waits for copies already issued keep the full limit.
     unsigned long long handoff_wait_ns;
+    // the step's plan (paged_decode_plan) or nullptr: the partition computed
+    // at the kernel's start instead
+    const int32_t *plan;
+    // unplanned calls: where to leave the partition as the step's plan
+    // (nullptr: nowhere)
+    int32_t *plan_out;
 };
+
+// Threads of a plan block.
+constexpr int kPlanThreads = 256;
+// int32 words of the plan for Bv virtual rows and a grid of `grid` blocks.
+inline size_t plan_words(int Bv, int grid)
+{
+    return 16 + (((size_t)Bv + 1 + 3) & ~(size_t)3) + (size_t)72 * grid;
+}
 
 // The hand-off wait limit launches use (pkv_testing_set_handoff_wait_ns).
 unsigned long long handoff_wait_ns();
@@ -164,6 +178,7 @@ struct PieceCombineParams {
     const int32_t *row_info;
     __nv_bfloat16 *out;
     int B, Bv, Hq, HQV;
+    int planned;           // row_info written by the plan kernel (read before the wait)
     // paged_decode_step_advance: one extra block runs the metadata advance
     // (adv.seq_lens == nullptr: none)
     AdvanceParams adv;
@@ -190,6 +205,10 @@ cudaError_t launch_combine(const CombineParams &p, cudaStream_t stream);
 cudaError_t launch_fused_decode(const FusedParams &p, int D, int grid, cudaStream_t stream);
 cudaError_t launch_piece_combine(const PieceCombineParams &p, int D, int grid_blocks,
                                  cudaStream_t stream);
+// The per-step plan for the decode kernel's grid of `grid` blocks; p carries
+// the shape, the tables, row_info and the status word.
+cudaError_t launch_decode_plan(const FusedParams &p, int grid, int32_t *plan,
+                               cudaStream_t stream);
 int fused_heads_per_block(int Hkv);
 
 // Resident split-decode blocks per SM for head dim D (shared-memory bound).

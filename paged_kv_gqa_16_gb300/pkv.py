@@ -38,7 +38,8 @@ EXPORTS = (
     "paged_decode_step", "paged_decode_partials", "decode_combine", "pkv_status_str",
     "pkv_version", "paged_decode_attn_noalloc", "paged_kv_advance", "decode_attn_contig",
     "paged_prefill_attn", "paged_kv_extend", "paged_decode_step_advance",
-    "pkv_testing_set_handoff_wait_ns",
+    "pkv_testing_set_handoff_wait_ns", "paged_decode_plan", "paged_decode_attn_planned",
+    "paged_decode_step_planned",
 )
 
 
@@ -87,6 +88,9 @@ def lib():
             "paged_kv_append": (I, [DP, P, P, P, P, P, P, P, P, P, I, I, P, P]),
             "paged_decode_attn": (I, [DP, P, P, P, P, P, P, I, P, Z, P, P]),
             "paged_decode_step": (I, [DP, P, P, P, P, P, P, P, P, P, I, I, P, Z, P, P]),
+            "paged_decode_plan": (I, [DP, P, P, P, I, P, Z, P]),
+            "paged_decode_attn_planned": (I, [DP, P, P, P, P, P, P, I, P, Z, P, P]),
+            "paged_decode_step_planned": (I, [DP, P, P, P, P, P, P, P, P, P, I, I, P, Z, P, P]),
             "paged_decode_partials": (I, [DP, P, P, P, P, P, P, I, P, Z, P]),
             "decode_combine": (I, [DP, P, P, I, P, P]),
             "paged_decode_attn_noalloc": (I, [DP, P, P, P, P, P, P, I, P, P, P]),
@@ -205,6 +209,35 @@ def paged_decode_step(d: Dims, q, k_new, v_new, k_pool, v_pool, kv_indices, kv_i
                       out, stream=None) -> None:
     ws_bytes = workspace.numel() * workspace.element_size()
     _check("paged_decode_step", lib().paged_decode_step(
+        ctypes.byref(d), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_pool), _ptr(v_pool),
+        _ptr(kv_indices), _ptr(kv_indptr), _ptr(seq_lens), _ptr(rope_cos_sin), rope_max_pos,
+        num_splits, _ptr(workspace), ws_bytes, _ptr(out), _stream(stream)))
+
+
+def paged_decode_plan(d: Dims, kv_indices, kv_indptr, seq_lens, num_splits: int, workspace,
+                      stream=None) -> None:
+    """The step's plan (the block partition and first page-table windows)
+    written into the workspace for the *_planned calls of the same step."""
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check("paged_decode_plan", lib().paged_decode_plan(
+        ctypes.byref(d), _ptr(kv_indices), _ptr(kv_indptr), _ptr(seq_lens), num_splits,
+        _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def paged_decode_attn_planned(d: Dims, q, k_pool, v_pool, kv_indices, kv_indptr, seq_lens,
+                              num_splits: int, workspace, out, stream=None) -> None:
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check("paged_decode_attn_planned", lib().paged_decode_attn_planned(
+        ctypes.byref(d), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(kv_indices),
+        _ptr(kv_indptr), _ptr(seq_lens), num_splits, _ptr(workspace), ws_bytes, _ptr(out),
+        _stream(stream)))
+
+
+def paged_decode_step_planned(d: Dims, q, k_new, v_new, k_pool, v_pool, kv_indices, kv_indptr,
+                              seq_lens, rope_cos_sin, rope_max_pos: int, num_splits: int,
+                              workspace, out, stream=None) -> None:
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check("paged_decode_step_planned", lib().paged_decode_step_planned(
         ctypes.byref(d), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_pool), _ptr(v_pool),
         _ptr(kv_indices), _ptr(kv_indptr), _ptr(seq_lens), _ptr(rope_cos_sin), rope_max_pos,
         num_splits, _ptr(workspace), ws_bytes, _ptr(out), _stream(stream)))

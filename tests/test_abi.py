@@ -230,3 +230,33 @@ def test_prefill_argument_checks():
     assert call(d, qo=fake + 2) == pkv.PKV_ERR_INVALID_ARG
     assert call(_d(B=70000 // 8, Hkv=8)) == pkv.PKV_ERR_UNSUPPORTED  # B * Hkv > 65535
     assert call(d, total_q=0) == pkv.PKV_OK                           # nothing to do
+
+
+def test_plan_argument_checks():
+    """paged_decode_plan refuses bad arguments on the host, before any launch."""
+    import ctypes
+    L = pkv.lib()
+    d = _d()
+    S = 8
+    need = pkv.workspace_bytes(d, S)
+    fake = 1 << 32
+    # num_splits out of range
+    assert L.paged_decode_plan(ctypes.byref(d), fake, fake, fake, 0, fake, need, None) == \
+        pkv.PKV_ERR_INVALID_ARG
+    # no workspace, or one too small
+    assert L.paged_decode_plan(ctypes.byref(d), fake, fake, fake, S, None, need, None) == \
+        pkv.PKV_ERR_INVALID_ARG
+    assert L.paged_decode_plan(ctypes.byref(d), fake, fake, fake, S, fake, need - 256, None) == \
+        pkv.PKV_ERR_WORKSPACE_TOO_SMALL
+    # a misaligned workspace
+    assert L.paged_decode_plan(ctypes.byref(d), fake, fake, fake, S, fake + 16, need, None) == \
+        pkv.PKV_ERR_INVALID_ARG
+    # an empty batch needs no plan
+    d0 = _d(B=0)
+    assert L.paged_decode_plan(ctypes.byref(d0), None, None, None, S, None, 0, None) == pkv.PKV_OK
+
+
+def test_workspace_holds_the_plan():
+    """The workspace grows with the plan: one 72-word entry per block."""
+    d = _d()
+    assert pkv.workspace_bytes(d, 152) - pkv.workspace_bytes(d, 8) >= 144 * 72 * 4
