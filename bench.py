@@ -53,6 +53,8 @@ if ROOT not in sys.path:
 METRIC = "paged GQA decode attn: µs/call and KV-read GB/s (% of GB300 HBM peak)"
 FALLBACK_HBM_GBS = 6800.0
 HEADLINE = "serving_b128"
+# layers of the pages' 1.2B model: the calls of one decode step in a replay
+LAYERS = 24
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "fused_decode_traffic.json")
 DECODE_SRC = os.path.join(ROOT, "paged_kv_gqa_16_gb300", "csrc", "pkv_fused.cu")
 
@@ -601,12 +603,13 @@ def measure_config(pkv, w, dev, stream, l2, flush_l2, peak, splits=0):
         return statistics.median(ms)
 
     out = {"splits": st.S, "kv_bytes": kv, "alg_bytes": alg, "tokens": w.total_tokens}
+    # a replay is one decode step of a 24-layer model (the pages' 1.2B model)
     if b2b:
-        n = 20
+        n = LAYERS
         mode = (f"back to back, {n} steps per replay (the first leaves the plan), "
                 f"K+V = {kv / l2:.1f} x L2, no flush")
     else:
-        n = max(copies, 20 // copies * copies)
+        n = -(-LAYERS // copies) * copies
         mode = (f"rotation over {copies} layers' pools ({copies * kv / l2:.1f} x L2 of K+V), "
                 f"{n} steps per replay (the first leaves the plan)")
     out.update(line(per_step(n, True), mode, {"replays": 15}))
