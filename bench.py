@@ -844,14 +844,6 @@ def run_pkv(args):
     del g_step
     planned = st.planned
     st_config = config_of(w, world, args.layout)
-    headline_entry = {"splits": S, "kv_bytes": kv_bytes, "alg_bytes": alg_bytes,
-                      "tokens": w.total_tokens, "us_per_call": round(1e3 * ms_region, 2),
-                      "kv_gbs": round(kv_bytes / (ms_region * 1e-3) / 1e9, 1),
-                      "pct_hbm": round(100.0 * kv_bytes / (ms_region * 1e-3) / 1e9 / peak, 1),
-                      "roofline_frac": round(achieved / peak, 4),
-                      "l2": "the headline's timed region (see config)"}
-    if args.layout != "paged":
-        headline_entry = None
     del st
     torch.cuda.empty_cache()
 
@@ -861,9 +853,6 @@ def run_pkv(args):
     if args.configs != "none":
         names_c = config_names() if args.configs == "all" else args.configs.split(",")
         for name in names_c:
-            if name == w.name and headline_entry is not None:
-                configs[name] = headline_entry
-                continue
             wc = wl.make(name, seed=rank)
             configs[name] = measure_config(pkv, wc, dev, stream, l2, flush_l2, peak)
             if name == "ragged_b32":

@@ -388,11 +388,12 @@ __global__ void __launch_bounds__(FusedCfg<D, HPC>::kThreads, 1)
             const int t0 = (e_start > e_lo ? e_start : e_lo) - e_lo;
             const int t1 = (e_end < e_hi ? e_end : e_hi) - e_lo;
             if (t1 > t0) {
-                if (q_staged)
-                    stage_q(b, hg, e_lo, e_hi);
+                // K/V first: the q block is small and lands long before them
                 int wb = plan_wb, idx0 = plan_w0, idx1 = plan_w1;
                 issue_stage(0, t0, t1, e_hi - e_lo, b, (size_t)hg * HPC * D, plan_pg0,
                             plan_npg, wb, idx0, idx1, policy_evict_first());
+                if (q_staged)
+                    stage_q(b, hg, e_lo, e_hi);
                 early = true;
             }
         }
