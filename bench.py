@@ -696,25 +696,28 @@ def run_pkv(args):
             ck[b, :L] = st.k_pool[pages].reshape(-1, w.Hkv, w.D)[:L]
             cv[b, :L] = st.v_pool[pages].reshape(-1, w.Hkv, w.D)[:L]
         del st.k_pool, st.v_pool, st.k_pools, st.v_pools
-        st.planned = False
         torch.cuda.empty_cache()
         cd = pkv.dims(w.B, w.Hq, w.Hkv, w.D, cache_len, w.B, w.B, cache_len, w.scale)
         cws = pkv.alloc_workspace(cd, S, dev)
         st.ws = cws
 
+        use_plan = not args.no_plan
+
         def step(i=0, a=None, planned=False):
             pkv.decode_attn_contig(cd, st.q, ck, cv, st.seq_lens, S, cws, st.out,
                                    k_new=st.k_new, v_new=st.v_new, rope_cos_sin=st.rope,
-                                   rope_max_pos=st.rope_rows)
+                                   rope_max_pos=st.rope_rows, planned=planned and use_plan)
 
         def decode(i=0, planned=False):
-            pkv.decode_attn_contig(cd, st.q, ck, cv, st.seq_lens, S, cws, st.out)
+            pkv.decode_attn_contig(cd, st.q, ck, cv, st.seq_lens, S, cws, st.out,
+                                   planned=planned and use_plan)
 
         args.no_e2e = True
         args.no_loop = True
         args.configs = "none"
 
-    launches_per_step = (1 if S == 1 else 2) + (1 if args.layout == "contig" else 0)
+    # (a contiguous cache adds its table launch to a step's first call only)
+    launches_per_step = (1 if S == 1 else 2)
     for _ in range(max(3, args.warmup)):
         step()
     torch.cuda.synchronize(dev)
@@ -1014,7 +1017,8 @@ def run_pkv(args):
                                      "event/launch floor of an isolated call"},
         "decode_only": {"call": "paged_decode_attn", "us": round(1e3 * ms_dec_max, 2),
                         "kv_read_gbs": round(kv_bytes / (ms_dec_max * 1e-3) / 1e9, 1)},
-        "gpu_launches": K * launches_per_step,
+        "gpu_launches": K * launches_per_step + (
+            0 if args.layout != "contig" else (reps if planned else K)),
         "clocks": clocks,
         "wall_s_timed": round(wall, 4),
         "e2e": e2e,

@@ -337,6 +337,19 @@ pkv_status decode_attn_contig(const pkv_dims *dims, const void *q, const void *k
                               void *workspace, size_t ws_bytes, void *out,
                               pkv_stream_t stream);
 
+/* decode_attn_contig for the later layers of a step: it reuses the one-entry
+ * table and the plan (paged_decode_plan) that the step's first
+ * decode_attn_contig call left in this workspace, so it launches no table
+ * kernel and runs the planned decode (or step).  Valid while dims,
+ * num_splits, cache_batch_idx and seq_lens are those of that first call.
+ * Arguments and results are those of decode_attn_contig, bit for bit. */
+pkv_status decode_attn_contig_planned(const pkv_dims *dims, const void *q, const void *k_new,
+                                      const void *v_new, void *k_cache, void *v_cache,
+                                      const int32_t *cache_batch_idx, const int32_t *seq_lens,
+                                      const float *rope_cos_sin, int rope_max_pos,
+                                      int num_splits, void *workspace, size_t ws_bytes,
+                                      void *out, pkv_stream_t stream);
+
 /* ---- the decode loop on the device --------------------------------------- */
 
 /* Advance the decode metadata by one token per live row, on the device, so

@@ -726,11 +726,12 @@ pkv_status paged_decode_step_advance(const pkv_dims *dims, const void *q, const 
     return launch_status(pkv::launch_advance(adv, (cudaStream_t)stream));
 }
 
-pkv_status decode_attn_contig(const pkv_dims *dims, const void *q, const void *k_new,
+static pkv_status contig_impl(const pkv_dims *dims, const void *q, const void *k_new,
                               const void *v_new, void *k_cache, void *v_cache,
                               const int32_t *cache_batch_idx, const int32_t *seq_lens,
                               const float *rope_cos_sin, int rope_max_pos, int num_splits,
-                              void *workspace, size_t ws_bytes, void *out, pkv_stream_t stream)
+                              void *workspace, size_t ws_bytes, void *out, pkv_stream_t stream,
+                              bool planned)
 {
     if (dims == nullptr)
         return PKV_ERR_INVALID_ARG;
@@ -755,16 +756,43 @@ pkv_status decode_attn_contig(const pkv_dims *dims, const void *q, const void *k
     const Layout L = layout_for(&d, num_splits);
     int32_t *kv_indptr = reinterpret_cast<int32_t *>(static_cast<char *>(workspace) + L.table_off);
     int32_t *kv_indices = kv_indptr + d.B + 1;
-    st = launch_status(
-        pkv::launch_contig_table(cache_batch_idx, d.B, kv_indptr, (cudaStream_t)stream));
-    if (st != PKV_OK)
-        return st;
+    // a planned call finds the table, like the plan, where the step's first
+    // call left it
+    if (!planned) {
+        st = launch_status(
+            pkv::launch_contig_table(cache_batch_idx, d.B, kv_indptr, (cudaStream_t)stream));
+        if (st != PKV_OK)
+            return st;
+    }
     if (k_new != nullptr)
-        return paged_decode_step(&d, q, k_new, v_new, k_cache, v_cache, kv_indices, kv_indptr,
-                                 seq_lens, rope_cos_sin, rope_max_pos, num_splits, workspace,
-                                 ws_bytes, out, stream);
-    return paged_decode_attn(&d, q, k_cache, v_cache, kv_indices, kv_indptr, seq_lens,
-                             num_splits, workspace, ws_bytes, out, stream);
+        return decode_step_impl(&d, q, k_new, v_new, k_cache, v_cache, kv_indices, kv_indptr,
+                                seq_lens, rope_cos_sin, rope_max_pos, num_splits, workspace,
+                                ws_bytes, out, stream, planned);
+    return decode_attn_impl(&d, q, k_cache, v_cache, kv_indices, kv_indptr, seq_lens,
+                            num_splits, workspace, ws_bytes, out, stream, planned);
+}
+
+pkv_status decode_attn_contig(const pkv_dims *dims, const void *q, const void *k_new,
+                              const void *v_new, void *k_cache, void *v_cache,
+                              const int32_t *cache_batch_idx, const int32_t *seq_lens,
+                              const float *rope_cos_sin, int rope_max_pos, int num_splits,
+                              void *workspace, size_t ws_bytes, void *out, pkv_stream_t stream)
+{
+    return contig_impl(dims, q, k_new, v_new, k_cache, v_cache, cache_batch_idx, seq_lens,
+                       rope_cos_sin, rope_max_pos, num_splits, workspace, ws_bytes, out, stream,
+                       false);
+}
+
+pkv_status decode_attn_contig_planned(const pkv_dims *dims, const void *q, const void *k_new,
+                                      const void *v_new, void *k_cache, void *v_cache,
+                                      const int32_t *cache_batch_idx, const int32_t *seq_lens,
+                                      const float *rope_cos_sin, int rope_max_pos,
+                                      int num_splits, void *workspace, size_t ws_bytes,
+                                      void *out, pkv_stream_t stream)
+{
+    return contig_impl(dims, q, k_new, v_new, k_cache, v_cache, cache_batch_idx, seq_lens,
+                       rope_cos_sin, rope_max_pos, num_splits, workspace, ws_bytes, out, stream,
+                       true);
 }
 
 pkv_status paged_prefill_attn(const pkv_dims *dims, const void *q, const int32_t *qo_indptr,

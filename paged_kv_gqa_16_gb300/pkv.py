@@ -39,7 +39,7 @@ EXPORTS = (
     "pkv_version", "paged_decode_attn_noalloc", "paged_kv_advance", "decode_attn_contig",
     "paged_prefill_attn", "paged_kv_extend", "paged_decode_step_advance",
     "pkv_testing_set_handoff_wait_ns", "paged_decode_plan", "paged_decode_attn_planned",
-    "paged_decode_step_planned",
+    "paged_decode_step_planned", "decode_attn_contig_planned",
 )
 
 
@@ -98,6 +98,7 @@ def lib():
             "paged_decode_step_advance": (I, [DP, P, P, P, P, P, P, P, P, P, I, I, P, Z, P,
                                               P, I, P, P]),
             "decode_attn_contig": (I, [DP, P, P, P, P, P, P, P, P, I, I, P, Z, P, P]),
+            "decode_attn_contig_planned": (I, [DP, P, P, P, P, P, P, P, P, I, I, P, Z, P, P]),
             "paged_prefill_attn": (I, [DP, P, P, I, I, P, P, P, P, P, P, P, P]),
             "paged_kv_extend": (I, [DP, P, P, P, P, I, P, P, P, P, P, P, I, I, P, P]),
             "pkv_testing_set_handoff_wait_ns": (I, [ctypes.c_ulonglong]),
@@ -272,12 +273,15 @@ def paged_decode_step_advance(d: Dims, q, k_new, v_new, k_pool, v_pool, kv_indic
 
 def decode_attn_contig(d: Dims, q, k_cache, v_cache, seq_lens, num_splits: int, workspace,
                        out, cache_batch_idx=None, k_new=None, v_new=None, rope_cos_sin=None,
-                       rope_max_pos: int = 0, stream=None) -> None:
+                       rope_max_pos: int = 0, stream=None, planned: bool = False) -> None:
     """Decode over a contiguous cache [num_slots, cache_len, Hkv, D] (d.page_size =
     cache_len, d.num_pages = num_slots); row b reads slot cache_batch_idx[b]
-    (None: slot b).  With k_new / v_new it is the whole decode step."""
+    (None: slot b).  With k_new / v_new it is the whole decode step.
+    planned: decode_attn_contig_planned (the table and plan the step's first
+    call left in the workspace)."""
     ws_bytes = workspace.numel() * workspace.element_size()
-    _check("decode_attn_contig", lib().decode_attn_contig(
+    name = "decode_attn_contig_planned" if planned else "decode_attn_contig"
+    _check(name, getattr(lib(), name)(
         ctypes.byref(d), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
         _ptr(cache_batch_idx), _ptr(seq_lens), _ptr(rope_cos_sin), rope_max_pos, num_splits,
         _ptr(workspace), ws_bytes, _ptr(out), _stream(stream)))

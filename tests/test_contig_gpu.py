@@ -104,3 +104,42 @@ def test_contig_equals_paged_bitwise():
                           torch.from_numpy(lens).cuda(), S, ws, out_p)
     torch.cuda.synchronize()
     assert torch.equal(out_c.view(torch.int16), out_p.view(torch.int16))
+
+
+def test_contig_planned_layers_bitwise():
+    """A step's later layers: decode_attn_contig_planned reuses the table and
+    the plan the first call left in the workspace, launches no table kernel,
+    and gives the first call's bits, for the attention and the whole step."""
+    c = wl.contig(Hq=32, Hkv=8, D=128, cache_len=512, num_slots=7, seq_lens=[512, 33, 1, 260],
+                  idx=[6, 2, 0, 4], seed=9, fill_new_slot=True)
+    d = pkv.dims(c.B, c.Hq, c.Hkv, c.D, c.cache_len, c.num_slots, c.B, c.cache_len, c.scale)
+    S = pkv.plan(d)[0]
+    ws = pkv.alloc_workspace(d, S, "cuda")
+    kc, vc = _dev(c.k_cache), _dev(c.v_cache)
+    q, lens = _dev(c.q), torch.from_numpy(c.seq_lens).cuda()
+    idx = torch.from_numpy(c.idx).cuda()
+    outs = [torch.empty(c.B, c.Hq, c.D, dtype=torch.bfloat16, device="cuda") for _ in range(3)]
+    pkv.decode_attn_contig(d, q, kc, vc, lens, S, ws, outs[0], cache_batch_idx=idx)
+    for o in outs[1:]:
+        pkv.decode_attn_contig(d, q, kc, vc, lens, S, ws, o, cache_batch_idx=idx, planned=True)
+    torch.cuda.synchronize()
+    assert pkv.status_word(ws) == 0
+    for o in outs[1:]:
+        assert torch.equal(o.view(torch.int16), outs[0].view(torch.int16))
+    compare_out(outs[1], _oracle(c)[0])
+    # the whole step (the new token written at seq_len - 1 of its slot)
+    rope = torch.empty(c.cache_len, c.D // 2, 2, dtype=torch.float32, device="cuda")
+    pkv.rope_table(rope, c.cache_len, c.D, c.rope_base)
+    kn, vn = _dev(c.k_new), _dev(c.v_new)
+    kc2, vc2 = kc.clone(), vc.clone()
+    step_outs = []
+    for planned, (k_, v_) in ((False, (kc, vc)), (True, (kc2, vc2))):
+        o = torch.empty_like(outs[0])
+        pkv.decode_attn_contig(d, q, k_, v_, lens, S, ws, o, cache_batch_idx=idx, k_new=kn,
+                               v_new=vn, rope_cos_sin=rope, rope_max_pos=c.cache_len,
+                               planned=planned)
+        step_outs.append(o)
+    torch.cuda.synchronize()
+    assert torch.equal(step_outs[0].view(torch.int16), step_outs[1].view(torch.int16))
+    assert torch.equal(kc.view(torch.int16), kc2.view(torch.int16))
+    assert torch.equal(vc.view(torch.int16), vc2.view(torch.int16))
