@@ -6,6 +6,7 @@
 #include <cstddef>
 #include <cstdint>
 #include <mutex>
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -110,6 +111,17 @@ struct PrefillParams {
     int B, Hq, Hkv, n_rep, page_size, ps_shift, num_pages, num_indices, max_seq_len, total_q;
     int tq;                        // query tokens per block: 128 / n_rep
     float scale_log2;
+    // the pools as 3-D tiled tensors {D, Hkv, pages x page_size} with a box of
+    // {64, 1, tma_rows} and 128-byte swizzle (use_tma != 0; set by
+    // launch_prefill when the page size is a power of two >= 8)
+    CUtensorMap tmap_k;
+    CUtensorMap tmap_v;
+    int use_tma;
+    int tma_rows;                  // min(page_size, 128)
+    // q as {D, Hq, total_q} with a box of {64, n_rep, tq}: one query tile's
+    // rows (token-major, head-minor), 128-byte swizzled (q_tma != 0)
+    CUtensorMap tmap_q;
+    int q_tma;
 };
 
 // Persistent token-balanced decode (pkv_fused.cu).
