@@ -289,6 +289,41 @@ __device__ __forceinline__ void umma_ta(uint32_t tmem_d, uint32_t tmem_a, uint64
                  : "memory");
 }
 
+// max(a, b, c) in one instruction.
+__device__ __forceinline__ float fmax3(float a, float b, float c)
+{
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// Two floats as one packed f32x2 operand.
+__device__ __forceinline__ uint64_t f32x2(float lo, float hi)
+{
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+
+// (y0, y1) = (a0, a1) * b + c, one packed FMA (b, c: f32x2 operands).
+__device__ __forceinline__ void ffma2(float &y0, float &y1, float a0, float a1, uint64_t b,
+                                      uint64_t c)
+{
+    asm("{\n .reg .b64 a, r;\n mov.b64 a, {%2, %3};\n fma.rn.f32x2 r, a, %4, %5;\n"
+        " mov.b64 {%0, %1}, r;\n}"
+        : "=f"(y0), "=f"(y1)
+        : "f"(a0), "f"(a1), "l"(b), "l"(c));
+}
+
+// (a0, a1) += (b0, b1), one packed add.
+__device__ __forceinline__ void fadd2(float &a0, float &a1, float b0, float b1)
+{
+    asm("{\n .reg .b64 a, b, r;\n mov.b64 a, {%0, %1};\n mov.b64 b, {%2, %3};\n"
+        " add.rn.f32x2 r, a, b;\n mov.b64 {%0, %1}, r;\n}"
+        : "+f"(a0), "+f"(a1)
+        : "f"(b0), "f"(b1));
+}
+
 // 2^x on the special-function unit (the PTX approximate instruction; 0 for -inf).
 __device__ __forceinline__ float ex2_fast(float x)
 {
@@ -574,12 +609,17 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
             }
             for (int j = 0; j < n_kb && ok; ++j) {
                 const bool more = j + 1 < n_kb;
-                if (!wait_p(0, j) || !wait_copy(&v_full[j % VS], j / VS, v_generic(j)))
+                // the data of tile A's next products first (normally there
+                // long before), then its P: P V and the next S go out back to
+                // back, with one wait between the two tiles' runs
+                if (!wait_copy(&v_full[j % VS], j / VS, v_generic(j)))
+                    break;
+                if (more && !wait_copy(&k_full[(j + 1) % KS], (j + 1) / KS, k_generic))
+                    break;
+                if (!wait_p(0, j))
                     break;
                 issue_pv(0, j);
                 if (more) {
-                    if (!wait_copy(&k_full[(j + 1) % KS], (j + 1) / KS, k_generic))
-                        break;
                     issue_s(0, j + 1);
                     umma_commit(&s_full[0]);
                 } else {
@@ -643,16 +683,16 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
                     sb[i] = key0 + 64 + i > pos ? -INFINITY : sb[i];
                 }
             }
-            // the row max as a tree (8 independent chains)
+            // the row max: three-input max over 8 independent chains
             float mx8[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i)
                 mx8[i] = fmaxf(sa[i], sb[i]);
 #pragma unroll
             for (int i = 8; i < 64; ++i)
-                mx8[i & 7] = fmaxf(mx8[i & 7], fmaxf(sa[i], sb[i]));
-            const float mraw = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                                     fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+                mx8[i & 7] = fmax3(mx8[i & 7], sa[i], sb[i]);
+            const float mraw = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
+                                     fmaxf(mx8[6], mx8[7]));
             const float mx = mraw * sl2;
             // a new base only when the max grows by more than 2^8 (or first)
             const bool rebase = mx > m_run + 8.f;
@@ -663,27 +703,31 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
                 l_run *= alpha;
             }
             const float nbase = m_run == -INFINITY ? 0.f : -m_run;
+            const uint64_t scale2 = f32x2(sl2, sl2), base2 = f32x2(nbase, nbase);
             float ls[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i)
                 ls[i] = 0.f;
             // P over the first 64 columns of this S, in two halves (each
-            // half's S values are in registers already)
+            // half's S values are in registers already); the exponent's
+            // argument and l (from the fp32 terms) as packed pairs
             uint32_t pw[32];
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
-                const float e0 = ex2_fast(fmaf(sa[2 * i], sl2, nbase));
-                const float e1 = ex2_fast(fmaf(sa[2 * i + 1], sl2, nbase));
+                float y0, y1;
+                ffma2(y0, y1, sa[2 * i], sa[2 * i + 1], scale2, base2);
+                const float e0 = ex2_fast(y0), e1 = ex2_fast(y1);
                 pw[i] = pack_bf16x2(e0, e1);
-                ls[i & 7] += e0 + e1;                  // l from the fp32 terms
+                fadd2(ls[2 * (i & 3)], ls[2 * (i & 3) + 1], e0, e1);
             }
             tmem_st32w(t_s, pw);
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
-                const float e0 = ex2_fast(fmaf(sb[2 * i], sl2, nbase));
-                const float e1 = ex2_fast(fmaf(sb[2 * i + 1], sl2, nbase));
+                float y0, y1;
+                ffma2(y0, y1, sb[2 * i], sb[2 * i + 1], scale2, base2);
+                const float e0 = ex2_fast(y0), e1 = ex2_fast(y1);
                 pw[i] = pack_bf16x2(e0, e1);
-                ls[i & 7] += e0 + e1;
+                fadd2(ls[2 * (i & 3)], ls[2 * (i & 3) + 1], e0, e1);
             }
             tmem_st32w(t_s + 32, pw);
             l_run += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));

@@ -1,6 +1,6 @@
 """paged_prefill_attn on the GPU against the fp64 oracle's prefill: ragged
 query chunks (full prefills, extends, single tokens, idle rows), GQA ratios
-1..16, page sizes 1..32, head dims 64 and 128, several query and key tiles per
+1..16, page sizes 1..256, head dims 64 and 128, several query and key tiles per
 row.  The pools hold NaN in every unreferenced page and past every row's
 tokens.  Tolerance: max-abs 2e-2, mean-abs 2e-3."""
 
@@ -53,8 +53,12 @@ def test_prefill_shapes(Hq, Hkv, D):
     compare_out(out, _want(c))
 
 
-@pytest.mark.parametrize("ps,D", [(1, 64), (5, 64), (32, 64), (1, 128), (5, 128), (32, 128)])
+@pytest.mark.parametrize("ps,D", [(1, 64), (5, 64), (32, 64), (1, 128), (5, 128), (32, 128),
+                                  (8, 128), (64, 64), (256, 128)])
 def test_prefill_page_sizes(ps, D):
+    """Page sizes that are powers of two >= 8 are loaded by TMA (one box per
+    page, or 128-row boxes inside a 256-row page); the others (1, 5) by the
+    cp.async gather."""
     lens = [100, 7, 250]
     qls = [37, 7, 129]
     c = wl.prefill("pfp", B=3, Hq=16, Hkv=4, D=D, page_size=ps, seq_lens=lens, q_lens=qls,
@@ -66,9 +70,9 @@ def test_prefill_page_sizes(ps, D):
 
 @pytest.mark.parametrize("Hq,Hkv,D", [(16, 4, 64), (16, 4, 128), (8, 8, 128)])
 def test_prefill_many_tiles(Hq, Hkv, D):
-    """Chunks of several query tiles against several key tiles each (at
-    D = 128: pairs of tiles, an odd tile count leaving one tile of a pair
-    idle, and the three K/V stages reused many times)."""
+    """Chunks of several query tiles against several key blocks each: pairs
+    of tiles, an odd tile count leaving tile A of a pair idle, and the K/V
+    rings reused many times."""
     lens = [1000, 700, 513, 129]
     qls = [700, 700, 200, 129]
     c = wl.prefill("pfm", B=4, Hq=Hq, Hkv=Hkv, D=D, page_size=16, seq_lens=lens, q_lens=qls,
