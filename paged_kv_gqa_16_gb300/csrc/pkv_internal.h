@@ -122,6 +122,10 @@ struct PrefillParams {
     // rows (token-major, head-minor), 128-byte swizzled (q_tma != 0)
     CUtensorMap tmap_q;
     int q_tma;
+    // the units of work (set by launch_prefill): pairs of query tiles per
+    // chunk (from max_q_len) and pairs x B x Hkv
+    int pairs;
+    int n_units;
 };
 
 // Persistent token-balanced decode (pkv_fused.cu).
@@ -206,7 +210,7 @@ struct CombineParams {
 cudaError_t launch_append(const AppendParams &p, cudaStream_t stream);
 cudaError_t launch_extend(const AppendParams &p, cudaStream_t stream);
 cudaError_t launch_advance(const AdvanceParams &p, cudaStream_t stream);
-// grid: (ceil(max_q_len / tq), B * Hkv)
+// one persistent block per SM over the units (pairs of query tiles x B x Hkv)
 cudaError_t launch_prefill(const PrefillParams &p, int D, int max_q_len, cudaStream_t stream);
 // table[0..B] = 0..B (kv_indptr), table[B+1+b] = idx ? idx[b] : b (kv_indices)
 cudaError_t launch_contig_table(const int32_t *idx, int B, int32_t *table, cudaStream_t stream);

@@ -192,11 +192,6 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32
                  : "memory");
 }
 
-__device__ __forceinline__ void cp_async_commit()
-{
-    asm volatile("cp.async.commit_group;" ::: "memory");
-}
-
 __device__ __forceinline__ void cp_async_wait_all()
 {
     asm volatile("cp.async.wait_group 0;" ::: "memory");
@@ -233,13 +228,20 @@ struct PrefillCfg {
     static constexpr int kKeys = 128;                      // keys of one K/V block
     static constexpr int kKStages = D <= 64 ? 4 : 2;
     static constexpr int kVStages = D <= 64 ? 4 : 2;
-    static constexpr int kMmaWarp = 8;                     // tensor-memory owner, MMA issue
-    // warp 9: K loads, warp 10: V loads.  11 warps keep at most 3 on an SM
-    // sub-partition, so a thread may hold 168 registers (a softmax row of S
-    // is 128 of them); a 13th warp would cap it at 128.
-    static constexpr int kLoadThreads = 64;
-    static constexpr int kLoadTid0 = (kMmaWarp + 1) * 32;
-    static constexpr int kThreads = kLoadTid0 + kLoadThreads;
+    // warps 0-7: softmax of tiles A, B; warp 8: tensor-memory owner and MMA
+    // issue; warps 9, 10: K, V loads; warp 11: Q loads.  12 warps keep at
+    // most 3 on an SM sub-partition, so a thread may hold 168 registers (a
+    // softmax row of S is 128 of them); a 13th warp would cap it at 128.
+    static constexpr int kMmaWarp = 8;
+    static constexpr int kQWarp = 11;
+    static constexpr int kThreads = 12 * 32;
+    // per-thread registers after the start: softmax warpgroups / the rest;
+    // the block holds kThreads x kRegsLaunch, which must cover the split
+    static constexpr int kRegsLaunch = 168;
+    static constexpr int kRegsSoftmax = 192;
+    static constexpr int kRegsOther = 112;
+    static_assert(256 * kRegsSoftmax + 128 * kRegsOther <= kThreads * kRegsLaunch,
+                  "register split above the block's registers");
     // a tile or block of 128 rows: D / 64 regions of 128 rows x 128 bytes
     // (64 dims each), 128-byte swizzled
     static constexpr int kRegionBytes = 128 * 128;
@@ -249,8 +251,8 @@ struct PrefillCfg {
     static constexpr int kVOff = kKOff + kKStages * kKVBytes;
     static constexpr int kBarOff = kVOff + kVStages * kKVBytes;
     // k_full[KS], k_empty[KS], v_full[VS], v_empty[VS], s_full[2], p_full[2],
-    // o_full[2], drain, q_full
-    static constexpr int kNumBars = 2 * kKStages + 2 * kVStages + 8;
+    // o_full[2], o_empty[2], q_full[2], q_empty[2], drain
+    static constexpr int kNumBars = 2 * kKStages + 2 * kVStages + 13;
     static constexpr int kTmemSlot = kBarOff + kNumBars * 8;
     static constexpr int kAbortOff = kTmemSlot + 4;
     static constexpr int kSmemBytes = kAbortOff + 12;
@@ -332,6 +334,58 @@ __device__ __forceinline__ float ex2_fast(float x)
     return y;
 }
 
+// One unit of work: query tiles tB = n_tiles - 1 - 2 pair (the most keys
+// first) and tA = tB - 1 (-1: idle) of row b's chunk, with kv head g.
+struct PrefillUnit {
+    int b, g, q0, q_len, L, tA, tB, kv_end, n_kb, pg0;
+    bool table_ok;
+};
+
+// Unit u of the list, pair-major (u = pair x rows + b x Hkv + g, so every
+// row's largest pairs come first); false when it has no work: a pair past
+// its row's chunk, or a refused row.  flag: report refusals in the status.
+__device__ __forceinline__ bool prefill_unit(const PrefillParams &p, int u, PrefillUnit &w,
+                                             bool flag)
+{
+    const int rows = p.B * p.Hkv;
+    const int pair = u / rows, rh = u - pair * rows;
+    w.b = rh / p.Hkv;
+    w.g = rh - w.b * p.Hkv;
+    w.q0 = p.qo_indptr[w.b];
+    const int q1 = p.qo_indptr[w.b + 1];
+    w.L = p.seq_lens[w.b];
+    const int k0 = p.kv_indptr[w.b], k1 = p.kv_indptr[w.b + 1];
+    w.q_len = q1 - w.q0;
+    const bool row_ok = w.q_len >= 0 && w.q0 >= 0 && q1 <= p.total_q && w.L >= 0 &&
+                        w.L <= p.max_seq_len && w.q_len <= w.L;
+    const bool first = flag && pair == 0 && w.g == 0;  // one report per row
+    if (!row_ok) {
+        if (first)
+            tc_flag(p.status, kFlagBadLen);
+        return false;
+    }
+    const int n_tiles = (w.q_len + p.tq - 1) / p.tq;
+    if (first && (n_tiles + 1) / 2 > p.pairs)
+        tc_flag(p.status, kFlagBadLen);                // chunk longer than max_q_len
+    w.tB = n_tiles - 1 - 2 * pair;
+    if (w.tB < 0)
+        return false;
+    w.tA = w.tB - 1;
+    w.kv_end = w.L - w.q_len + min(w.q_len, (w.tB + 1) * p.tq);
+    w.n_kb = (w.kv_end + 127) / 128;
+    w.pg0 = k0;
+    const int npg = k1 - k0;
+    w.table_ok = k0 >= 0 && npg >= 0 && k1 <= p.num_indices &&
+                 (long long)npg * p.page_size >= (long long)w.L;
+    if (!w.table_ok && flag)
+        tc_flag(p.status, kFlagBadPage);
+    return true;
+}
+
+// A persistent block (one per SM) takes one unit per round of gridDim.x
+// units; every role walks the same list and keeps its ring and phase
+// counters across units, so one unit's epilogue overlaps the next unit's
+// loads and first products.
 template <int D>
 __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
     prefill_kernel(const __grid_constant__ PrefillParams p)
@@ -344,42 +398,22 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
     uint64_t *k_full = bars, *k_empty = k_full + KS;
     uint64_t *v_full = k_empty + KS, *v_empty = v_full + VS;
     uint64_t *s_full = v_empty + VS, *p_full = s_full + 2, *o_full = p_full + 2;
-    uint64_t *drain = o_full + 2, *q_full = drain + 1;
+    uint64_t *o_empty = o_full + 2, *q_full = o_empty + 2, *q_empty = q_full + 2;
+    uint64_t *drain = q_empty + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kTmemSlot);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kAbortOff);
     const uint32_t sbase = smem_addr(smem);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-
-    const int b = blockIdx.y / p.Hkv, g = blockIdx.y % p.Hkv;
     const int n_rep = p.n_rep, tq = p.tq;
-
-    grid_dependency_wait();
-    const int q0 = p.qo_indptr[b], q1 = p.qo_indptr[b + 1];
-    const int L = p.seq_lens[b];
-    const int q_len = q1 - q0;
-    const bool row_ok = q_len >= 0 && q0 >= 0 && q1 <= p.total_q && L >= 0 &&
-                        L <= p.max_seq_len && q_len <= L;
-    if (!row_ok) {
-        if (blockIdx.x == 0 && g == 0 && tid == 0)
-            tc_flag(p.status, kFlagBadLen);
-        return;
-    }
-    const int n_tiles = (q_len + tq - 1) / tq;
-    if ((n_tiles + 1) / 2 > (int)gridDim.x && blockIdx.x == 0 && g == 0 && tid == 0)
-        tc_flag(p.status, kFlagBadLen);                // chunk longer than max_q_len
-    // tiles B = n_tiles - 1 - 2x (the most keys first) and A = B - 1
-    const int tB = n_tiles - 1 - 2 * (int)blockIdx.x;
-    if (tB < 0)
-        return;
-    const int tA = tB - 1;                             // -1: tile A is idle
-    const int kv_end = L - q_len + min(q_len, (tB + 1) * tq);
-    const int n_kb = (kv_end + C::kKeys - 1) / C::kKeys;
-    const int pg0 = p.kv_indptr[b];
-    const int npg = p.kv_indptr[b + 1] - pg0;
-    const bool table_ok = pg0 >= 0 && npg >= 0 && p.kv_indptr[b + 1] <= p.num_indices &&
-                          (long long)npg * p.page_size >= (long long)L;
-    if (!table_ok && tid == 0)
-        tc_flag(p.status, kFlagBadPage);
+    const int rows_used = tq * n_rep;
+    const int n_units = p.n_units;
+    // round r's unit of this block: the rounds run the list alternately
+    // forwards and backwards over the blocks, so a block with a large unit
+    // in one round gets a small one in the next
+    auto unit_index = [&](int r) {
+        const int G = (int)gridDim.x, c = (int)blockIdx.x;
+        return r * G + ((r & 1) ? G - 1 - c : c);
+    };
 
     if (tid == 0) {
         for (int s = 0; s < KS; ++s) {
@@ -394,9 +428,11 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
             mbar_init(&s_full[x], 1);
             mbar_init(&p_full[x], C::kRows);
             mbar_init(&o_full[x], 1);
+            mbar_init(&o_empty[x], C::kRows);          // the tile's epilogue has read O
+            mbar_init(&q_full[x], 32);                 // the Q warp's lanes
+            mbar_init(&q_empty[x], 1);                 // the unit's last S has read Q
         }
         mbar_init(drain, 1);
-        mbar_init(q_full, 32);                         // the K warp's lanes
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -407,360 +443,426 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
-    const int rows_used = tq * n_rep;
+    grid_dependency_wait();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    auto fail = [&]() {
+        *abort_flag = 1;
+        tc_flag(p.status, kFlagTimeout);
+    };
 
-    if (tid >= C::kLoadTid0) {
-        // ====================== K/V loads ===================================
-        // warp 9 fills the K ring, warp 10 the V ring.  A slot holds a block's
-        // 128 keys as D / 64 regions of 128 rows x 128 bytes (64 dims of a
-        // key), 128-byte swizzled: 16-byte chunk c of row r at c ^ (r & 7).
-        const bool is_v = warp == C::kMmaWarp + 2;
-        const int ns = is_v ? VS : KS;
-        uint64_t *full = is_v ? v_full : k_full;
-        uint64_t *empty = is_v ? v_empty : k_empty;
-        const uint32_t ring = sbase + (is_v ? C::kVOff : C::kKOff);
-        const __nv_bfloat16 *pool = is_v ? p.v_pool : p.k_pool;
-        const CUtensorMap *tmap = is_v ? &p.tmap_v : &p.tmap_k;
-        // cp.async: one instruction copies chunks [4 cq, 4 cq + 4) of 8
-        // keys, lane = key (lane & 7), chunk 4 cq + (lane >> 3): each key's
-        // 64 bytes are two whole L2 sectors, and the swizzle spreads the 8
-        // rows' chunks over all banks
-        const int kl = lane & 7, cl = lane >> 3;
-        if (!is_v) {
-            // Q of both tiles (row m of tile x = token m / n_rep, head
-            // m % n_rep), swizzled like K; an idle tile A is not loaded (its
-            // rows are masked out whatever they hold)
-            if (p.q_tma) {
-                const uint32_t tile_bytes = (uint32_t)((D / 64) * rows_used * 128);
-                if (lane == 0)
-                    mbar_arrive_expect_tx(q_full, (tA >= 0 ? 2u : 1u) * tile_bytes);
-                else
-                    mbar_arrive(q_full);
-                __syncwarp();
-                if (lane < 2 * (D / 64)) {
-                    const int x = lane / (D / 64), hh = lane % (D / 64);
-                    const int t = x == 0 ? tA : tB;
-                    if (t >= 0)
-                        tma_load_3d(sbase + x * C::kQBytes + hh * C::kRegionBytes, &p.tmap_q,
-                                    64 * hh, g * n_rep, q0 + t * tq, q_full);
-                }
-            } else {
-                for (int e = lane; e < 2 * C::kRows * CH; e += 32) {
-                    const int x = e / (C::kRows * CH), ee = e % (C::kRows * CH);
-                    const int m = ee / CH, c = ee % CH;
-                    const int t = x == 0 ? tA : tB;
-                    const int tok = m / n_rep, hq = m - tok * n_rep;
-                    const bool live = t >= 0 && m < rows_used && tok < q_len - t * tq;
-                    const __nv_bfloat16 *src =
-                        live ? p.q + ((size_t)(q0 + t * tq + tok) * p.Hq + (size_t)g * n_rep + hq) *
-                                         D + c * 8
-                             : p.q;
-                    cp_async16(sbase + x * C::kQBytes + (c >> 3) * C::kRegionBytes + m * 128 +
-                                   (((c & 7) ^ (m & 7)) << 4),
-                               src, live ? 16u : 0u);
-                }
-                cp_async_arrive(q_full);
-            }
-        }
-        int issued = 0;
-        for (int j = 0; j < n_kb; ++j, ++issued) {
-            const int slot = j % ns;
-            if (j >= ns) {
-                if (!mbar_wait_bounded(&empty[slot], (uint32_t)(((j / ns) - 1) & 1))) {
-                    *abort_flag = 1;
-                    tc_flag(p.status, kFlagTimeout);
-                }
-                if (*abort_flag)
-                    break;
-            }
-            const uint32_t dst = ring + slot * C::kKVBytes;
-            const int key0 = j * C::kKeys;
-            const int nkeys = min(C::kKeys, kv_end - key0);
-            // K rows past kv_end are masked out of S whatever they hold, so a
-            // K block loads whole boxes; V rows past it meet P = 0 and must be
-            // finite, so a partial V block is copied with zero fill
-            if (p.use_tma && (!is_v || nkeys == C::kKeys)) {
-                const int R = p.tma_rows;
-                const int nbox = (nkeys + R - 1) / R;
-                if (lane == 0)
-                    mbar_arrive_expect_tx(&full[slot], (uint32_t)(nbox * (D / 64) * R * 128));
-                else
-                    mbar_arrive(&full[slot]);
-                __syncwarp();
-                for (int bx = lane; bx < nbox; bx += 32) {
-                    const int tok = key0 + bx * R;
-                    const int pi = tok >> p.ps_shift;
-                    int page = table_ok ? __ldg(p.kv_indices + pg0 + pi) : 0;
-                    if (page < 0 || page >= p.num_pages) {
-                        tc_flag(p.status, kFlagBadPage);
-                        page = 0;
+    // registers: warpgroup 2 (MMA issue, loads) gives up most of its share
+    // to the softmax warpgroups, whose row of S alone is 128 registers; each
+    // warpgroup changes its limit at one point for all its warps, then
+    // dispatches its warps' roles (the launcher checks that the block holds
+    // enough registers for the split)
+    if (warp >= C::kMmaWarp) {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::kRegsOther));
+        if (warp == C::kQWarp) {
+            // ====================== Q loads =====================================
+            // tile x's Q (row m = token m / n_rep, head m % n_rep), swizzled like
+            // K, once the previous unit's last S of that tile has read it; an
+            // idle tile A is not loaded (its rows are masked out whatever they
+            // hold)
+            int it = 0;
+            for (int r = 0; r * (int)gridDim.x < n_units && !*abort_flag; ++r) {
+                const int u = unit_index(r);
+                PrefillUnit w;
+                if (u >= n_units || !prefill_unit(p, u, w, lane == 0))
+                    continue;
+                for (int x = 0; x < 2 && !*abort_flag; ++x) {
+                    if (it > 0 && !mbar_wait_bounded(&q_empty[x], (uint32_t)((it - 1) & 1))) {
+                        if (lane == 0)
+                            fail();
+                        break;
                     }
-                    const int row = (page << p.ps_shift) + (tok - (pi << p.ps_shift));
-#pragma unroll
-                    for (int h = 0; h < D / 64; ++h)
-                        tma_load_3d(dst + h * C::kRegionBytes + bx * R * 128, tmap, 64 * h, g, row,
-                                    &full[slot]);
-                }
-            } else {
-                size_t offs[C::kKeys / 8];
-                unsigned live = 0u;
-#pragma unroll
-                for (int kg = 0; kg < C::kKeys / 8; ++kg) {
-                    const int tok = key0 + kg * 8 + kl;
-                    offs[kg] = 0;
-                    if (tok < kv_end) {
-                        const int pi = p.ps_shift >= 0 ? (tok >> p.ps_shift) : (tok / p.page_size);
-                        const int sl = tok - pi * p.page_size;
-                        int page = table_ok ? __ldg(p.kv_indices + pg0 + pi) : 0;
-                        if (page < 0 || page >= p.num_pages) {
-                            tc_flag(p.status, kFlagBadPage);
-                            page = 0;
+                    const int t = x == 0 ? w.tA : w.tB;
+                    const uint32_t dst = sbase + x * C::kQBytes;
+                    if (p.q_tma) {
+                        const uint32_t bytes = t >= 0 ? (uint32_t)((D / 64) * rows_used * 128) : 0u;
+                        if (lane == 0)
+                            mbar_arrive_expect_tx(&q_full[x], bytes);
+                        else
+                            mbar_arrive(&q_full[x]);
+                        __syncwarp();
+                        if (t >= 0 && lane < D / 64)
+                            tma_load_3d(dst + lane * C::kRegionBytes, &p.tmap_q, 64 * lane,
+                                        w.g * n_rep, w.q0 + t * tq, &q_full[x]);
+                    } else {
+                        for (int e = lane; e < C::kRows * CH; e += 32) {
+                            const int m = e / CH, c = e % CH;
+                            const int tok = m / n_rep, hq = m - tok * n_rep;
+                            const bool live = t >= 0 && m < rows_used && tok < w.q_len - t * tq;
+                            const __nv_bfloat16 *src =
+                                live ? p.q + ((size_t)(w.q0 + t * tq + tok) * p.Hq +
+                                              (size_t)w.g * n_rep + hq) * D + c * 8
+                                     : p.q;
+                            cp_async16(dst + (c >> 3) * C::kRegionBytes + m * 128 +
+                                           (((c & 7) ^ (m & 7)) << 4),
+                                       src, live ? 16u : 0u);
                         }
-                        offs[kg] = (((size_t)page * p.page_size + sl) * p.Hkv + g) * D;
-                        live |= 1u << kg;
+                        cp_async_arrive(&q_full[x]);
                     }
                 }
-#pragma unroll
-                for (int kg = 0; kg < C::kKeys / 8; ++kg) {
-                    const uint32_t row = dst + (kg * 8 + kl) * 128;
-#pragma unroll
-                    for (int cq = 0; cq < CH / 4; ++cq) {
-                        const int c = 4 * cq + cl;
-                        cp_async16(row + (c >> 3) * C::kRegionBytes + (((c & 7) ^ kl) << 4),
-                                   pool + offs[kg] + c * 8, ((live >> kg) & 1u) ? 16u : 0u);
+                ++it;
+            }
+            cp_async_wait_all();
+            // the block exits only after its copies land
+            if (it > 0)
+                for (int x = 0; x < 2; ++x)
+                    (void)mbar_wait_bounded(&q_full[x], (uint32_t)((it - 1) & 1));
+        } else if (warp == C::kMmaWarp + 1 || warp == C::kMmaWarp + 2) {
+            // ====================== K/V loads ===================================
+            // warp 9 fills the K ring, warp 10 the V ring.  A slot holds a block's
+            // 128 keys as D / 64 regions of 128 rows x 128 bytes (64 dims of a
+            // key), 128-byte swizzled: 16-byte chunk c of row r at c ^ (r & 7).
+            const bool is_v = warp == C::kMmaWarp + 2;
+            const int ns = is_v ? VS : KS;
+            uint64_t *full = is_v ? v_full : k_full;
+            uint64_t *empty = is_v ? v_empty : k_empty;
+            const uint32_t ring = sbase + (is_v ? C::kVOff : C::kKOff);
+            const __nv_bfloat16 *pool = is_v ? p.v_pool : p.k_pool;
+            const CUtensorMap *tmap = is_v ? &p.tmap_v : &p.tmap_k;
+            // cp.async: one instruction copies chunks [4 cq, 4 cq + 4) of 8
+            // keys, lane = key (lane & 7), chunk 4 cq + (lane >> 3): each key's
+            // 64 bytes are two whole L2 sectors, and the swizzle spreads the 8
+            // rows' chunks over all banks
+            const int kl = lane & 7, cl = lane >> 3;
+            int kb = 0;                                    // blocks issued, over all units
+            for (int r = 0; r * (int)gridDim.x < n_units && !*abort_flag; ++r) {
+                const int u = unit_index(r);
+                PrefillUnit w;
+                if (u >= n_units || !prefill_unit(p, u, w, false))
+                    continue;
+                for (int j = 0; j < w.n_kb; ++j) {
+                    const int slot = kb % ns;
+                    if (kb >= ns) {
+                        if (!mbar_wait_bounded(&empty[slot], (uint32_t)(((kb / ns) - 1) & 1)) &&
+                            lane == 0)
+                            fail();
+                        __syncwarp();
                     }
+                    if (*abort_flag)
+                        break;
+                    const uint32_t dst = ring + slot * C::kKVBytes;
+                    const int key0 = j * C::kKeys;
+                    const int nkeys = min(C::kKeys, w.kv_end - key0);
+                    // K rows past kv_end are masked out of S whatever they hold,
+                    // so a K block loads whole boxes; V rows past it meet P = 0 and
+                    // must be finite, so a partial V block is copied with zero fill
+                    if (p.use_tma && (!is_v || nkeys == C::kKeys)) {
+                        const int R = p.tma_rows;
+                        const int nbox = (nkeys + R - 1) / R;
+                        if (lane == 0)
+                            mbar_arrive_expect_tx(&full[slot],
+                                                  (uint32_t)(nbox * (D / 64) * R * 128));
+                        else
+                            mbar_arrive(&full[slot]);
+                        __syncwarp();
+                        for (int bx = lane; bx < nbox; bx += 32) {
+                            const int tok = key0 + bx * R;
+                            const int pi = tok >> p.ps_shift;
+                            int page = w.table_ok ? __ldg(p.kv_indices + w.pg0 + pi) : 0;
+                            if (page < 0 || page >= p.num_pages) {
+                                tc_flag(p.status, kFlagBadPage);
+                                page = 0;
+                            }
+                            const int row = (page << p.ps_shift) + (tok - (pi << p.ps_shift));
+    #pragma unroll
+                            for (int h = 0; h < D / 64; ++h)
+                                tma_load_3d(dst + h * C::kRegionBytes + bx * R * 128, tmap, 64 * h,
+                                            w.g, row, &full[slot]);
+                        }
+                    } else {
+                        size_t offs[C::kKeys / 8];
+                        unsigned live = 0u;
+    #pragma unroll
+                        for (int kg = 0; kg < C::kKeys / 8; ++kg) {
+                            const int tok = key0 + kg * 8 + kl;
+                            offs[kg] = 0;
+                            if (tok < w.kv_end) {
+                                const int pi =
+                                    p.ps_shift >= 0 ? (tok >> p.ps_shift) : (tok / p.page_size);
+                                const int sl = tok - pi * p.page_size;
+                                int page = w.table_ok ? __ldg(p.kv_indices + w.pg0 + pi) : 0;
+                                if (page < 0 || page >= p.num_pages) {
+                                    tc_flag(p.status, kFlagBadPage);
+                                    page = 0;
+                                }
+                                offs[kg] = (((size_t)page * p.page_size + sl) * p.Hkv + w.g) * D;
+                                live |= 1u << kg;
+                            }
+                        }
+    #pragma unroll
+                        for (int kg = 0; kg < C::kKeys / 8; ++kg) {
+                            const uint32_t row = dst + (kg * 8 + kl) * 128;
+    #pragma unroll
+                            for (int cq = 0; cq < CH / 4; ++cq) {
+                                const int c = 4 * cq + cl;
+                                cp_async16(row + (c >> 3) * C::kRegionBytes + (((c & 7) ^ kl) << 4),
+                                           pool + offs[kg] + c * 8, ((live >> kg) & 1u) ? 16u : 0u);
+                            }
+                        }
+                        cp_async_arrive(&full[slot]);
+                    }
+                    ++kb;
                 }
-                cp_async_arrive(&full[slot]);
             }
-        }
-        cp_async_wait_all();
-        // the block exits only after its copies land: after an abort the MMA
-        // thread may not have waited for the last slots issued
-        for (int j = max(0, issued - ns); j < issued; ++j)
-            (void)mbar_wait_bounded(&full[j % ns], (uint32_t)((j / ns) & 1));
-    } else if (warp == C::kMmaWarp) {
-        // ====================== tensor-core issue ===========================
-        constexpr uint32_t kIdescS = instr_desc(128, C::kKeys, 0);
-        constexpr uint32_t kIdescO = instr_desc(128, D, 1);
-        // Q and K: 128-byte swizzle, K-major: 8-row groups 1 KB apart (SBO),
-        // a 16-dim step 32 bytes into the row, the next 64 dims in the next
-        // region.  V: 128-byte swizzle, MN-major:
-        // 64-dim atoms one region apart (LBO), 8-key groups 1 KB apart (SBO).
-        const uint64_t dq = smem_desc_sw128(sbase, 16, 1024);
-        const uint64_t dk = smem_desc_sw128(sbase + C::kKOff, 16, 1024);
-        // (at D = 64 one atom spans N, so LBO is unused; 1 KB keeps every
-        // address inside the slot however it were read)
-        const uint64_t dv =
-            smem_desc_sw128(sbase + C::kVOff, D > 64 ? C::kRegionBytes : 1024, 1024);
-        if (lane == 0) {
-            bool ok = true;
-            // a stage the copies filled; where cp.async filled it, the
-            // generic-proxy writes (visible once the barrier completes) are
-            // ordered before the tensor cores' reads by a proxy fence
-            auto wait_copy = [&](uint64_t *bar, int use, bool generic) {
-                ok = ok && mbar_wait_bounded(bar, (uint32_t)(use & 1)) && !*abort_flag;
-                if (ok) {
-                    if (generic)
-                        fence_proxy_async_smem();
-                    tc_fence_after();
-                }
-                return ok;
-            };
-            const bool k_generic = !p.use_tma;
-            auto v_generic = [&](int j) {
-                return !p.use_tma || kv_end - j * C::kKeys < C::kKeys;
-            };
-            auto wait_p = [&](int x, int j) {
-                ok = ok && mbar_wait_bounded(&p_full[x], (uint32_t)(j & 1)) && !*abort_flag;
-                if (ok)
-                    tc_fence_after();
-                return ok;
-            };
-            auto issue_s = [&](int x, int j) {
-                const uint64_t dq_x = dq + (uint64_t)((x * C::kQBytes) >> 4);
-                // Q and K share the swizzled K-major form: step s is 32 bytes
-                // into region s / 4
-                const uint64_t dk_s = dk + (uint64_t)(((j % KS) * C::kKVBytes) >> 4);
-#pragma unroll
-                for (int s = 0; s < D / 16; ++s)
-                    umma(tmem + 128 * x,
-                         dq_x + (uint64_t)(((s >> 2) * C::kRegionBytes + (s & 3) * 32) >> 4),
-                         dk_s + (uint64_t)(((s >> 2) * C::kRegionBytes + (s & 3) * 32) >> 4),
-                         kIdescS, s > 0);
-            };
-            auto issue_pv = [&](int x, int j) {
-                const uint64_t dv_s = dv + (uint64_t)(((j % VS) * C::kKVBytes) >> 4);
-#pragma unroll
-                for (int s = 0; s < C::kKeys / 16; ++s)
-                    umma_ta(tmem + C::kOCol + D * x, tmem + 128 * x + 8 * s,
-                            dv_s + (uint64_t)((s * 16 * 128) >> 4), kIdescO,
-                            (j > 0 || s > 0) ? 1u : 0u);
-            };
-            if (wait_copy(q_full, 0, !p.q_tma) && wait_copy(&k_full[0], 0, k_generic)) {
-                issue_s(0, 0);
-                umma_commit(&s_full[0]);
-                issue_s(1, 0);
-                umma_commit(&s_full[1]);
-                umma_commit(&k_empty[0]);
-            }
-            for (int j = 0; j < n_kb && ok; ++j) {
-                const bool more = j + 1 < n_kb;
-                // the data of tile A's next products first (normally there
-                // long before), then its P: P V and the next S go out back to
-                // back, with one wait between the two tiles' runs
-                if (!wait_copy(&v_full[j % VS], j / VS, v_generic(j)))
-                    break;
-                if (more && !wait_copy(&k_full[(j + 1) % KS], (j + 1) / KS, k_generic))
-                    break;
-                if (!wait_p(0, j))
-                    break;
-                issue_pv(0, j);
-                if (more) {
-                    issue_s(0, j + 1);
+            cp_async_wait_all();
+            // the block exits only after its copies land: after an abort the MMA
+            // thread may not have waited for the last slots issued
+            for (int k = max(0, kb - ns); k < kb; ++k)
+                (void)mbar_wait_bounded(&full[k % ns], (uint32_t)((k / ns) & 1));
+        } else if (warp == C::kMmaWarp) {
+            // ====================== tensor-core issue ===========================
+            constexpr uint32_t kIdescS = instr_desc(128, C::kKeys, 0);
+            constexpr uint32_t kIdescO = instr_desc(128, D, 1);
+            // Q and K: 128-byte swizzle, K-major: 8-row groups 1 KB apart (SBO),
+            // a 16-dim step 32 bytes into the row, the next 64 dims in the next
+            // region.  V: 128-byte swizzle, MN-major: 64-dim atoms one region
+            // apart (LBO), 8-key groups 1 KB apart (SBO); at D = 64 one atom spans
+            // N, so LBO is unused (1 KB keeps every address inside the slot
+            // however it were read).
+            const uint64_t dq = smem_desc_sw128(sbase, 16, 1024);
+            const uint64_t dk = smem_desc_sw128(sbase + C::kKOff, 16, 1024);
+            const uint64_t dv =
+                smem_desc_sw128(sbase + C::kVOff, D > 64 ? C::kRegionBytes : 1024, 1024);
+            if (lane == 0) {
+                bool ok = true;
+                // a stage the copies filled; where cp.async filled it, the
+                // generic-proxy writes (visible once the barrier completes) are
+                // ordered before the tensor cores' reads by a proxy fence
+                auto wait_copy = [&](uint64_t *bar, int use, bool generic) {
+                    ok = ok && mbar_wait_bounded(bar, (uint32_t)(use & 1)) && !*abort_flag;
+                    if (ok) {
+                        if (generic)
+                            fence_proxy_async_smem();
+                        tc_fence_after();
+                    }
+                    return ok;
+                };
+                auto wait_plain = [&](uint64_t *bar, uint32_t parity) {
+                    ok = ok && mbar_wait_bounded(bar, parity) && !*abort_flag;
+                    if (ok)
+                        tc_fence_after();
+                    return ok;
+                };
+                const bool k_generic = !p.use_tma;
+                // Q and K share the swizzled K-major form: step s is 32 bytes into
+                // region s / 4
+                auto issue_s = [&](int x, int kslot) {
+                    const uint64_t dq_x = dq + (uint64_t)((x * C::kQBytes) >> 4);
+                    const uint64_t dk_s = dk + (uint64_t)((kslot * C::kKVBytes) >> 4);
+    #pragma unroll
+                    for (int s = 0; s < D / 16; ++s) {
+                        const uint64_t ks =
+                            (uint64_t)(((s >> 2) * C::kRegionBytes + (s & 3) * 32) >> 4);
+                        umma(tmem + 128 * x, dq_x + ks, dk_s + ks, kIdescS, s > 0);
+                    }
+                };
+                auto issue_pv = [&](int x, int vslot, bool first) {
+                    const uint64_t dv_s = dv + (uint64_t)((vslot * C::kKVBytes) >> 4);
+    #pragma unroll
+                    for (int s = 0; s < C::kKeys / 16; ++s)
+                        umma_ta(tmem + C::kOCol + D * x, tmem + 128 * x + 8 * s,
+                                dv_s + (uint64_t)((s * 16 * 128) >> 4), kIdescO,
+                                (!first || s > 0) ? 1u : 0u);
+                };
+                int kb = 0, it = 0;                        // blocks and units consumed
+                uint32_t pc[2] = {0u, 0u};                 // P hand-offs consumed per tile
+                for (int r = 0; r * (int)gridDim.x < n_units && ok; ++r) {
+                    const int u = unit_index(r);
+                    PrefillUnit w;
+                    if (u >= n_units || !prefill_unit(p, u, w, false))
+                        continue;
+                    const int n_kb = w.n_kb;
+                    if (!wait_copy(&q_full[0], it, !p.q_tma) ||
+                        !wait_copy(&q_full[1], it, !p.q_tma) ||
+                        !wait_copy(&k_full[kb % KS], kb / KS, k_generic))
+                        break;
+                    // S of block 0 (the tile's last S of the previous unit was
+                    // issued before its P V, so these columns are free in order)
+                    issue_s(0, kb % KS);
                     umma_commit(&s_full[0]);
-                } else {
-                    umma_commit(&o_full[0]);
-                }
-                if (!wait_p(1, j))
-                    break;
-                issue_pv(1, j);
-                umma_commit(&v_empty[j % VS]);
-                if (more) {
-                    issue_s(1, j + 1);
+                    if (n_kb == 1)
+                        umma_commit(&q_empty[0]);
+                    issue_s(1, kb % KS);
                     umma_commit(&s_full[1]);
-                    umma_commit(&k_empty[(j + 1) % KS]);
-                } else {
-                    umma_commit(&o_full[1]);
+                    if (n_kb == 1)
+                        umma_commit(&q_empty[1]);
+                    umma_commit(&k_empty[kb % KS]);
+                    for (int j = 0; j < n_kb && ok; ++j) {
+                        const int kj = kb + j;
+                        const bool more = j + 1 < n_kb;
+                        // the data of tile A's next products first (normally there
+                        // long before), then its P: P V and the next S go out back
+                        // to back, with one wait between the two tiles' runs
+                        const bool v_gen = !p.use_tma || w.kv_end - j * C::kKeys < C::kKeys;
+                        if (!wait_copy(&v_full[kj % VS], kj / VS, v_gen))
+                            break;
+                        if (more && !wait_copy(&k_full[(kj + 1) % KS], (kj + 1) / KS, k_generic))
+                            break;
+                        for (int x = 0; x < 2; ++x) {
+                            if (!wait_plain(&p_full[x], pc[x] & 1u))
+                                break;
+                            ++pc[x];
+                            // the unit's first P V overwrites O: the previous
+                            // unit's epilogue must have read it
+                            if (j == 0 && it > 0 &&
+                                !wait_plain(&o_empty[x], (uint32_t)((it - 1) & 1)))
+                                break;
+                            issue_pv(x, kj % VS, j == 0);
+                            if (x == 1)
+                                umma_commit(&v_empty[kj % VS]);
+                            if (more) {
+                                issue_s(x, (kj + 1) % KS);
+                                umma_commit(&s_full[x]);
+                                if (j + 2 == n_kb)
+                                    umma_commit(&q_empty[x]);
+                                if (x == 1)
+                                    umma_commit(&k_empty[(kj + 1) % KS]);
+                            } else {
+                                umma_commit(&o_full[x]);
+                            }
+                        }
+                    }
+                    kb += n_kb;
+                    ++it;
                 }
+                if (!ok)
+                    fail();
             }
-            if (!ok) {
-                *abort_flag = 1;
-                tc_flag(p.status, kFlagTimeout);
-            }
+            __syncwarp();
         }
-        __syncwarp();
     } else {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::kRegsSoftmax));
         // ====================== softmax of tile x, row m ====================
         const int x = warp >> 2;
         const int m = tid & (C::kRows - 1);
-        const int t = x == 0 ? tA : tB;
         const int tok_m = m / n_rep;
-        const int ntok = t >= 0 ? min(tq, q_len - t * tq) : 0;
-        const int pos_first = L - q_len + (t >= 0 ? t * tq : 0);
-        const int pos = (t >= 0 && m < rows_used && tok_m < ntok) ? pos_first + tok_m : -1;
         const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
         const uint32_t t_s = tmem + 128 * x + lane_off;
         const uint32_t t_o = tmem + C::kOCol + D * x + lane_off;
         const float sl2 = p.scale_log2;
-        float m_run = -INFINITY, l_run = 0.f;
         bool ok = true;
         auto timed_out = [&]() {
             ok = false;
-            if (lane == 0) {
-                *abort_flag = 1;
-                tc_flag(p.status, kFlagTimeout);
-            }
+            if (lane == 0)
+                fail();
         };
-        for (int j = 0; j < n_kb; ++j) {
-            ok = mbar_wait_bounded(&s_full[x], (uint32_t)(j & 1)) && !*abort_flag;
+        uint32_t sc = 0u;                              // S hand-offs consumed
+        int it = 0;
+        for (int r = 0; r * (int)gridDim.x < n_units && ok; ++r) {
+            const int u = unit_index(r);
+            PrefillUnit w;
+            if (u >= n_units || !prefill_unit(p, u, w, false))
+                continue;
+            const int t = x == 0 ? w.tA : w.tB;
+            const int ntok = t >= 0 ? min(tq, w.q_len - t * tq) : 0;
+            const int pos_first = w.L - w.q_len + (t >= 0 ? t * tq : 0);
+            const int pos = (t >= 0 && m < rows_used && tok_m < ntok) ? pos_first + tok_m : -1;
+            float m_run = -INFINITY, l_run = 0.f;
+            for (int j = 0; j < w.n_kb; ++j) {
+                ok = mbar_wait_bounded(&s_full[x], sc & 1u) && !*abort_flag;
+                ++sc;
+                if (!__all_sync(kAllTc, ok)) {
+                    timed_out();
+                    break;
+                }
+                tc_fence_after();
+                float sa[64], sb[64];
+                tmem_ld64(t_s, sa);
+                tmem_ld64(t_s + 64, sb);
+                const int key0 = j * C::kKeys;
+                if (key0 + C::kKeys - 1 > pos_first) {
+#pragma unroll
+                    for (int i = 0; i < 64; ++i) {
+                        sa[i] = key0 + i > pos ? -INFINITY : sa[i];
+                        sb[i] = key0 + 64 + i > pos ? -INFINITY : sb[i];
+                    }
+                }
+                // the row max: three-input max over 8 independent chains
+                float mx8[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    mx8[i] = fmaxf(sa[i], sb[i]);
+#pragma unroll
+                for (int i = 8; i < 64; ++i)
+                    mx8[i & 7] = fmax3(mx8[i & 7], sa[i], sb[i]);
+                const float mraw = fmax3(fmax3(mx8[0], mx8[1], mx8[2]),
+                                         fmax3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
+                const float mx = mraw * sl2;
+                // a new base only when the max grows by more than 2^8 (or first)
+                const bool rebase = mx > m_run + 8.f;
+                float alpha = 1.f;
+                if (rebase) {
+                    alpha = ex2_fast(m_run - mx);      // 0 while m_run is -inf
+                    m_run = mx;
+                    l_run *= alpha;
+                }
+                const float nbase = m_run == -INFINITY ? 0.f : -m_run;
+                const uint64_t scale2 = f32x2(sl2, sl2), base2 = f32x2(nbase, nbase);
+                float ls[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    ls[i] = 0.f;
+                // P over the first 64 columns of this S, in two halves (each
+                // half's S values are in registers already); the exponent's
+                // argument and l (from the fp32 terms) as packed pairs
+                uint32_t pw[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    float y0, y1;
+                    ffma2(y0, y1, sa[2 * i], sa[2 * i + 1], scale2, base2);
+                    const float e0 = ex2_fast(y0), e1 = ex2_fast(y1);
+                    pw[i] = pack_bf16x2(e0, e1);
+                    fadd2(ls[2 * (i & 3)], ls[2 * (i & 3) + 1], e0, e1);
+                }
+                tmem_st32w(t_s, pw);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    float y0, y1;
+                    ffma2(y0, y1, sb[2 * i], sb[2 * i + 1], scale2, base2);
+                    const float e0 = ex2_fast(y0), e1 = ex2_fast(y1);
+                    pw[i] = pack_bf16x2(e0, e1);
+                    fadd2(ls[2 * (i & 3)], ls[2 * (i & 3) + 1], e0, e1);
+                }
+                tmem_st32w(t_s + 32, pw);
+                l_run += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+                // O is quiescent here: the commit behind this S covered the
+                // last P V, and the next one waits for this P
+                if (__any_sync(kAllTc, rebase && j > 0)) {
+#pragma unroll 1
+                    for (int c0 = 0; c0 < D; c0 += 32) {
+                        float v[32];
+                        tmem_ld32(t_o + c0, v);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            v[i] *= alpha;
+                        tmem_st32(t_o + c0, v);
+                    }
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(&p_full[x]);
+            }
+            if (!ok)
+                break;
+            // ---- normalise and store this tile's rows; then O is free ------
+            ok = mbar_wait_bounded(&o_full[x], (uint32_t)(it & 1)) && !*abort_flag;
             if (!__all_sync(kAllTc, ok)) {
                 timed_out();
                 break;
             }
             tc_fence_after();
-            float sa[64], sb[64];
-            tmem_ld64(t_s, sa);
-            tmem_ld64(t_s + 64, sb);
-            const int key0 = j * C::kKeys;
-            if (key0 + C::kKeys - 1 > pos_first) {
-#pragma unroll
-                for (int i = 0; i < 64; ++i) {
-                    sa[i] = key0 + i > pos ? -INFINITY : sa[i];
-                    sb[i] = key0 + 64 + i > pos ? -INFINITY : sb[i];
-                }
-            }
-            // the row max: three-input max over 8 independent chains
-            float mx8[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-                mx8[i] = fmaxf(sa[i], sb[i]);
-#pragma unroll
-            for (int i = 8; i < 64; ++i)
-                mx8[i & 7] = fmax3(mx8[i & 7], sa[i], sb[i]);
-            const float mraw = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
-                                     fmaxf(mx8[6], mx8[7]));
-            const float mx = mraw * sl2;
-            // a new base only when the max grows by more than 2^8 (or first)
-            const bool rebase = mx > m_run + 8.f;
-            float alpha = 1.f;
-            if (rebase) {
-                alpha = ex2_fast(m_run - mx);          // 0 while m_run is -inf
-                m_run = mx;
-                l_run *= alpha;
-            }
-            const float nbase = m_run == -INFINITY ? 0.f : -m_run;
-            const uint64_t scale2 = f32x2(sl2, sl2), base2 = f32x2(nbase, nbase);
-            float ls[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-                ls[i] = 0.f;
-            // P over the first 64 columns of this S, in two halves (each
-            // half's S values are in registers already); the exponent's
-            // argument and l (from the fp32 terms) as packed pairs
-            uint32_t pw[32];
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                float y0, y1;
-                ffma2(y0, y1, sa[2 * i], sa[2 * i + 1], scale2, base2);
-                const float e0 = ex2_fast(y0), e1 = ex2_fast(y1);
-                pw[i] = pack_bf16x2(e0, e1);
-                fadd2(ls[2 * (i & 3)], ls[2 * (i & 3) + 1], e0, e1);
-            }
-            tmem_st32w(t_s, pw);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                float y0, y1;
-                ffma2(y0, y1, sb[2 * i], sb[2 * i + 1], scale2, base2);
-                const float e0 = ex2_fast(y0), e1 = ex2_fast(y1);
-                pw[i] = pack_bf16x2(e0, e1);
-                fadd2(ls[2 * (i & 3)], ls[2 * (i & 3) + 1], e0, e1);
-            }
-            tmem_st32w(t_s + 32, pw);
-            l_run += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
-            // O is quiescent here: the commit behind this S covered the last
-            // P V, and the next one waits for this P
-            if (__any_sync(kAllTc, rebase && j > 0)) {
-#pragma unroll 1
-                for (int c0 = 0; c0 < D; c0 += 32) {
-                    float v[32];
-                    tmem_ld32(t_o + c0, v);
-#pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        v[i] *= alpha;
-                    tmem_st32(t_o + c0, v);
-                }
-            }
-            tmem_st_wait();
-            tc_fence_before();
-            mbar_arrive(&p_full[x]);
-        }
-        // ---- normalise and store this row ----------------------------------
-        if (ok) {
-            ok = mbar_wait_bounded(&o_full[x], 0u) && !*abort_flag;
-            if (!__all_sync(kAllTc, ok))
-                timed_out();
-        }
-        tc_fence_after();
-        if (__all_sync(kAllTc, ok)) {
             const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
             __nv_bfloat16 *orow = nullptr;
             if (pos >= 0) {
                 const int hh = m - tok_m * n_rep;
-                orow = p.out + ((size_t)(q0 + t * tq + tok_m) * p.Hq + (size_t)g * n_rep + hh) * D;
+                orow = p.out +
+                       ((size_t)(w.q0 + t * tq + tok_m) * p.Hq + (size_t)w.g * n_rep + hh) * D;
             }
 #pragma unroll 1
             for (int c0 = 0; c0 < D; c0 += 32) {
@@ -776,6 +878,9 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
                                        pack_bf16x2(v[8 * h + 6] * inv, v[8 * h + 7] * inv));
                 }
             }
+            tc_fence_before();
+            mbar_arrive(&o_empty[x]);
+            ++it;
         }
     }
     // every role is done; on an abort the MMA warp waits (bounded) for the
@@ -796,25 +901,35 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
 }
 
 template <int D>
-cudaError_t launch_prefill_d(const PrefillParams &p, int max_q_len, cudaStream_t stream)
+cudaError_t launch_prefill_d(const PrefillParams &p, cudaStream_t stream)
 {
     using C = PrefillCfg<D>;
     static DeviceOnce attrs;
     const cudaError_t attr_err = attrs.run([] {
+        // the kernel moves registers between its warpgroups (setmaxnreg):
+        // a launch with fewer registers per thread than the split assumes
+        // would leave the softmax warps waiting for registers forever
+        cudaFuncAttributes fa;
+        cudaError_t e = cudaFuncGetAttributes(&fa, prefill_kernel<D>);
+        if (e != cudaSuccess)
+            return e;
+        if (fa.numRegs < C::kRegsLaunch)
+            return cudaErrorInvalidConfiguration;
         return cudaFuncSetAttribute(prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     C::kSmemBytes);
     });
     if (attr_err != cudaSuccess)
         return attr_err;
-    const long long tiles = ((long long)max_q_len + p.tq - 1) / p.tq;
-    const long long pairs = (tiles + 1) / 2;
-    const long long rows = (long long)p.B * p.Hkv;
-    if (pairs <= 0 || rows <= 0)
-        return cudaSuccess;
-    if (pairs > 0x7fffffffLL || rows > 65535)
-        return cudaErrorInvalidValue;
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess)
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess)
+        return e;
+    // one persistent block per SM (each holds all of an SM's tensor memory)
+    const int grid = p.n_units < sms ? p.n_units : sms;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)pairs, (unsigned)rows);
+    cfg.gridDim = dim3((unsigned)grid);
     cfg.blockDim = dim3(C::kThreads);
     cfg.dynamicSmemBytes = C::kSmemBytes;
     cfg.stream = stream;
@@ -823,7 +938,7 @@ cudaError_t launch_prefill_d(const PrefillParams &p, int max_q_len, cudaStream_t
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, prefill_kernel<D>, p);
+    e = cudaLaunchKernelEx(&cfg, prefill_kernel<D>, p);
     if (e != cudaSuccess)
         return e;
     return cudaGetLastError();
@@ -893,8 +1008,18 @@ cudaError_t launch_prefill(const PrefillParams &p_in, int D, int max_q_len, cuda
         p.q_tma = 1;
     // the paired, warp-specialised layout is 27-31% faster at D = 128; at
     // D = 64 the single-tile blocks, three to an SM, are 16% faster
-    return D == 64 ? launch_prefill_d<64>(p, max_q_len, stream)
-                   : launch_prefill_d<128>(p, max_q_len, stream);
+    // the units: pairs of query tiles (max_q_len bounds a chunk's tiles) x
+    // rows x kv heads
+    const long long tiles = ((long long)max_q_len + p.tq - 1) / p.tq;
+    const long long pairs = (tiles + 1) / 2;
+    const long long units = pairs * p.B * p.Hkv;
+    if (units <= 0)
+        return cudaSuccess;
+    if (units > 0x7fffffffLL)
+        return cudaErrorInvalidValue;
+    p.pairs = (int)pairs;
+    p.n_units = (int)units;
+    return D == 64 ? launch_prefill_d<64>(p, stream) : launch_prefill_d<128>(p, stream);
 }
 
 } // namespace pkv
