@@ -228,20 +228,16 @@ struct PrefillCfg {
     static constexpr int kKeys = 128;                      // keys of one K/V block
     static constexpr int kKStages = D <= 64 ? 4 : 2;
     static constexpr int kVStages = D <= 64 ? 4 : 2;
-    // warps 0-7: softmax of tiles A, B; warp 8: tensor-memory owner and MMA
-    // issue; warps 9, 10: K, V loads; warp 11: Q loads.  12 warps keep at
-    // most 3 on an SM sub-partition, so a thread may hold 168 registers (a
-    // softmax row of S is 128 of them); a 13th warp would cap it at 128.
-    static constexpr int kMmaWarp = 8;
-    static constexpr int kQWarp = 11;
-    static constexpr int kThreads = 12 * 32;
-    // per-thread registers after the start: softmax warpgroups / the rest;
-    // the block holds kThreads x kRegsLaunch, which must cover the split
-    static constexpr int kRegsLaunch = 168;
-    static constexpr int kRegsSoftmax = 192;
-    static constexpr int kRegsOther = 112;
-    static_assert(256 * kRegsSoftmax + 128 * kRegsOther <= kThreads * kRegsLaunch,
-                  "register split above the block's registers");
+    // warps 0-7: softmax of tile A, 8-15: tile B (a row's two threads, in
+    // warpgroups 2x and 2x + 1, take 64 of a block's 128 keys each); warp
+    // 16: tensor-memory owner and tile A's products; warp 17: K loads; warp
+    // 18: V and Q loads; warp 19: tile B's products
+    static constexpr int kSoftmaxWarps = 16;
+    static constexpr int kMmaWarp = kSoftmaxWarps;
+    static constexpr int kMmaWarpB = 19;               // tile B's products
+    static constexpr int kThreads = 20 * 32;
+    // 20 warps leave a thread 96 registers (65,536 / 640, in steps of 8):
+    // enough for a half row of S (64) in the softmax and for the other roles
     // a tile or block of 128 rows: D / 64 regions of 128 rows x 128 bytes
     // (64 dims each), 128-byte swizzled
     static constexpr int kRegionBytes = 128 * 128;
@@ -251,9 +247,13 @@ struct PrefillCfg {
     static constexpr int kVOff = kKOff + kKStages * kKVBytes;
     static constexpr int kBarOff = kVOff + kVStages * kKVBytes;
     // k_full[KS], k_empty[KS], v_full[VS], v_empty[VS], s_full[2], p_full[2],
-    // o_full[2], o_empty[2], q_full[2], q_empty[2], drain
-    static constexpr int kNumBars = 2 * kKStages + 2 * kVStages + 13;
-    static constexpr int kTmemSlot = kBarOff + kNumBars * 8;
+    // o_full[2], o_empty[2], q_full[2], q_empty[2], drain, xch_bar[2], turn[2]
+    static constexpr int kNumBars = 2 * kKStages + 2 * kVStages + 17;
+    // a row's two halves exchange their max (and at the end their l) here:
+    // [tile][block parity][half][row] floats
+    static constexpr int kXchOff = kBarOff + kNumBars * 8;
+    static constexpr int kXchBytes = 2 * 2 * 2 * kRows * 4;
+    static constexpr int kTmemSlot = kXchOff + kXchBytes;
     static constexpr int kAbortOff = kTmemSlot + 4;
     static constexpr int kSmemBytes = kAbortOff + 12;
     static_assert(kSmemBytes <= 232448, "shared memory per block");
@@ -399,7 +399,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
     uint64_t *v_full = k_empty + KS, *v_empty = v_full + VS;
     uint64_t *s_full = v_empty + VS, *p_full = s_full + 2, *o_full = p_full + 2;
     uint64_t *o_empty = o_full + 2, *q_full = o_empty + 2, *q_empty = q_full + 2;
-    uint64_t *drain = q_empty + 2;
+    uint64_t *drain = q_empty + 2, *xch_bar = drain + 1, *turn = xch_bar + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kTmemSlot);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kAbortOff);
     const uint32_t sbase = smem_addr(smem);
@@ -418,21 +418,25 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
     if (tid == 0) {
         for (int s = 0; s < KS; ++s) {
             mbar_init(&k_full[s], 32);                 // the K warp's lanes
-            mbar_init(&k_empty[s], 1);
+            mbar_init(&k_empty[s], 2);                 // both tiles' S
         }
         for (int s = 0; s < VS; ++s) {
             mbar_init(&v_full[s], 32);                 // the V warp's lanes
-            mbar_init(&v_empty[s], 1);
+            mbar_init(&v_empty[s], 2);                 // both tiles' P V
         }
         for (int x = 0; x < 2; ++x) {
             mbar_init(&s_full[x], 1);
-            mbar_init(&p_full[x], C::kRows);
+            mbar_init(&p_full[x], 8);                  // the tile's 8 softmax warps
             mbar_init(&o_full[x], 1);
-            mbar_init(&o_empty[x], C::kRows);          // the tile's epilogue has read O
-            mbar_init(&q_full[x], 32);                 // the Q warp's lanes
+            mbar_init(&o_empty[x], 8);                 // the tile's epilogue has read O
+            mbar_init(&xch_bar[x], 8);                 // a block's halves exchanged
+            mbar_init(&q_full[x], 32);                 // the V warp's lanes
             mbar_init(&q_empty[x], 1);                 // the unit's last S has read Q
         }
-        mbar_init(drain, 1);
+        mbar_init(drain, 2);                           // both issuing threads
+        mbar_init(&turn[0], 1);
+        mbar_init(&turn[1], 1);
+        mbar_arrive(&turn[0]);                         // tile A's run goes first
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -453,27 +457,39 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
         tc_flag(p.status, kFlagTimeout);
     };
 
-    // registers: warpgroup 2 (MMA issue, loads) gives up most of its share
-    // to the softmax warpgroups, whose row of S alone is 128 registers; each
-    // warpgroup changes its limit at one point for all its warps, then
-    // dispatches its warps' roles (the launcher checks that the block holds
-    // enough registers for the split)
     if (warp >= C::kMmaWarp) {
-        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::kRegsOther));
-        if (warp == C::kQWarp) {
-            // ====================== Q loads =====================================
-            // tile x's Q (row m = token m / n_rep, head m % n_rep), swizzled like
-            // K, once the previous unit's last S of that tile has read it; an
-            // idle tile A is not loaded (its rows are masked out whatever they
-            // hold)
-            int it = 0;
+        if (warp == C::kMmaWarp + 1 || warp == C::kMmaWarp + 2) {
+            // ====================== K/V loads ===================================
+            // warp 17 fills the K ring, warp 18 the V ring.  A slot holds a block's
+            // 128 keys as D / 64 regions of 128 rows x 128 bytes (64 dims of a
+            // key), 128-byte swizzled: 16-byte chunk c of row r at c ^ (r & 7).
+            const bool is_v = warp == C::kMmaWarp + 2;
+            const int ns = is_v ? VS : KS;
+            uint64_t *full = is_v ? v_full : k_full;
+            uint64_t *empty = is_v ? v_empty : k_empty;
+            const uint32_t ring = sbase + (is_v ? C::kVOff : C::kKOff);
+            const __nv_bfloat16 *pool = is_v ? p.v_pool : p.k_pool;
+            const CUtensorMap *tmap = is_v ? &p.tmap_v : &p.tmap_k;
+            // cp.async: one instruction copies chunks [4 cq, 4 cq + 4) of 8
+            // keys, lane = key (lane & 7), chunk 4 cq + (lane >> 3): each key's
+            // 64 bytes are two whole L2 sectors, and the swizzle spreads the 8
+            // rows' chunks over all banks
+            const int kl = lane & 7, cl = lane >> 3;
+            int kb = 0;                                    // blocks issued, over all units
+            int qit = 0;                                   // units whose Q the V warp loaded
             for (int r = 0; r * (int)gridDim.x < n_units && !*abort_flag; ++r) {
                 const int u = unit_index(r);
                 PrefillUnit w;
-                if (u >= n_units || !prefill_unit(p, u, w, lane == 0))
+                if (u >= n_units || !prefill_unit(p, u, w, is_v && lane == 0))
                     continue;
-                for (int x = 0; x < 2 && !*abort_flag; ++x) {
-                    if (it > 0 && !mbar_wait_bounded(&q_empty[x], (uint32_t)((it - 1) & 1))) {
+                // the V warp also loads the unit's Q (row m = token m / n_rep,
+                // head m % n_rep, swizzled like K), each tile's once the previous
+                // unit's last S of that tile has read it, before the unit's V;
+                // an idle tile A is not loaded (its rows are masked out whatever
+                // they hold)
+                for (int x = 0; x < 2 && is_v && !*abort_flag; ++x) {
+                    if (qit > 0 &&
+                        !mbar_wait_bounded(&q_empty[x], (uint32_t)((qit - 1) & 1))) {
                         if (lane == 0)
                             fail();
                         break;
@@ -506,36 +522,8 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
                         cp_async_arrive(&q_full[x]);
                     }
                 }
-                ++it;
-            }
-            cp_async_wait_all();
-            // the block exits only after its copies land
-            if (it > 0)
-                for (int x = 0; x < 2; ++x)
-                    (void)mbar_wait_bounded(&q_full[x], (uint32_t)((it - 1) & 1));
-        } else if (warp == C::kMmaWarp + 1 || warp == C::kMmaWarp + 2) {
-            // ====================== K/V loads ===================================
-            // warp 9 fills the K ring, warp 10 the V ring.  A slot holds a block's
-            // 128 keys as D / 64 regions of 128 rows x 128 bytes (64 dims of a
-            // key), 128-byte swizzled: 16-byte chunk c of row r at c ^ (r & 7).
-            const bool is_v = warp == C::kMmaWarp + 2;
-            const int ns = is_v ? VS : KS;
-            uint64_t *full = is_v ? v_full : k_full;
-            uint64_t *empty = is_v ? v_empty : k_empty;
-            const uint32_t ring = sbase + (is_v ? C::kVOff : C::kKOff);
-            const __nv_bfloat16 *pool = is_v ? p.v_pool : p.k_pool;
-            const CUtensorMap *tmap = is_v ? &p.tmap_v : &p.tmap_k;
-            // cp.async: one instruction copies chunks [4 cq, 4 cq + 4) of 8
-            // keys, lane = key (lane & 7), chunk 4 cq + (lane >> 3): each key's
-            // 64 bytes are two whole L2 sectors, and the swizzle spreads the 8
-            // rows' chunks over all banks
-            const int kl = lane & 7, cl = lane >> 3;
-            int kb = 0;                                    // blocks issued, over all units
-            for (int r = 0; r * (int)gridDim.x < n_units && !*abort_flag; ++r) {
-                const int u = unit_index(r);
-                PrefillUnit w;
-                if (u >= n_units || !prefill_unit(p, u, w, false))
-                    continue;
+                if (is_v)
+                    ++qit;
                 for (int j = 0; j < w.n_kb; ++j) {
                     const int slot = kb % ns;
                     if (kb >= ns) {
@@ -570,7 +558,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
                                 page = 0;
                             }
                             const int row = (page << p.ps_shift) + (tok - (pi << p.ps_shift));
-    #pragma unroll
+#pragma unroll
                             for (int h = 0; h < D / 64; ++h)
                                 tma_load_3d(dst + h * C::kRegionBytes + bx * R * 128, tmap, 64 * h,
                                             w.g, row, &full[slot]);
@@ -578,7 +566,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
                     } else {
                         size_t offs[C::kKeys / 8];
                         unsigned live = 0u;
-    #pragma unroll
+#pragma unroll
                         for (int kg = 0; kg < C::kKeys / 8; ++kg) {
                             const int tok = key0 + kg * 8 + kl;
                             offs[kg] = 0;
@@ -595,10 +583,10 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
                                 live |= 1u << kg;
                             }
                         }
-    #pragma unroll
+#pragma unroll
                         for (int kg = 0; kg < C::kKeys / 8; ++kg) {
                             const uint32_t row = dst + (kg * 8 + kl) * 128;
-    #pragma unroll
+#pragma unroll
                             for (int cq = 0; cq < CH / 4; ++cq) {
                                 const int c = 4 * cq + cl;
                                 cp_async16(row + (c >> 3) * C::kRegionBytes + (((c & 7) ^ kl) << 4),
@@ -615,8 +603,18 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
             // thread may not have waited for the last slots issued
             for (int k = max(0, kb - ns); k < kb; ++k)
                 (void)mbar_wait_bounded(&full[k % ns], (uint32_t)((k / ns) & 1));
-        } else if (warp == C::kMmaWarp) {
+            if (is_v && qit > 0)
+                for (int x = 0; x < 2; ++x)
+                    (void)mbar_wait_bounded(&q_full[x], (uint32_t)((qit - 1) & 1));
+        } else {
             // ====================== tensor-core issue ===========================
+            // warp 16 issues tile A's products, warp 19 tile B's.  They take
+            // turns, one run each (the S of a unit's first block; then P V of
+            // block j with S of block j + 1), in the order one thread would
+            // issue them.  Each thread waits for its next run's data and P, and
+            // makes its commits, while the other's run goes out, so the tensor
+            // cores always have a run queued.
+            const int x = warp == C::kMmaWarpB ? 1 : 0;
             constexpr uint32_t kIdescS = instr_desc(128, C::kKeys, 0);
             constexpr uint32_t kIdescO = instr_desc(128, D, 1);
             // Q and K: 128-byte swizzle, K-major: 8-row groups 1 KB apart (SBO),
@@ -631,101 +629,101 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
                 smem_desc_sw128(sbase + C::kVOff, D > 64 ? C::kRegionBytes : 1024, 1024);
             if (lane == 0) {
                 bool ok = true;
-                // a stage the copies filled; where cp.async filled it, the
-                // generic-proxy writes (visible once the barrier completes) are
-                // ordered before the tensor cores' reads by a proxy fence
-                auto wait_copy = [&](uint64_t *bar, int use, bool generic) {
-                    ok = ok && mbar_wait_bounded(bar, (uint32_t)(use & 1)) && !*abort_flag;
-                    if (ok) {
-                        if (generic)
-                            fence_proxy_async_smem();
-                        tc_fence_after();
-                    }
-                    return ok;
-                };
-                auto wait_plain = [&](uint64_t *bar, uint32_t parity) {
+                auto wait_only = [&](uint64_t *bar, uint32_t parity) {
                     ok = ok && mbar_wait_bounded(bar, parity) && !*abort_flag;
-                    if (ok)
-                        tc_fence_after();
                     return ok;
                 };
                 const bool k_generic = !p.use_tma;
                 // Q and K share the swizzled K-major form: step s is 32 bytes into
                 // region s / 4
-                auto issue_s = [&](int x, int kslot) {
-                    const uint64_t dq_x = dq + (uint64_t)((x * C::kQBytes) >> 4);
+                const uint64_t dq_x = dq + (uint64_t)((x * C::kQBytes) >> 4);
+                auto issue_s = [&](int kslot) {
                     const uint64_t dk_s = dk + (uint64_t)((kslot * C::kKVBytes) >> 4);
-    #pragma unroll
+#pragma unroll
                     for (int s = 0; s < D / 16; ++s) {
                         const uint64_t ks =
                             (uint64_t)(((s >> 2) * C::kRegionBytes + (s & 3) * 32) >> 4);
                         umma(tmem + 128 * x, dq_x + ks, dk_s + ks, kIdescS, s > 0);
                     }
                 };
-                auto issue_pv = [&](int x, int vslot, bool first) {
+                auto issue_pv = [&](int vslot, bool first) {
                     const uint64_t dv_s = dv + (uint64_t)((vslot * C::kKVBytes) >> 4);
-    #pragma unroll
+#pragma unroll
                     for (int s = 0; s < C::kKeys / 16; ++s)
                         umma_ta(tmem + C::kOCol + D * x, tmem + 128 * x + 8 * s,
                                 dv_s + (uint64_t)((s * 16 * 128) >> 4), kIdescO,
                                 (!first || s > 0) ? 1u : 0u);
                 };
+                // the turn: this tile's run of products goes out once the other
+                // tile's run has been issued, then passes the turn back
+                uint32_t turns = 0u;
+                auto take_turn = [&]() {
+                    ok = ok && mbar_wait_bounded(&turn[x], turns & 1u) && !*abort_flag;
+                    ++turns;
+                    if (ok)
+                        tc_fence_after();
+                    return ok;
+                };
+                auto pass_turn = [&]() { mbar_arrive(&turn[x ^ 1]); };
                 int kb = 0, it = 0;                        // blocks and units consumed
-                uint32_t pc[2] = {0u, 0u};                 // P hand-offs consumed per tile
+                uint32_t pc = 0u;                          // P hand-offs consumed
                 for (int r = 0; r * (int)gridDim.x < n_units && ok; ++r) {
                     const int u = unit_index(r);
                     PrefillUnit w;
                     if (u >= n_units || !prefill_unit(p, u, w, false))
                         continue;
                     const int n_kb = w.n_kb;
-                    if (!wait_copy(&q_full[0], it, !p.q_tma) ||
-                        !wait_copy(&q_full[1], it, !p.q_tma) ||
-                        !wait_copy(&k_full[kb % KS], kb / KS, k_generic))
+                    if (!wait_only(&q_full[x], (uint32_t)(it & 1)) ||
+                        !wait_only(&k_full[kb % KS], (uint32_t)((kb / KS) & 1)))
                         break;
+                    // stages filled by cp.async: their generic-proxy writes
+                    // before the tensor cores' reads
+                    if (!p.q_tma || k_generic)
+                        fence_proxy_async_smem();
                     // S of block 0 (the tile's last S of the previous unit was
                     // issued before its P V, so these columns are free in order)
-                    issue_s(0, kb % KS);
-                    umma_commit(&s_full[0]);
+                    if (!take_turn())
+                        break;
+                    issue_s(kb % KS);
+                    pass_turn();
+                    umma_commit(&s_full[x]);
                     if (n_kb == 1)
-                        umma_commit(&q_empty[0]);
-                    issue_s(1, kb % KS);
-                    umma_commit(&s_full[1]);
-                    if (n_kb == 1)
-                        umma_commit(&q_empty[1]);
+                        umma_commit(&q_empty[x]);
                     umma_commit(&k_empty[kb % KS]);
                     for (int j = 0; j < n_kb && ok; ++j) {
                         const int kj = kb + j;
                         const bool more = j + 1 < n_kb;
-                        // the data of tile A's next products first (normally there
-                        // long before), then its P: P V and the next S go out back
-                        // to back, with one wait between the two tiles' runs
+                        // this run's data and P, waited for while the other
+                        // tile's run is issued
                         const bool v_gen = !p.use_tma || w.kv_end - j * C::kKeys < C::kKeys;
-                        if (!wait_copy(&v_full[kj % VS], kj / VS, v_gen))
+                        if (!wait_only(&v_full[kj % VS], (uint32_t)((kj / VS) & 1)))
                             break;
-                        if (more && !wait_copy(&k_full[(kj + 1) % KS], (kj + 1) / KS, k_generic))
+                        if (more &&
+                            !wait_only(&k_full[(kj + 1) % KS], (uint32_t)(((kj + 1) / KS) & 1)))
                             break;
-                        for (int x = 0; x < 2; ++x) {
-                            if (!wait_plain(&p_full[x], pc[x] & 1u))
-                                break;
-                            ++pc[x];
-                            // the unit's first P V overwrites O: the previous
-                            // unit's epilogue must have read it
-                            if (j == 0 && it > 0 &&
-                                !wait_plain(&o_empty[x], (uint32_t)((it - 1) & 1)))
-                                break;
-                            issue_pv(x, kj % VS, j == 0);
-                            if (x == 1)
-                                umma_commit(&v_empty[kj % VS]);
-                            if (more) {
-                                issue_s(x, (kj + 1) % KS);
-                                umma_commit(&s_full[x]);
-                                if (j + 2 == n_kb)
-                                    umma_commit(&q_empty[x]);
-                                if (x == 1)
-                                    umma_commit(&k_empty[(kj + 1) % KS]);
-                            } else {
-                                umma_commit(&o_full[x]);
-                            }
+                        if (v_gen || (more && k_generic))
+                            fence_proxy_async_smem();
+                        if (!wait_only(&p_full[x], pc & 1u))
+                            break;
+                        ++pc;
+                        // the unit's first P V overwrites O: the previous unit's
+                        // epilogue must have read it
+                        if (j == 0 && it > 0 && !wait_only(&o_empty[x], (uint32_t)((it - 1) & 1)))
+                            break;
+                        if (!take_turn())
+                            break;
+                        issue_pv(kj % VS, j == 0);
+                        if (more)
+                            issue_s((kj + 1) % KS);
+                        pass_turn();
+                        umma_commit(&v_empty[kj % VS]);
+                        if (more) {
+                            umma_commit(&s_full[x]);
+                            if (j + 2 == n_kb)
+                                umma_commit(&q_empty[x]);
+                            umma_commit(&k_empty[(kj + 1) % KS]);
+                        } else {
+                            umma_commit(&o_full[x]);
                         }
                     }
                     kb += n_kb;
@@ -733,18 +731,29 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
                 }
                 if (!ok)
                     fail();
+                // tracks every product this thread issued: tensor memory is
+                // released only after both threads' products are done
+                umma_commit(drain);
             }
             __syncwarp();
         }
     } else {
-        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::kRegsSoftmax));
-        // ====================== softmax of tile x, row m ====================
-        const int x = warp >> 2;
+        // ====================== softmax of tile x, row m, half h ============
+        // warps 0-7 run tile A, 8-15 tile B; warpgroup h of a tile takes keys
+        // [64 h, 64 h + 64) of each 128-key block, so a row's two threads
+        // (one tensor-memory lane) each handle half of its keys.  Per block
+        // they exchange their halves' max through shared memory (buffers
+        // alternating with the block, one mbarrier phase per block and tile),
+        // keep their own part of l, and each rescales and stores its D / 2
+        // columns of O.  The hand-offs to the MMA thread take one arrival per
+        // warp.
+        const int x = warp >> 3, h = (warp >> 2) & 1;
         const int m = tid & (C::kRows - 1);
         const int tok_m = m / n_rep;
         const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
         const uint32_t t_s = tmem + 128 * x + lane_off;
-        const uint32_t t_o = tmem + C::kOCol + D * x + lane_off;
+        const uint32_t t_o = tmem + C::kOCol + D * x + (D / 2) * h + lane_off;
+        float *xch = reinterpret_cast<float *>(smem + C::kXchOff) + x * 2 * 2 * C::kRows;
         const float sl2 = p.scale_log2;
         bool ok = true;
         auto timed_out = [&]() {
@@ -753,6 +762,23 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
                 fail();
         };
         uint32_t sc = 0u;                              // S hand-offs consumed
+        uint32_t xc = 0u;                              // exchanges done
+        // publish v as this half's value of exchange xc and return the other
+        // half's (false: the wait timed out).  The tensor-memory fences order
+        // each half's reads of S before the other half's P overwrites them.
+        auto exchange = [&](float v, float &other) {
+            float *buf = xch + (xc & 1u) * 2 * C::kRows;
+            buf[h * C::kRows + m] = v;
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&xch_bar[x]);
+            const bool got = mbar_wait_bounded(&xch_bar[x], xc & 1u) && !*abort_flag;
+            tc_fence_after();
+            ++xc;
+            other = buf[(h ^ 1) * C::kRows + m];
+            return got;
+        };
         int it = 0;
         for (int r = 0; r * (int)gridDim.x < n_units && ok; ++r) {
             const int u = unit_index(r);
@@ -772,28 +798,35 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
                     break;
                 }
                 tc_fence_after();
-                float sa[64], sb[64];
-                tmem_ld64(t_s, sa);
-                tmem_ld64(t_s + 64, sb);
-                const int key0 = j * C::kKeys;
-                if (key0 + C::kKeys - 1 > pos_first) {
+                float sv[64];
+                tmem_ld64(t_s + 64 * h, sv);
+                const int key0 = j * C::kKeys + 64 * h;
+                if (key0 + 63 > pos_first) {
 #pragma unroll
-                    for (int i = 0; i < 64; ++i) {
-                        sa[i] = key0 + i > pos ? -INFINITY : sa[i];
-                        sb[i] = key0 + 64 + i > pos ? -INFINITY : sb[i];
-                    }
+                    for (int i = 0; i < 64; ++i)
+                        sv[i] = key0 + i > pos ? -INFINITY : sv[i];
                 }
-                // the row max: three-input max over 8 independent chains
+                // this half's max: three-input max over 8 independent chains
                 float mx8[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i)
-                    mx8[i] = fmaxf(sa[i], sb[i]);
+                    mx8[i] = fmaxf(sv[i], sv[8 + i]);
 #pragma unroll
-                for (int i = 8; i < 64; ++i)
-                    mx8[i & 7] = fmax3(mx8[i & 7], sa[i], sb[i]);
-                const float mraw = fmax3(fmax3(mx8[0], mx8[1], mx8[2]),
-                                         fmax3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
-                const float mx = mraw * sl2;
+                for (int k = 1; k < 4; ++k)
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        mx8[i] = fmax3(mx8[i], sv[16 * k + i], sv[16 * k + 8 + i]);
+                const float mh = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
+                                       fmaxf(mx8[6], mx8[7]));
+                // the row's max from both halves (both threads of the row
+                // then take the same decisions below)
+                float mo;
+                ok = exchange(mh, mo);
+                if (!__all_sync(kAllTc, ok)) {
+                    timed_out();
+                    break;
+                }
+                const float mx = fmaxf(mh, mo) * sl2;
                 // a new base only when the max grows by more than 2^8 (or first)
                 const bool rebase = mx > m_run + 8.f;
                 float alpha = 1.f;
@@ -808,34 +841,26 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
 #pragma unroll
                 for (int i = 0; i < 8; ++i)
                     ls[i] = 0.f;
-                // P over the first 64 columns of this S, in two halves (each
-                // half's S values are in registers already); the exponent's
-                // argument and l (from the fp32 terms) as packed pairs
+                // P of this half's keys over columns [32 h, 32 h + 32) of S
+                // (the other half's S there was read before the exchange);
+                // the exponent's argument and l (from the fp32 terms) as
+                // packed pairs
                 uint32_t pw[32];
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
                     float y0, y1;
-                    ffma2(y0, y1, sa[2 * i], sa[2 * i + 1], scale2, base2);
+                    ffma2(y0, y1, sv[2 * i], sv[2 * i + 1], scale2, base2);
                     const float e0 = ex2_fast(y0), e1 = ex2_fast(y1);
                     pw[i] = pack_bf16x2(e0, e1);
                     fadd2(ls[2 * (i & 3)], ls[2 * (i & 3) + 1], e0, e1);
                 }
-                tmem_st32w(t_s, pw);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    float y0, y1;
-                    ffma2(y0, y1, sb[2 * i], sb[2 * i + 1], scale2, base2);
-                    const float e0 = ex2_fast(y0), e1 = ex2_fast(y1);
-                    pw[i] = pack_bf16x2(e0, e1);
-                    fadd2(ls[2 * (i & 3)], ls[2 * (i & 3) + 1], e0, e1);
-                }
-                tmem_st32w(t_s + 32, pw);
+                tmem_st32w(t_s + 32 * h, pw);
                 l_run += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
                 // O is quiescent here: the commit behind this S covered the
                 // last P V, and the next one waits for this P
                 if (__any_sync(kAllTc, rebase && j > 0)) {
 #pragma unroll 1
-                    for (int c0 = 0; c0 < D; c0 += 32) {
+                    for (int c0 = 0; c0 < D / 2; c0 += 32) {
                         float v[32];
                         tmem_ld32(t_o + c0, v);
 #pragma unroll
@@ -846,40 +871,48 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
                 }
                 tmem_st_wait();
                 tc_fence_before();
-                mbar_arrive(&p_full[x]);
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&p_full[x]);
             }
             if (!ok)
                 break;
             // ---- normalise and store this tile's rows; then O is free ------
-            ok = mbar_wait_bounded(&o_full[x], (uint32_t)(it & 1)) && !*abort_flag;
+            float lo;
+            ok = exchange(l_run, lo);
+            ok = ok && mbar_wait_bounded(&o_full[x], (uint32_t)(it & 1)) && !*abort_flag;
             if (!__all_sync(kAllTc, ok)) {
                 timed_out();
                 break;
             }
             tc_fence_after();
-            const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+            const float l_row = l_run + lo;
+            const float inv = l_row > 0.f ? 1.f / l_row : 0.f;
             __nv_bfloat16 *orow = nullptr;
             if (pos >= 0) {
                 const int hh = m - tok_m * n_rep;
                 orow = p.out +
-                       ((size_t)(w.q0 + t * tq + tok_m) * p.Hq + (size_t)w.g * n_rep + hh) * D;
+                       ((size_t)(w.q0 + t * tq + tok_m) * p.Hq + (size_t)w.g * n_rep + hh) * D +
+                       (D / 2) * h;
             }
 #pragma unroll 1
-            for (int c0 = 0; c0 < D; c0 += 32) {
+            for (int c0 = 0; c0 < D / 2; c0 += 32) {
                 float v[32];
                 tmem_ld32(t_o + c0, v);
                 if (orow != nullptr) {
 #pragma unroll
-                    for (int h = 0; h < 4; ++h)
-                        *reinterpret_cast<uint4 *>(orow + c0 + 8 * h) =
-                            make_uint4(pack_bf16x2(v[8 * h] * inv, v[8 * h + 1] * inv),
-                                       pack_bf16x2(v[8 * h + 2] * inv, v[8 * h + 3] * inv),
-                                       pack_bf16x2(v[8 * h + 4] * inv, v[8 * h + 5] * inv),
-                                       pack_bf16x2(v[8 * h + 6] * inv, v[8 * h + 7] * inv));
+                    for (int q = 0; q < 4; ++q)
+                        *reinterpret_cast<uint4 *>(orow + c0 + 8 * q) =
+                            make_uint4(pack_bf16x2(v[8 * q] * inv, v[8 * q + 1] * inv),
+                                       pack_bf16x2(v[8 * q + 2] * inv, v[8 * q + 3] * inv),
+                                       pack_bf16x2(v[8 * q + 4] * inv, v[8 * q + 5] * inv),
+                                       pack_bf16x2(v[8 * q + 6] * inv, v[8 * q + 7] * inv));
                 }
             }
             tc_fence_before();
-            mbar_arrive(&o_empty[x]);
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&o_empty[x]);
             ++it;
         }
     }
@@ -888,10 +921,8 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
     tc_fence_before();
     __syncthreads();
     if (warp == C::kMmaWarp) {
-        if (*abort_flag && lane == 0) {
-            umma_commit(drain);
+        if (lane == 0)
             (void)mbar_wait_bounded(drain, 0u);
-        }
         __syncwarp();
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
@@ -906,15 +937,6 @@ cudaError_t launch_prefill_d(const PrefillParams &p, cudaStream_t stream)
     using C = PrefillCfg<D>;
     static DeviceOnce attrs;
     const cudaError_t attr_err = attrs.run([] {
-        // the kernel moves registers between its warpgroups (setmaxnreg):
-        // a launch with fewer registers per thread than the split assumes
-        // would leave the softmax warps waiting for registers forever
-        cudaFuncAttributes fa;
-        cudaError_t e = cudaFuncGetAttributes(&fa, prefill_kernel<D>);
-        if (e != cudaSuccess)
-            return e;
-        if (fa.numRegs < C::kRegsLaunch)
-            return cudaErrorInvalidConfiguration;
         return cudaFuncSetAttribute(prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     C::kSmemBytes);
     });
