@@ -126,6 +126,7 @@ struct PrefillParams {
     // chunk (from max_q_len) and pairs x B x Hkv
     int pairs;
     int n_units;
+    int group_rows;                // rows per group of the unit list
 };
 
 // Persistent token-balanced decode (pkv_fused.cu).

@@ -341,14 +341,25 @@ struct PrefillUnit {
     bool table_ok;
 };
 
-// Unit u of the list, pair-major (u = pair x rows + b x Hkv + g, so every
-// row's largest pairs come first); false when it has no work: a pair past
-// its row's chunk, or a refused row.  flag: report refusals in the status.
+// Unit u of the list: rows (b x Hkv + g) in groups of p.group_rows, the
+// groups one after another and each group pair-major (its rows' largest
+// pairs first); false when the unit has no work: a pair past its row's
+// chunk, or a refused row.  flag: report refusals in the status.
 __device__ __forceinline__ bool prefill_unit(const PrefillParams &p, int u, PrefillUnit &w,
                                              bool flag)
 {
     const int rows = p.B * p.Hkv;
-    const int pair = u / rows, rh = u - pair * rows;
+    int pair, rh;
+    if (p.group_rows >= rows) {                        // one group: pair-major
+        pair = u / rows;
+        rh = u - pair * rows;
+    } else {
+        const int per_group = p.group_rows * p.pairs;
+        const int grp = u / per_group, ul = u - grp * per_group;
+        const int g_rows = min(p.group_rows, rows - grp * p.group_rows);
+        pair = ul / g_rows;
+        rh = grp * p.group_rows + (ul - pair * g_rows);
+    }
     w.b = rh / p.Hkv;
     w.g = rh - w.b * p.Hkv;
     w.q0 = p.qo_indptr[w.b];
@@ -1006,6 +1017,9 @@ bool encode_map(CUtensorMap *map, const void *base, int D, int mid, long long ro
 
 } // namespace
 
+// Chunks of at most this many pairs of query tiles get a grouped unit list.
+constexpr int kGroupMaxPairs = 4;
+
 cudaError_t launch_prefill(const PrefillParams &p_in, int D, int max_q_len, cudaStream_t stream)
 {
     // K/V pages by TMA when a page is a power of two >= 8 rows (whole 8-row
@@ -1041,6 +1055,23 @@ cudaError_t launch_prefill(const PrefillParams &p_in, int D, int max_q_len, cuda
         return cudaErrorInvalidValue;
     p.pairs = (int)pairs;
     p.n_units = (int)units;
+    // rows per group of the unit list.  A chunk of many pairs (a long causal
+    // prefill) has units from one to hundreds of key blocks: one group,
+    // pair-major, keeps each round's units of about one size.  A chunk of a
+    // few pairs (an extend, a short prompt) has units of about one size
+    // anyway: groups of about one round of units (SMs / pairs rows) keep the
+    // rows in flight few enough to share L2.
+    const long long row_heads = (long long)p.B * p.Hkv;
+    long long grp = row_heads;
+    if (pairs <= kGroupMaxPairs) {
+        int dev = 0, sms = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            sms = 1;
+        grp = (long long)sms / pairs;
+        grp = grp < 1 ? 1 : (grp > row_heads ? row_heads : grp);
+    }
+    p.group_rows = (int)grp;
     return D == 64 ? launch_prefill_d<64>(p, stream) : launch_prefill_d<128>(p, stream);
 }
 
