@@ -11,21 +11,26 @@
 // h / n_rep gathered through the page table.
 //
 // A query tile is 128 query rows = 128 / n_rep tokens x the kv head's n_rep
-// query heads (token-major) of one (row, kv head); the thread that owns query
-// row t of a tile owns lane t of tensor memory.  A block takes two
-// consecutive tiles (A, B) and streams their keys in blocks of 128:
+// query heads (token-major) of one (row, kv head); query row t of a tile
+// lives in lane t of tensor memory.  A unit is two consecutive tiles (A, B)
+// whose keys stream in blocks of 128; one persistent block per SM walks a
+// list of units:
 //   - Q, K and V are loaded by TMA (3-D tiled tensor maps, 128-byte swizzle):
 //     Q as one box per tile and 64 dims, K and V as one box per page and 64
 //     dims; page sizes that are not a power of two >= 8 are gathered with
 //     16-byte cp.async into the same swizzled layout;
 //   - S = Q K^T (M 128, N 128, K = D in steps of 16) goes to tensor memory;
-//   - each row's thread reads its row of S, masks keys past its position,
-//     updates its own fp32 online softmax (log2 domain, the scale folded into
-//     one FFMA per exponent, l from the fp32 terms), rescales its row of O in
-//     tensor memory only when its max has grown by more than 2^8, and writes
-//     P (bf16) back over its S;
+//   - a row's two threads each read half of its S (64 keys), mask keys past
+//     its position, exchange their halves' max, update the fp32 online
+//     softmax (log2 domain, the scale folded into one FFMA per exponent, l
+//     from the fp32 terms), rescale their halves of O in tensor memory only
+//     when the max has grown by more than 2^8, and write P (bf16) back over
+//     S;
 //   - O += P V (M 128, N = D, K = 128) takes P from tensor memory and V
-//     (MN-major) from shared memory.
+//     (MN-major) from shared memory;
+//   - tile A's products are issued by one thread and tile B's by another,
+//     taking turns one run at a time, so each makes its waits and commits
+//     while the other's run goes out.
 // Every mbarrier wait is time-bounded; tensor memory is allocated at the
 // start and released on every path.
 #include <cmath>
