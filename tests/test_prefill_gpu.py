@@ -20,7 +20,7 @@ def _bits(t):
     return t.contiguous().view(torch.int16).numpy().view(np.uint16)
 
 
-def _run(c, status=None):
+def _run(c, status=None, max_q_len=None):
     w = c.w
     t = w.to_device("cuda")
     P = t["k_pool"].shape[0]
@@ -28,8 +28,9 @@ def _run(c, status=None):
                  w.max_seq_len, w.scale)
     out = torch.full((c.total_q, w.Hq, w.D), float("nan"), dtype=torch.bfloat16, device="cuda")
     st = torch.zeros(1, dtype=torch.int32, device="cuda") if status is None else status
+    kw = {} if max_q_len is None else {"max_q_len": max_q_len}
     pkv.paged_prefill_attn(d, c.q.cuda(), c.qo_indptr.cuda(), t["k_pool"], t["v_pool"],
-                           t["kv_indices"], t["kv_indptr"], t["seq_lens"], out, status=st)
+                           t["kv_indices"], t["kv_indptr"], t["seq_lens"], out, status=st, **kw)
     torch.cuda.synchronize()
     return out, int(st.item()) & 0xFFFFFFFF, (d, t)
 
@@ -81,6 +82,23 @@ def test_prefill_many_tiles(Hq, Hkv, D):
     assert st == 0
     compare_out(out, _want(c))
 
+
+
+@pytest.mark.parametrize("Hq,Hkv,D", [(8, 4, 64), (16, 4, 128)])
+def test_prefill_grouped_rows(Hq, Hkv, D):
+    """Chunks of at most 4 pairs of query tiles over more row-heads than one
+    group: the unit list takes rows in groups of about one round of units,
+    the last group partial (160 row-heads, groups of 152 / pairs rows)."""
+    rng = np.random.default_rng(11 + D)
+    B = 40
+    qls = [int(x) for x in rng.integers(1, 129, size=B)]
+    lens = [q + int(x) for q, x in zip(qls, rng.integers(0, 200, size=B))]
+    c = wl.prefill("pfgr", B=B, Hq=Hq, Hkv=Hkv, D=D, page_size=16, seq_lens=lens, q_lens=qls,
+                   seed=31 + D)
+    # the chunks' true bound: at most 2 pairs of tiles, so the list is grouped
+    out, st, _ = _run(c, max_q_len=max(qls))
+    assert st == 0
+    compare_out(out, _want(c))
 
 def test_prefill_graph_replay_bitwise():
     lens, qls = [300, 90, 33], [120, 90, 1]
