@@ -378,11 +378,13 @@ def run_reference(args):
 
 
 def prefill_leg(pkv, wl, dev, stream, flush_l2, rank, names, reps=20):
-    """paged_prefill_attn on each named shape: one call per graph replay, the
-    L2 flushed before each, median of `reps`; tensor roofline against the
-    measured dense bf16 peak (burst: each call runs alone)."""
+    """paged_prefill_attn_ws (the prefill with its key-split workspace) on each
+    named shape: one call per graph replay, the L2 flushed before each,
+    median of `reps`; tensor roofline against the measured dense bf16 peak
+    (burst: each call runs alone)."""
     import torch
     tf_peak = load_bf16_peak()
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
     out_rows = []
     for name in names:
         label, kw = wl.PREFILL_SHAPES[name]
@@ -394,11 +396,13 @@ def prefill_leg(pkv, wl, dev, stream, flush_l2, rank, names, reps=20):
         pout = torch.empty(c.total_q, c.w.Hq, c.w.D, dtype=torch.bfloat16, device=dev)
         pst = torch.zeros(1, dtype=torch.int32, device=dev)
         max_q = max(kw["q_lens"])
+        pws = torch.empty(pkv.prefill_workspace_bytes(c.w.D, sms), dtype=torch.uint8,
+                          device=dev)
 
         def prun():
             pkv.paged_prefill_attn(pd, pq, pqo, pt["k_pool"], pt["v_pool"], pt["kv_indices"],
                                    pt["kv_indptr"], pt["seq_lens"], pout, status=pst,
-                                   max_q_len=max_q)
+                                   max_q_len=max_q, workspace=pws)
 
         for _ in range(3):
             prun()
@@ -423,7 +427,7 @@ def prefill_leg(pkv, wl, dev, stream, flush_l2, rank, names, reps=20):
                                       "peak": tf_peak, "unit": "TFLOP/s",
                                       "frac": round(tf / tf_peak, 4)},
                          "flops": c.flops()})
-        del pt, pg
+        del pt, pg, pws
     return out_rows
 
 

@@ -293,6 +293,41 @@ pkv_status paged_prefill_attn(const pkv_dims *dims, const void *q, const int32_t
                               const int32_t *seq_lens, void *out, uint32_t *status,
                               pkv_stream_t stream);
 
+/* paged_prefill_attn with a workspace, which lets it split keys: the pages'
+ * split-KV (partials over ranges of keys merged by their (max, sum), as
+ * decode_combine merges decode splits), applied to prefill's units of work.
+ * Those units are pairs of query tiles of one (row, kv head); one block per
+ * SM takes one unit per round.  When the last round would fill at most half
+ * the SMs (every unit, when they are that few), each of its units runs as
+ * up to min(16, SMs / units in that round, n / 2) parts over consecutive
+ * ranges of its n key blocks, each on an SM of its own.  Every entry of that
+ * round leaves its rows in a workspace slot, normalised on a base of its own
+ * and rounded to bf16 as outputs are, with each row's fp32 (base, l); a
+ * second, small kernel merges each unit's parts in part order and writes
+ * its outputs.  The result differs from paged_prefill_attn's by that one
+ * extra bf16 rounding of each part (within one bf16 step), and is the same
+ * bits from call to call.
+ * workspace: device scratch, 256-byte aligned, ws_bytes long, needing no
+ * initialisation; pkv_prefill_workspace_bytes(D, SMs) has a slot for every
+ * entry a round can hold.  A smaller workspace gets fewer parts; NULL, or
+ * one with fewer slots than two per unit of that round, runs
+ * paged_prefill_attn.  Calls that share a workspace must not overlap on the
+ * GPU.  Other arguments, errors and flags are paged_prefill_attn's;
+ * graph-capturable (one or two kernel launches). */
+pkv_status paged_prefill_attn_ws(const pkv_dims *dims, const void *q, const int32_t *qo_indptr,
+                                 int total_q, int max_q_len, const void *k_pool,
+                                 const void *v_pool, const int32_t *kv_indices,
+                                 const int32_t *kv_indptr, const int32_t *seq_lens,
+                                 void *workspace, size_t ws_bytes, void *out, uint32_t *status,
+                                 pkv_stream_t stream);
+
+/* Bytes of the paged_prefill_attn_ws workspace with a slot for each of
+ * num_sms SMs (the most entries a round holds) at head dim D: per slot two
+ * tiles of 128 bf16 rows of D and 128 fp32 (base, l) pairs,
+ * num_sms x (512 D + 2048) bytes (9.8 MiB at D = 128 on 152 SMs).  0 for D
+ * other than 64 or 128, or num_sms outside 1..1024. */
+size_t pkv_prefill_workspace_bytes(int D, int num_sms);
+
 /* Extend: the K/V write of a prefill / extend chunk, the multi-token form of
  * paged_kv_append (compare v1.3.12..6f09b1d, attention_backend.py: the
  * prefill path stores every new token's K/V at its slot).  Row b's

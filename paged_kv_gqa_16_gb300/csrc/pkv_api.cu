@@ -795,16 +795,27 @@ pkv_status decode_attn_contig_planned(const pkv_dims *dims, const void *q, const
                        true);
 }
 
-pkv_status paged_prefill_attn(const pkv_dims *dims, const void *q, const int32_t *qo_indptr,
-                              int total_q, int max_q_len, const void *k_pool, const void *v_pool,
-                              const int32_t *kv_indices, const int32_t *kv_indptr,
-                              const int32_t *seq_lens, void *out, uint32_t *status,
-                              pkv_stream_t stream)
+size_t pkv_prefill_workspace_bytes(int D, int num_sms)
+{
+    if ((D != 64 && D != 128) || num_sms <= 0 || num_sms > pkv::kPrefillMaxSms)
+        return 0;
+    return (size_t)num_sms * pkv::prefill_slot_bytes(D);
+}
+
+namespace {
+
+pkv_status prefill_impl(const pkv_dims *dims, const void *q, const int32_t *qo_indptr,
+                        int total_q, int max_q_len, const void *k_pool, const void *v_pool,
+                        const int32_t *kv_indices, const int32_t *kv_indptr,
+                        const int32_t *seq_lens, void *workspace, size_t ws_bytes, void *out,
+                        uint32_t *status, pkv_stream_t stream)
 {
     pkv_status st = check_dims(dims);
     if (st != PKV_OK)
         return st;
     if (total_q < 0 || max_q_len < 0 || !(dims->scale > 0.f))
+        return PKV_ERR_INVALID_ARG;
+    if (workspace != nullptr && !aligned(workspace, 256))
         return PKV_ERR_INVALID_ARG;
     if (dims->B == 0 || total_q == 0 || max_q_len == 0)
         return PKV_OK;
@@ -844,7 +855,32 @@ pkv_status paged_prefill_attn(const pkv_dims *dims, const void *q, const int32_t
     p.total_q = total_q;
     p.tq = 128 / p.n_rep;
     p.scale_log2 = (float)((double)dims->scale * 1.4426950408889634);
-    return launch_status(pkv::launch_prefill(p, dims->D, max_q_len, (cudaStream_t)stream));
+    return launch_status(pkv::launch_prefill(p, dims->D, max_q_len, workspace,
+                                             workspace != nullptr ? ws_bytes : 0,
+                                             (cudaStream_t)stream));
+}
+
+} // namespace
+
+pkv_status paged_prefill_attn(const pkv_dims *dims, const void *q, const int32_t *qo_indptr,
+                              int total_q, int max_q_len, const void *k_pool, const void *v_pool,
+                              const int32_t *kv_indices, const int32_t *kv_indptr,
+                              const int32_t *seq_lens, void *out, uint32_t *status,
+                              pkv_stream_t stream)
+{
+    return prefill_impl(dims, q, qo_indptr, total_q, max_q_len, k_pool, v_pool, kv_indices,
+                        kv_indptr, seq_lens, nullptr, 0, out, status, stream);
+}
+
+pkv_status paged_prefill_attn_ws(const pkv_dims *dims, const void *q, const int32_t *qo_indptr,
+                                 int total_q, int max_q_len, const void *k_pool,
+                                 const void *v_pool, const int32_t *kv_indices,
+                                 const int32_t *kv_indptr, const int32_t *seq_lens,
+                                 void *workspace, size_t ws_bytes, void *out, uint32_t *status,
+                                 pkv_stream_t stream)
+{
+    return prefill_impl(dims, q, qo_indptr, total_q, max_q_len, k_pool, v_pool, kv_indices,
+                        kv_indptr, seq_lens, workspace, ws_bytes, out, status, stream);
 }
 
 pkv_status paged_decode_partials(const pkv_dims *dims, const void *q, const void *k_pool,

@@ -125,9 +125,30 @@ struct PrefillParams {
     // the units of work (set by launch_prefill): pairs of query tiles per
     // chunk (from max_q_len) and pairs x B x Hkv
     int pairs;
-    int n_units;
+    int n_units;                   // entries of the list: units, then split parts
     int group_rows;                // rows per group of the unit list
+    // the key split (split > 1): entries [split_base, n_units) are the parts
+    // of the list's last units, split to a unit; entry e's tile x leaves its
+    // normalised rows at ws_o [(2 e + x) x 128 + row][D] and each row's
+    // (base, l) at ws_ml [(2 e + x) x 128 + row] for the merge kernel
+    int split;
+    int split_base;
+    __nv_bfloat16 *ws_o;
+    float2 *ws_ml;
 };
+
+// The prefill's key split.  When the unit list's last round would leave at
+// least half the SMs idle, its units are cut along their key blocks into
+// parts on separate SMs (at most kPrefillMaxParts, each of at least
+// kPrefillMinPartBlocks blocks).
+constexpr int kPrefillMaxParts = 16;
+constexpr int kPrefillMinPartBlocks = 2;
+// Workspace: per entry of the split round, two tiles of 128 bf16 rows of D
+// (all entries' rows first) and two tiles of 128 fp32 (base, l) pairs; for
+// up to kPrefillMaxSms SMs.
+constexpr int kPrefillMaxSms = 1024;
+inline size_t prefill_slot_o_bytes(int D) { return (size_t)2 * 128 * D * 2; }
+inline size_t prefill_slot_bytes(int D) { return prefill_slot_o_bytes(D) + (size_t)2 * 128 * 8; }
 
 // Persistent token-balanced decode (pkv_fused.cu).
 constexpr int kFusedMaxRows = 4096;     // virtual rows whose prefix sums fit in smem
@@ -212,7 +233,10 @@ cudaError_t launch_append(const AppendParams &p, cudaStream_t stream);
 cudaError_t launch_extend(const AppendParams &p, cudaStream_t stream);
 cudaError_t launch_advance(const AdvanceParams &p, cudaStream_t stream);
 // one persistent block per SM over the units (pairs of query tiles x B x Hkv)
-cudaError_t launch_prefill(const PrefillParams &p, int D, int max_q_len, cudaStream_t stream);
+// workspace (nullable, 256-byte aligned, ws_bytes long) enables the key
+// split with as many part slots as it holds.
+cudaError_t launch_prefill(const PrefillParams &p, int D, int max_q_len, void *workspace,
+                           size_t ws_bytes, cudaStream_t stream);
 // table[0..B] = 0..B (kv_indptr), table[B+1+b] = idx ? idx[b] : b (kv_indices)
 cudaError_t launch_contig_table(const int32_t *idx, int B, int32_t *table, cudaStream_t stream);
 cudaError_t launch_rope_table(float *cos_sin, int max_pos, int D, double base,

@@ -44,6 +44,8 @@ namespace pkv {
 namespace {
 
 constexpr unsigned kAllTc = 0xffffffffu;
+// the position of a softmax row with no query: below every key
+constexpr int kNoQuery = -(1 << 30);
 
 __device__ __forceinline__ void tc_flag(uint32_t *status, unsigned bits)
 {
@@ -260,7 +262,10 @@ struct PrefillCfg {
     static constexpr int kXchBytes = 2 * 2 * 2 * kRows * 4;
     static constexpr int kTmemSlot = kXchOff + kXchBytes;
     static constexpr int kAbortOff = kTmemSlot + 4;
-    static constexpr int kSmemBytes = kAbortOff + 12;
+    // a split list's entry of each tile, by unit parity: its slot when it is
+    // a part of a split unit, else -1
+    static constexpr int kPartSlotOff = kAbortOff + 4;
+    static constexpr int kSmemBytes = kPartSlotOff + 16;
     static_assert(kSmemBytes <= 232448, "shared memory per block");
     // the block holds all of tensor memory: its shared memory keeps a second
     // block off the SM (whose allocation would wait for this one's release)
@@ -342,16 +347,31 @@ __device__ __forceinline__ float ex2_fast(float x)
 // One unit of work: query tiles tB = n_tiles - 1 - 2 pair (the most keys
 // first) and tA = tB - 1 (-1: idle) of row b's chunk, with kv head g.
 struct PrefillUnit {
-    int b, g, q0, q_len, L, tA, tB, kv_end, n_kb, pg0;
+    int b, g, q0, q_len, L, tA, tB, kv_end, pg0;
+    int kb0, n_kb;                 // the key blocks [kb0, kb0 + n_kb) this entry runs
+    // a part of a split unit: slot << 9 | parts << 4 | part; -1 for a whole unit
+    int part_id;
     bool table_ok;
 };
+
+// 32 outputs of a row, v x inv rounded to bf16, as four 16-byte stores.
+__device__ __forceinline__ void store_out_row(__nv_bfloat16 *dst, const float (&v)[32], float inv)
+{
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+        *reinterpret_cast<uint4 *>(dst + 8 * q) =
+            make_uint4(pack_bf16x2(v[8 * q] * inv, v[8 * q + 1] * inv),
+                       pack_bf16x2(v[8 * q + 2] * inv, v[8 * q + 3] * inv),
+                       pack_bf16x2(v[8 * q + 4] * inv, v[8 * q + 5] * inv),
+                       pack_bf16x2(v[8 * q + 6] * inv, v[8 * q + 7] * inv));
+}
 
 // Unit u of the list: rows (b x Hkv + g) in groups of p.group_rows, the
 // groups one after another and each group pair-major (its rows' largest
 // pairs first); false when the unit has no work: a pair past its row's
 // chunk, or a refused row.  flag: report refusals in the status.
-__device__ __forceinline__ bool prefill_unit(const PrefillParams &p, int u, PrefillUnit &w,
-                                             bool flag)
+__device__ __forceinline__ bool prefill_whole_unit(const PrefillParams &p, int u, PrefillUnit &w,
+                                                   bool flag)
 {
     const int rows = p.B * p.Hkv;
     int pair, rh;
@@ -389,6 +409,8 @@ __device__ __forceinline__ bool prefill_unit(const PrefillParams &p, int u, Pref
     w.tA = w.tB - 1;
     w.kv_end = w.L - w.q_len + min(w.q_len, (w.tB + 1) * p.tq);
     w.n_kb = (w.kv_end + 127) / 128;
+    w.kb0 = 0;
+    w.part_id = -1;
     w.pg0 = k0;
     const int npg = k1 - k0;
     w.table_ok = k0 >= 0 && npg >= 0 && k1 <= p.num_indices &&
@@ -398,11 +420,39 @@ __device__ __forceinline__ bool prefill_unit(const PrefillParams &p, int u, Pref
     return true;
 }
 
+// Entry u of the list: unit u, or in a list with a key split (kSplit), from
+// p.split_base on, parts, p.split to a unit: part k of a unit of n blocks in
+// np = min(p.split, n / kPrefillMinPartBlocks) parts (at least one) takes
+// blocks [k n / np, (k + 1) n / np); false when the entry has no work (also
+// a part past its unit's share).
+template <bool kSplit>
+__device__ __forceinline__ bool prefill_unit(const PrefillParams &p, int u, PrefillUnit &w,
+                                             bool flag)
+{
+    if (kSplit && u >= p.split_base) {
+        const int slot = u - p.split_base, part = slot % p.split;
+        if (!prefill_whole_unit(p, p.split_base + slot / p.split, w, flag && part == 0))
+            return false;
+        const int np = max(1, min(p.split, w.n_kb / kPrefillMinPartBlocks));
+        if (part >= np)
+            return false;
+        const int lo = part * w.n_kb / np, hi = (part + 1) * w.n_kb / np;
+        w.kb0 = lo;
+        w.n_kb = hi - lo;
+        if (np > 1)
+            w.part_id = slot << 9 | np << 4 | part;
+        return true;
+    }
+    return prefill_whole_unit(p, u, w, flag);
+}
+
 // A persistent block (one per SM) takes one unit per round of gridDim.x
 // units; every role walks the same list and keeps its ring and phase
 // counters across units, so one unit's epilogue overlaps the next unit's
 // loads and first products.
-template <int D>
+// kSplit: the list ends in a key split's parts (p.split > 1); without one the
+// kernel has no trace of it (every entry a whole unit from key 0).
+template <int D, bool kSplit>
 __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
     prefill_kernel(const __grid_constant__ PrefillParams p)
 {
@@ -418,6 +468,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
     uint64_t *drain = q_empty + 2, *xch_bar = drain + 1, *turn = xch_bar + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kTmemSlot);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kAbortOff);
+    volatile int *part_slot = reinterpret_cast<volatile int *>(smem + C::kPartSlotOff);
     const uint32_t sbase = smem_addr(smem);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int n_rep = p.n_rep, tq = p.tq;
@@ -496,7 +547,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
             for (int r = 0; r * (int)gridDim.x < n_units && !*abort_flag; ++r) {
                 const int u = unit_index(r);
                 PrefillUnit w;
-                if (u >= n_units || !prefill_unit(p, u, w, is_v && lane == 0))
+                if (u >= n_units || !prefill_unit<kSplit>(p, u, w, is_v && lane == 0))
                     continue;
                 // the V warp also loads the unit's Q (row m = token m / n_rep,
                 // head m % n_rep, swizzled like K), each tile's once the previous
@@ -551,7 +602,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
                     if (*abort_flag)
                         break;
                     const uint32_t dst = ring + slot * C::kKVBytes;
-                    const int key0 = j * C::kKeys;
+                    const int key0 = (w.kb0 + j) * C::kKeys;
                     const int nkeys = min(C::kKeys, w.kv_end - key0);
                     // K rows past kv_end are masked out of S whatever they hold,
                     // so a K block loads whole boxes; V rows past it meet P = 0 and
@@ -686,7 +737,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
                 for (int r = 0; r * (int)gridDim.x < n_units && ok; ++r) {
                     const int u = unit_index(r);
                     PrefillUnit w;
-                    if (u >= n_units || !prefill_unit(p, u, w, false))
+                    if (u >= n_units || !prefill_unit<kSplit>(p, u, w, false))
                         continue;
                     const int n_kb = w.n_kb;
                     if (!wait_only(&q_full[x], (uint32_t)(it & 1)) ||
@@ -711,7 +762,8 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
                         const bool more = j + 1 < n_kb;
                         // this run's data and P, waited for while the other
                         // tile's run is issued
-                        const bool v_gen = !p.use_tma || w.kv_end - j * C::kKeys < C::kKeys;
+                        const bool v_gen =
+                            !p.use_tma || w.kv_end - (w.kb0 + j) * C::kKeys < C::kKeys;
                         if (!wait_only(&v_full[kj % VS], (uint32_t)((kj / VS) & 1)))
                             break;
                         if (more &&
@@ -799,12 +851,17 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
         for (int r = 0; r * (int)gridDim.x < n_units && ok; ++r) {
             const int u = unit_index(r);
             PrefillUnit w;
-            if (u >= n_units || !prefill_unit(p, u, w, false))
+            if (u >= n_units || !prefill_unit<kSplit>(p, u, w, false))
                 continue;
+            if (kSplit && m == 0 && h == 0)
+                part_slot[2 * x + (it & 1)] = w.part_id >= 0 ? w.part_id >> 9 : -1;
             const int t = x == 0 ? w.tA : w.tB;
             const int ntok = t >= 0 ? min(tq, w.q_len - t * tq) : 0;
-            const int pos_first = w.L - w.q_len + (t >= 0 ? t * tq : 0);
-            const int pos = (t >= 0 && m < rows_used && tok_m < ntok) ? pos_first + tok_m : -1;
+            // positions counted from the entry's first key (a part of a split
+            // unit starts at block kb0); a row with no query masks every key
+            const int pos_first = w.L - w.q_len + (t >= 0 ? t * tq : 0) - w.kb0 * C::kKeys;
+            const int pos =
+                (t >= 0 && m < rows_used && tok_m < ntok) ? pos_first + tok_m : kNoQuery;
             float m_run = -INFINITY, l_run = 0.f;
             for (int j = 0; j < w.n_kb; ++j) {
                 ok = mbar_wait_bounded(&s_full[x], sc & 1u) && !*abort_flag;
@@ -904,8 +961,18 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
             tc_fence_after();
             const float l_row = l_run + lo;
             const float inv = l_row > 0.f ? 1.f / l_row : 0.f;
+            // a part of a split unit stores its rows like any entry, into its
+            // workspace slot, with the row's (base, l) beside them for the
+            // merge kernel (its slot was published at the unit's start, two
+            // exchanges ago)
             __nv_bfloat16 *orow = nullptr;
-            if (pos >= 0) {
+            const int slot = kSplit ? part_slot[2 * x + (it & 1)] : -1;
+            if (slot >= 0) {
+                const size_t tile = (size_t)slot * 2 + x;
+                orow = p.ws_o + (tile * C::kRows + m) * D + (D / 2) * h;
+                if (h == 0)
+                    p.ws_ml[tile * C::kRows + m] = make_float2(m_run, l_row);
+            } else if (pos != kNoQuery) {
                 const int hh = m - tok_m * n_rep;
                 orow = p.out +
                        ((size_t)(w.q0 + t * tq + tok_m) * p.Hq + (size_t)w.g * n_rep + hh) * D +
@@ -915,15 +982,8 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
             for (int c0 = 0; c0 < D / 2; c0 += 32) {
                 float v[32];
                 tmem_ld32(t_o + c0, v);
-                if (orow != nullptr) {
-#pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        *reinterpret_cast<uint4 *>(orow + c0 + 8 * q) =
-                            make_uint4(pack_bf16x2(v[8 * q] * inv, v[8 * q + 1] * inv),
-                                       pack_bf16x2(v[8 * q + 2] * inv, v[8 * q + 3] * inv),
-                                       pack_bf16x2(v[8 * q + 4] * inv, v[8 * q + 5] * inv),
-                                       pack_bf16x2(v[8 * q + 6] * inv, v[8 * q + 7] * inv));
-                }
+                if (orow != nullptr)
+                    store_out_row(orow + c0, v, inv);
             }
             tc_fence_before();
             __syncwarp();
@@ -947,23 +1007,85 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
     }
 }
 
+// The key split's merge: D / 8 blocks per split unit and tile, a thread per
+// (row, 16-byte column group); units of the split round that were not cut
+// wrote their outputs themselves.  Each part left its rows normalised on a base
+// of its own with (base, l): part i weighs l_i 2^(base_i - the largest
+// base), and the parts are summed in part order (the pages' split-KV merge
+// by (max, sum), as decode_combine does per split).
 template <int D>
-cudaError_t launch_prefill_d(const PrefillParams &p, cudaStream_t stream)
+__global__ void __launch_bounds__(128) prefill_merge_kernel(const __grid_constant__ PrefillParams p)
+{
+    using C = PrefillCfg<D>;
+    constexpr int kGroups = D / 8;                     // 16-byte column groups per row
+    grid_dependency_wait();
+    const int blk = (int)blockIdx.x / kGroups, sub = (int)blockIdx.x - blk * kGroups;
+    const int su = blk >> 1, x = blk & 1;
+    PrefillUnit w;
+    // the unit as its first part sees it: np parts (one when not cut)
+    if (!prefill_unit<true>(p, p.split_base + su * p.split, w, false))
+        return;
+    if (w.part_id < 0)
+        return;                                        // not cut: written whole
+    const int np = (w.part_id >> 4) & 31;
+    const int t = x == 0 ? w.tA : w.tB;
+    const int e = sub * (int)blockDim.x + (int)threadIdx.x;   // (row, group) of the tile
+    const int m = e / kGroups, c = (e - m * kGroups) * 8;
+    const int n_rep = p.n_rep, tq = p.tq;
+    if (t < 0 || m >= min(tq, w.q_len - t * tq) * n_rep)
+        return;
+    const size_t tile0 = (size_t)su * p.split * 2 + x;    // part i: tile0 + 2 i
+    float mm = -INFINITY;
+#pragma unroll 4
+    for (int i = 0; i < np; ++i) {
+        const float2 ml = __ldcg(&p.ws_ml[(tile0 + 2 * i) * C::kRows + m]);
+        if (ml.y > 0.f)
+            mm = fmaxf(mm, ml.x);
+    }
+    float v[8], l_sum = 0.f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+        v[k] = 0.f;
+#pragma unroll 4
+    for (int i = 0; i < np; ++i) {
+        const size_t tile = tile0 + 2 * (size_t)i;
+        const float2 ml = __ldcg(&p.ws_ml[tile * C::kRows + m]);
+        const uint4 a =
+            __ldcg(reinterpret_cast<const uint4 *>(p.ws_o + (tile * C::kRows + m) * D + c));
+        const float wl = ml.y > 0.f ? ex2_fast(ml.x - mm) * ml.y : 0.f;
+        l_sum += wl;
+        const uint32_t pa[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&pa[k]));
+            v[2 * k] += wl * f.x;
+            v[2 * k + 1] += wl * f.y;
+        }
+    }
+    const float inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
+    const int tok = m / n_rep, hh = m - tok * n_rep;
+    __nv_bfloat16 *orow =
+        p.out + ((size_t)(w.q0 + t * tq + tok) * p.Hq + (size_t)w.g * n_rep + hh) * D + c;
+    *reinterpret_cast<uint4 *>(orow) =
+        make_uint4(pack_bf16x2(v[0] * inv, v[1] * inv), pack_bf16x2(v[2] * inv, v[3] * inv),
+                   pack_bf16x2(v[4] * inv, v[5] * inv), pack_bf16x2(v[6] * inv, v[7] * inv));
+}
+
+template <int D>
+cudaError_t launch_prefill_d(const PrefillParams &p, int sms, cudaStream_t stream)
 {
     using C = PrefillCfg<D>;
     static DeviceOnce attrs;
     const cudaError_t attr_err = attrs.run([] {
-        return cudaFuncSetAttribute(prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    C::kSmemBytes);
+        cudaError_t e = cudaFuncSetAttribute(
+            prefill_kernel<D, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(prefill_kernel<D, true>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+        return e;
     });
     if (attr_err != cudaSuccess)
         return attr_err;
-    int dev = 0, sms = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e == cudaSuccess)
-        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess)
-        return e;
     // one persistent block per SM (each holds all of an SM's tensor memory)
     const int grid = p.n_units < sms ? p.n_units : sms;
     cudaLaunchConfig_t cfg = {};
@@ -976,7 +1098,15 @@ cudaError_t launch_prefill_d(const PrefillParams &p, cudaStream_t stream)
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, prefill_kernel<D>, p);
+    cudaError_t e = p.split > 1 ? cudaLaunchKernelEx(&cfg, prefill_kernel<D, true>, p)
+                                : cudaLaunchKernelEx(&cfg, prefill_kernel<D, false>, p);
+    if (e == cudaSuccess && p.split > 1) {
+        // the split units' merge, once the kernel above has finished
+        cfg.gridDim = dim3((unsigned)(2 * ((p.n_units - p.split_base) / p.split) * (D / 8)));
+        cfg.blockDim = dim3(C::kRows);
+        cfg.dynamicSmemBytes = 0;
+        e = cudaLaunchKernelEx(&cfg, prefill_merge_kernel<D>, p);
+    }
     if (e != cudaSuccess)
         return e;
     return cudaGetLastError();
@@ -1025,7 +1155,8 @@ bool encode_map(CUtensorMap *map, const void *base, int D, int mid, long long ro
 // Chunks of at most this many pairs of query tiles get a grouped unit list.
 constexpr int kGroupMaxPairs = 4;
 
-cudaError_t launch_prefill(const PrefillParams &p_in, int D, int max_q_len, cudaStream_t stream)
+cudaError_t launch_prefill(const PrefillParams &p_in, int D, int max_q_len, void *workspace,
+                           size_t ws_bytes, cudaStream_t stream)
 {
     // K/V pages by TMA when a page is a power of two >= 8 rows (whole 8-row
     // swizzle atoms; a 128-key block is whole pages or a part of one) and
@@ -1047,8 +1178,6 @@ cudaError_t launch_prefill(const PrefillParams &p_in, int D, int max_q_len, cuda
     if ((D == 64 || D == 128) && p.total_q > 0 && p.n_rep <= 256 && p.tq >= 1 && p.tq <= 256 &&
         encode_map(&p.tmap_q, p.q, D, p.Hq, p.total_q, p.n_rep, p.tq))
         p.q_tma = 1;
-    // the paired, warp-specialised layout is 27-31% faster at D = 128; at
-    // D = 64 the single-tile blocks, three to an SM, are 16% faster
     // the units: pairs of query tiles (max_q_len bounds a chunk's tiles) x
     // rows x kv heads
     const long long tiles = ((long long)max_q_len + p.tq - 1) / p.tq;
@@ -1060,6 +1189,12 @@ cudaError_t launch_prefill(const PrefillParams &p_in, int D, int max_q_len, cuda
         return cudaErrorInvalidValue;
     p.pairs = (int)pairs;
     p.n_units = (int)units;
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess)
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess)
+        return e;
     // rows per group of the unit list.  A chunk of many pairs (a long causal
     // prefill) has units from one to hundreds of key blocks: one group,
     // pair-major, keeps each round's units of about one size.  A chunk of a
@@ -1069,15 +1204,40 @@ cudaError_t launch_prefill(const PrefillParams &p_in, int D, int max_q_len, cuda
     const long long row_heads = (long long)p.B * p.Hkv;
     long long grp = row_heads;
     if (pairs <= kGroupMaxPairs) {
-        int dev = 0, sms = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-            sms = 1;
         grp = (long long)sms / pairs;
         grp = grp < 1 ? 1 : (grp > row_heads ? row_heads : grp);
     }
     p.group_rows = (int)grp;
-    return D == 64 ? launch_prefill_d<64>(p, stream) : launch_prefill_d<128>(p, stream);
+    // the key split: a last round of at most half the SMs (every unit, when
+    // they are that few) becomes up to SMs / last entries per unit, as many
+    // as the workspace has slots for; every entry of that region leaves its
+    // result in its slot and the merge kernel writes the outputs
+    p.split = 1;
+    p.split_base = p.n_units;
+    p.ws_o = nullptr;
+    p.ws_ml = nullptr;
+    if (workspace != nullptr) {
+        const long long g0 = units < sms ? units : sms;
+        const long long last = units - (units - 1) / g0 * g0;
+        const long long slots = (long long)(ws_bytes / prefill_slot_bytes(D));
+        long long split = sms / last;
+        split = split < kPrefillMaxParts ? split : kPrefillMaxParts;
+        split = split < slots / last ? split : slots / last;
+        // a pair-major list of many rounds ends on its smallest pairs (the
+        // first query tiles of long chunks: a few key blocks each), so only
+        // a grouped list (chunks of a few tile pairs, units of about one
+        // size) or a list of one round is cut
+        const bool big_last = pairs <= kGroupMaxPairs || units <= g0;
+        if (big_last && 2 * last <= sms && split >= 2) {
+            p.split = (int)split;
+            p.split_base = (int)(units - last);
+            p.n_units = (int)(units - last + last * split);
+            p.ws_o = static_cast<__nv_bfloat16 *>(workspace);
+            p.ws_ml = reinterpret_cast<float2 *>(static_cast<char *>(workspace) +
+                                                 (size_t)last * split * prefill_slot_o_bytes(D));
+        }
+    }
+    return D == 64 ? launch_prefill_d<64>(p, sms, stream) : launch_prefill_d<128>(p, sms, stream);
 }
 
 } // namespace pkv

@@ -39,7 +39,8 @@ EXPORTS = (
     "pkv_version", "paged_decode_attn_noalloc", "paged_kv_advance", "decode_attn_contig",
     "paged_prefill_attn", "paged_kv_extend", "paged_decode_step_advance",
     "pkv_testing_set_handoff_wait_ns", "paged_decode_plan", "paged_decode_attn_planned",
-    "paged_decode_step_planned", "decode_attn_contig_planned",
+    "paged_decode_step_planned", "decode_attn_contig_planned", "paged_prefill_attn_ws",
+    "pkv_prefill_workspace_bytes",
 )
 
 
@@ -100,6 +101,8 @@ def lib():
             "decode_attn_contig": (I, [DP, P, P, P, P, P, P, P, P, I, I, P, Z, P, P]),
             "decode_attn_contig_planned": (I, [DP, P, P, P, P, P, P, P, P, I, I, P, Z, P, P]),
             "paged_prefill_attn": (I, [DP, P, P, I, I, P, P, P, P, P, P, P, P]),
+            "paged_prefill_attn_ws": (I, [DP, P, P, I, I, P, P, P, P, P, P, Z, P, P, P]),
+            "pkv_prefill_workspace_bytes": (Z, [I, I]),
             "paged_kv_extend": (I, [DP, P, P, P, P, I, P, P, P, P, P, P, I, I, P, P]),
             "pkv_testing_set_handoff_wait_ns": (I, [ctypes.c_ulonglong]),
             "pkv_status_str": (ctypes.c_char_p, [I]),
@@ -288,18 +291,33 @@ def decode_attn_contig(d: Dims, q, k_cache, v_cache, seq_lens, num_splits: int, 
 
 
 def paged_prefill_attn(d: Dims, q, qo_indptr, k_pool, v_pool, kv_indices, kv_indptr, seq_lens,
-                       out, status=None, max_q_len: Optional[int] = None, stream=None) -> None:
+                       out, status=None, max_q_len: Optional[int] = None, stream=None,
+                       workspace=None) -> None:
     """Ragged prefill / extend: q [total_q, Hq, D], row b's chunk the last
     q_len of its seq_lens[b] tokens, each query attending causally.
     max_q_len (>= every chunk length) sizes the grid; None: total_q, always
     safe but many rows then launch many blocks that exit at once -- pass the
-    real maximum when it is known."""
+    real maximum when it is known.  workspace (a device tensor of
+    prefill_workspace_bytes, no initialisation needed): paged_prefill_attn_ws,
+    which splits the keys of an under-filled last round."""
     total_q = int(q.shape[0])
-    _check("paged_prefill_attn", lib().paged_prefill_attn(
-        ctypes.byref(d), _ptr(q), _ptr(qo_indptr), total_q,
-        total_q if max_q_len is None else int(max_q_len), _ptr(k_pool), _ptr(v_pool),
-        _ptr(kv_indices), _ptr(kv_indptr), _ptr(seq_lens), _ptr(out), _ptr(status),
-        _stream(stream)))
+    mq = total_q if max_q_len is None else int(max_q_len)
+    if workspace is None:
+        _check("paged_prefill_attn", lib().paged_prefill_attn(
+            ctypes.byref(d), _ptr(q), _ptr(qo_indptr), total_q, mq, _ptr(k_pool), _ptr(v_pool),
+            _ptr(kv_indices), _ptr(kv_indptr), _ptr(seq_lens), _ptr(out), _ptr(status),
+            _stream(stream)))
+        return
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check("paged_prefill_attn_ws", lib().paged_prefill_attn_ws(
+        ctypes.byref(d), _ptr(q), _ptr(qo_indptr), total_q, mq, _ptr(k_pool), _ptr(v_pool),
+        _ptr(kv_indices), _ptr(kv_indptr), _ptr(seq_lens), _ptr(workspace), ws_bytes,
+        _ptr(out), _ptr(status), _stream(stream)))
+
+
+def prefill_workspace_bytes(D: int, num_sms: int) -> int:
+    """pkv_prefill_workspace_bytes: a key-split slot for every SM."""
+    return int(lib().pkv_prefill_workspace_bytes(int(D), int(num_sms)))
 
 
 def paged_kv_extend(d: Dims, q, k_new, v_new, qo_indptr, k_pool, v_pool, kv_indices, kv_indptr,

@@ -260,3 +260,15 @@ def test_workspace_holds_the_plan():
     """The workspace grows with the plan: one 72-word entry per block."""
     d = _d()
     assert pkv.workspace_bytes(d, 152) - pkv.workspace_bytes(d, 8) >= 144 * 72 * 4
+
+
+def test_prefill_workspace_bytes():
+    """Per SM a slot of two tiles x 128 rows: D bf16 and an fp32 (base, l)
+    pair each; 0 for an unbuilt head dim or SM count."""
+    assert pkv.prefill_workspace_bytes(128, 152) == 152 * 2 * 128 * (128 * 2 + 8)
+    assert pkv.prefill_workspace_bytes(64, 152) == 152 * 2 * 128 * (64 * 2 + 8)
+    assert pkv.prefill_workspace_bytes(64, 1) == 2 * 128 * (64 * 2 + 8)
+    # the rows of any number of slots end on a 256-byte boundary
+    assert (2 * 128 * 128 * 2) % 256 == 0 and (2 * 128 * 64 * 2) % 256 == 0
+    for D, n in [(96, 152), (256, 152), (128, 0), (128, -3), (64, 1025)]:
+        assert pkv.prefill_workspace_bytes(D, n) == 0

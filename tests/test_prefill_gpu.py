@@ -222,7 +222,8 @@ def test_prefill_bench_shape_sampled(name, runs, n_random):
 
 
 def _run_bench_config(c):
-    """One call as the benchmark makes it: max_q_len is the longest chunk."""
+    """One call as the benchmark makes it: max_q_len is the longest chunk, and
+    a workspace with a part slot per SM (paged_prefill_attn_ws)."""
     w = c.w
     t = w.to_device("cuda")
     P = t["k_pool"].shape[0]
@@ -231,8 +232,10 @@ def _run_bench_config(c):
     out = torch.full((c.total_q, w.Hq, w.D), float("nan"), dtype=torch.bfloat16, device="cuda")
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
     ql = (c.qo_indptr[1:] - c.qo_indptr[:-1]).tolist()
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    ws = torch.zeros(pkv.prefill_workspace_bytes(w.D, sms), dtype=torch.uint8, device="cuda")
     pkv.paged_prefill_attn(d, c.q.cuda(), c.qo_indptr.cuda(), t["k_pool"], t["v_pool"],
                            t["kv_indices"], t["kv_indptr"], t["seq_lens"], out, status=st,
-                           max_q_len=max(ql))
+                           max_q_len=max(ql), workspace=ws)
     torch.cuda.synchronize()
     return out.cpu(), int(st.item()) & 0xFFFFFFFF, (d, t)
