@@ -1009,8 +1009,8 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
 
 // The key split's merge: D / 8 blocks per split unit and tile, a thread per
 // (row, 16-byte column group); units of the split round that were not cut
-// wrote their outputs themselves.  Each part left its rows normalised on a base
-// of its own with (base, l): part i weighs l_i 2^(base_i - the largest
+// wrote their outputs themselves.  Each part left its rows normalised on a
+// base of its own with (base, l): part i weighs l_i 2^(base_i - the largest
 // base), and the parts are summed in part order (the pages' split-KV merge
 // by (max, sum), as decode_combine does per split).
 template <int D>
@@ -1018,48 +1018,69 @@ __global__ void __launch_bounds__(128) prefill_merge_kernel(const __grid_constan
 {
     using C = PrefillCfg<D>;
     constexpr int kGroups = D / 8;                     // 16-byte column groups per row
-    grid_dependency_wait();
     const int blk = (int)blockIdx.x / kGroups, sub = (int)blockIdx.x - blk * kGroups;
     const int su = blk >> 1, x = blk & 1;
-    PrefillUnit w;
-    // the unit as its first part sees it: np parts (one when not cut)
-    if (!prefill_unit<true>(p, p.split_base + su * p.split, w, false))
-        return;
-    if (w.part_id < 0)
-        return;                                        // not cut: written whole
-    const int np = (w.part_id >> 4) & 31;
-    const int t = x == 0 ? w.tA : w.tB;
     const int e = sub * (int)blockDim.x + (int)threadIdx.x;   // (row, group) of the tile
     const int m = e / kGroups, c = (e - m * kGroups) * 8;
+    const size_t tile0 = (size_t)su * p.split * 2 + x;    // part i: tile0 + 2 i
+    grid_dependency_wait();
+    // the first four parts' rows load while the unit is looked up (every
+    // unit of the split round owns p.split slots, written or not)
+    float2 ml[4];
+    uint4 a[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const size_t tile = tile0 + 2 * (size_t)(j < p.split ? j : 0);
+        ml[j] = __ldcg(&p.ws_ml[tile * C::kRows + m]);
+        a[j] = __ldcg(reinterpret_cast<const uint4 *>(p.ws_o + (tile * C::kRows + m) * D + c));
+    }
+    PrefillUnit w;
+    // the unit as its first part sees it: np parts, or not cut
+    if (!prefill_unit<true>(p, p.split_base + su * p.split, w, false) || w.part_id < 0)
+        return;                                        // no work, or written whole
+    const int np = (w.part_id >> 4) & 31;
+    const int t = x == 0 ? w.tA : w.tB;
     const int n_rep = p.n_rep, tq = p.tq;
     if (t < 0 || m >= min(tq, w.q_len - t * tq) * n_rep)
         return;
-    const size_t tile0 = (size_t)su * p.split * 2 + x;    // part i: tile0 + 2 i
-    float mm = -INFINITY;
-#pragma unroll 4
-    for (int i = 0; i < np; ++i) {
-        const float2 ml = __ldcg(&p.ws_ml[(tile0 + 2 * i) * C::kRows + m]);
-        if (ml.y > 0.f)
-            mm = fmaxf(mm, ml.x);
-    }
-    float v[8], l_sum = 0.f;
+    // one pass over the parts in part order; a running largest base
+    // rescales what is summed so far
+    float mm = -INFINITY, l_sum = 0.f, v[8];
 #pragma unroll
     for (int k = 0; k < 8; ++k)
         v[k] = 0.f;
-#pragma unroll 4
-    for (int i = 0; i < np; ++i) {
-        const size_t tile = tile0 + 2 * (size_t)i;
-        const float2 ml = __ldcg(&p.ws_ml[tile * C::kRows + m]);
-        const uint4 a =
-            __ldcg(reinterpret_cast<const uint4 *>(p.ws_o + (tile * C::kRows + m) * D + c));
-        const float wl = ml.y > 0.f ? ex2_fast(ml.x - mm) * ml.y : 0.f;
-        l_sum += wl;
-        const uint32_t pa[4] = {a.x, a.y, a.z, a.w};
+    for (int i0 = 0; i0 < np; i0 += 4) {
+        if (i0 > 0) {
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&pa[k]));
-            v[2 * k] += wl * f.x;
-            v[2 * k + 1] += wl * f.y;
+            for (int j = 0; j < 4; ++j) {
+                const size_t tile = tile0 + 2 * (size_t)(i0 + j < np ? i0 + j : i0);
+                ml[j] = __ldcg(&p.ws_ml[tile * C::kRows + m]);
+                a[j] = __ldcg(
+                    reinterpret_cast<const uint4 *>(p.ws_o + (tile * C::kRows + m) * D + c));
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            if (i0 + j >= np || !(ml[j].y > 0.f))
+                continue;
+            if (ml[j].x > mm) {
+                const float r = ex2_fast(mm - ml[j].x);        // 0 while mm is -inf
+                l_sum *= r;
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    v[k] *= r;
+                mm = ml[j].x;
+            }
+            const float wl = ex2_fast(ml[j].x - mm) * ml[j].y;
+            l_sum += wl;
+            const uint32_t pa[4] = {a[j].x, a[j].y, a[j].z, a[j].w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float2 f =
+                    __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&pa[k]));
+                v[2 * k] += wl * f.x;
+                v[2 * k + 1] += wl * f.y;
+            }
         }
     }
     const float inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
