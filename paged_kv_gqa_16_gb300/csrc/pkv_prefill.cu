@@ -31,6 +31,11 @@
 //   - tile A's products are issued by one thread and tile B's by another,
 //     taking turns one run at a time, so each makes its waits and commits
 //     while the other's run goes out.
+// With a workspace (paged_prefill_attn_ws), a list whose last round would
+// leave at least half the SMs idle cuts that round's units along their key
+// blocks (the split-KV of the decode, applied to prefill): each part stores
+// its rows normalised on its own base, with the rows' (base, l), in a
+// workspace slot, and prefill_merge_kernel combines the parts.
 // Every mbarrier wait is time-bounded; tensor memory is allocated at the
 // start and released on every path.
 #include <cmath>
