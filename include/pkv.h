@@ -328,6 +328,26 @@ pkv_status paged_prefill_attn_ws(const pkv_dims *dims, const void *q, const int3
  * other than 64 or 128, or num_sms outside 1..1024. */
 size_t pkv_prefill_workspace_bytes(int D, int num_sms);
 
+/* The list of work paged_prefill_attn / paged_prefill_attn_ws would launch
+ * on num_sms SMs (host only; no device is touched), for planning and tests.
+ * plan (host, 7 int32) receives:
+ *   [0] pairs      tile pairs in a chunk of max_q_len (a tile is 128 / n_rep
+ *                  tokens x n_rep query heads)
+ *   [1] units      pairs x B x Hkv
+ *   [2] group_rows rows (b, kv head) per group of the list: all of them
+ *                  (pair-major) when a chunk has more than 4 pairs
+ *   [3] entries    units, or with a key split units - last + last x split
+ *   [4] split      parts per unit of the last round (1: no split); a split
+ *                  needs ws_bytes > 0, a last round of at most num_sms / 2
+ *                  units, and a grouped list or a single round
+ *   [5] split_base the last round's first entry
+ *   [6] grid       blocks launched: min(entries, num_sms)
+ * ws_bytes: the workspace paged_prefill_attn_ws would get (0: none).  Errors:
+ * check_dims's, PKV_ERR_INVALID_ARG for a null plan, max_q_len < 0 or
+ * num_sms outside 1..1024, PKV_ERR_UNSUPPORTED past 2^31 - 1 units. */
+pkv_status pkv_prefill_plan(const pkv_dims *dims, int max_q_len, int num_sms, size_t ws_bytes,
+                            int32_t *plan);
+
 /* Extend: the K/V write of a prefill / extend chunk, the multi-token form of
  * paged_kv_append (compare v1.3.12..6f09b1d, attention_backend.py: the
  * prefill path stores every new token's K/V at its slot).  Row b's

@@ -795,6 +795,26 @@ pkv_status decode_attn_contig_planned(const pkv_dims *dims, const void *q, const
                        true);
 }
 
+pkv_status pkv_prefill_plan(const pkv_dims *dims, int max_q_len, int num_sms, size_t ws_bytes,
+                            int32_t *plan)
+{
+    pkv_status st = check_dims(dims);
+    if (st != PKV_OK)
+        return st;
+    if (plan == nullptr || max_q_len < 0 || num_sms < 1 || num_sms > pkv::kPrefillMaxSms)
+        return PKV_ERR_INVALID_ARG;
+    pkv::PrefillPlan pl;
+    const int n_rep = dims->Hq / dims->Hkv;
+    if (!pkv::prefill_plan(dims->B, dims->Hkv, 128 / n_rep, max_q_len, num_sms, dims->D,
+                           ws_bytes, &pl))
+        return PKV_ERR_UNSUPPORTED;
+    const int32_t v[7] = {pl.pairs, pl.units, pl.group_rows, pl.entries, pl.split,
+                          pl.split_base, pl.grid};
+    for (int i = 0; i < 7; ++i)
+        plan[i] = v[i];
+    return PKV_OK;
+}
+
 size_t pkv_prefill_workspace_bytes(int D, int num_sms)
 {
     if ((D != 64 && D != 128) || num_sms <= 0 || num_sms > pkv::kPrefillMaxSms)

@@ -233,6 +233,22 @@ cudaError_t launch_append(const AppendParams &p, cudaStream_t stream);
 cudaError_t launch_extend(const AppendParams &p, cudaStream_t stream);
 cudaError_t launch_advance(const AdvanceParams &p, cudaStream_t stream);
 // one persistent block per SM over the units (pairs of query tiles x B x Hkv)
+// The prefill's list for a launch (host only): units of tile pairs, their
+// grouping, and the key split of the last round.
+struct PrefillPlan {
+    int pairs;       // tile pairs a chunk of max_q_len has
+    int units;       // pairs x B x Hkv (0: nothing to run)
+    int group_rows;  // rows per group of the list
+    int entries;     // units, or with a split units - last + last x split
+    int split;       // parts per unit of the last round (1: no split)
+    int split_base;  // the last round's first entry
+    int grid;        // blocks: min(entries, sms)
+};
+// false when the list would exceed 2^31 - 1 units.  ws_bytes: the key
+// split's workspace (0: none).
+bool prefill_plan(int B, int Hkv, int tq, int max_q_len, int sms, int D, size_t ws_bytes,
+                  PrefillPlan *pl);
+
 // workspace (nullable, 256-byte aligned, ws_bytes long) enables the key
 // split with as many part slots as it holds.
 cudaError_t launch_prefill(const PrefillParams &p, int D, int max_q_len, void *workspace,

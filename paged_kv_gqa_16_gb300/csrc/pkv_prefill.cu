@@ -1181,6 +1181,61 @@ bool encode_map(CUtensorMap *map, const void *base, int D, int mid, long long ro
 // Chunks of at most this many pairs of query tiles get a grouped unit list.
 constexpr int kGroupMaxPairs = 4;
 
+bool prefill_plan(int B, int Hkv, int tq, int max_q_len, int sms, int D, size_t ws_bytes,
+                  PrefillPlan *pl)
+{
+    *pl = PrefillPlan{};
+    pl->split = 1;
+    if (B <= 0 || Hkv <= 0 || tq <= 0 || max_q_len <= 0 || sms <= 0)
+        return true;                                   // no units
+    // the units: pairs of query tiles (max_q_len bounds a chunk's tiles) x
+    // rows x kv heads
+    const long long tiles = ((long long)max_q_len + tq - 1) / tq;
+    const long long pairs = (tiles + 1) / 2;
+    const long long units = pairs * B * Hkv;
+    if (units > 0x7fffffffLL)
+        return false;
+    pl->pairs = (int)pairs;
+    pl->units = (int)units;
+    pl->entries = (int)units;
+    pl->split_base = (int)units;
+    // rows per group of the unit list.  A chunk of many pairs (a long causal
+    // prefill) has units from one to hundreds of key blocks: one group,
+    // pair-major, keeps each round's units of about one size.  A chunk of a
+    // few pairs (an extend, a short prompt) has units of about one size
+    // anyway: groups of about one round of units (SMs / pairs rows) keep the
+    // rows in flight few enough to share L2.
+    const long long row_heads = (long long)B * Hkv;
+    long long grp = row_heads;
+    if (pairs <= kGroupMaxPairs) {
+        grp = (long long)sms / pairs;
+        grp = grp < 1 ? 1 : (grp > row_heads ? row_heads : grp);
+    }
+    pl->group_rows = (int)grp;
+    // the key split: a last round of at most half the SMs (every unit, when
+    // they are that few) becomes up to SMs / last entries per unit, as many
+    // as the workspace has slots for; every entry of that round leaves its
+    // result in its slot and the merge kernel writes the outputs.  A
+    // pair-major list of many rounds ends on its smallest pairs (the first
+    // query tiles of long chunks: a few key blocks each), so only a grouped
+    // list (chunks of a few tile pairs, units of about one size) or a list of
+    // one round is cut.
+    const long long g0 = units < sms ? units : sms;
+    const long long last = units - (units - 1) / g0 * g0;
+    const long long slots = (long long)(ws_bytes / prefill_slot_bytes(D));
+    long long split = sms / last;
+    split = split < kPrefillMaxParts ? split : kPrefillMaxParts;
+    split = split < slots / last ? split : slots / last;
+    const bool big_last = pairs <= kGroupMaxPairs || units <= g0;
+    if (big_last && 2 * last <= sms && split >= 2) {
+        pl->split = (int)split;
+        pl->split_base = (int)(units - last);
+        pl->entries = (int)(units - last + last * split);
+    }
+    pl->grid = pl->entries < sms ? pl->entries : sms;
+    return true;
+}
+
 cudaError_t launch_prefill(const PrefillParams &p_in, int D, int max_q_len, void *workspace,
                            size_t ws_bytes, cudaStream_t stream)
 {
@@ -1204,64 +1259,30 @@ cudaError_t launch_prefill(const PrefillParams &p_in, int D, int max_q_len, void
     if ((D == 64 || D == 128) && p.total_q > 0 && p.n_rep <= 256 && p.tq >= 1 && p.tq <= 256 &&
         encode_map(&p.tmap_q, p.q, D, p.Hq, p.total_q, p.n_rep, p.tq))
         p.q_tma = 1;
-    // the units: pairs of query tiles (max_q_len bounds a chunk's tiles) x
-    // rows x kv heads
-    const long long tiles = ((long long)max_q_len + p.tq - 1) / p.tq;
-    const long long pairs = (tiles + 1) / 2;
-    const long long units = pairs * p.B * p.Hkv;
-    if (units <= 0)
-        return cudaSuccess;
-    if (units > 0x7fffffffLL)
-        return cudaErrorInvalidValue;
-    p.pairs = (int)pairs;
-    p.n_units = (int)units;
     int dev = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess)
         e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess)
         return e;
-    // rows per group of the unit list.  A chunk of many pairs (a long causal
-    // prefill) has units from one to hundreds of key blocks: one group,
-    // pair-major, keeps each round's units of about one size.  A chunk of a
-    // few pairs (an extend, a short prompt) has units of about one size
-    // anyway: groups of about one round of units (SMs / pairs rows) keep the
-    // rows in flight few enough to share L2.
-    const long long row_heads = (long long)p.B * p.Hkv;
-    long long grp = row_heads;
-    if (pairs <= kGroupMaxPairs) {
-        grp = (long long)sms / pairs;
-        grp = grp < 1 ? 1 : (grp > row_heads ? row_heads : grp);
-    }
-    p.group_rows = (int)grp;
-    // the key split: a last round of at most half the SMs (every unit, when
-    // they are that few) becomes up to SMs / last entries per unit, as many
-    // as the workspace has slots for; every entry of that region leaves its
-    // result in its slot and the merge kernel writes the outputs
-    p.split = 1;
-    p.split_base = p.n_units;
+    PrefillPlan pl;
+    if (!prefill_plan(p.B, p.Hkv, p.tq, max_q_len, sms, D, workspace != nullptr ? ws_bytes : 0,
+                      &pl))
+        return cudaErrorInvalidValue;
+    if (pl.units == 0)
+        return cudaSuccess;
+    p.pairs = pl.pairs;
+    p.n_units = pl.entries;
+    p.group_rows = pl.group_rows;
+    p.split = pl.split;
+    p.split_base = pl.split_base;
     p.ws_o = nullptr;
     p.ws_ml = nullptr;
-    if (workspace != nullptr) {
-        const long long g0 = units < sms ? units : sms;
-        const long long last = units - (units - 1) / g0 * g0;
-        const long long slots = (long long)(ws_bytes / prefill_slot_bytes(D));
-        long long split = sms / last;
-        split = split < kPrefillMaxParts ? split : kPrefillMaxParts;
-        split = split < slots / last ? split : slots / last;
-        // a pair-major list of many rounds ends on its smallest pairs (the
-        // first query tiles of long chunks: a few key blocks each), so only
-        // a grouped list (chunks of a few tile pairs, units of about one
-        // size) or a list of one round is cut
-        const bool big_last = pairs <= kGroupMaxPairs || units <= g0;
-        if (big_last && 2 * last <= sms && split >= 2) {
-            p.split = (int)split;
-            p.split_base = (int)(units - last);
-            p.n_units = (int)(units - last + last * split);
-            p.ws_o = static_cast<__nv_bfloat16 *>(workspace);
-            p.ws_ml = reinterpret_cast<float2 *>(static_cast<char *>(workspace) +
-                                                 (size_t)last * split * prefill_slot_o_bytes(D));
-        }
+    if (pl.split > 1) {
+        const size_t entries = (size_t)(pl.entries - pl.split_base);
+        p.ws_o = static_cast<__nv_bfloat16 *>(workspace);
+        p.ws_ml = reinterpret_cast<float2 *>(static_cast<char *>(workspace) +
+                                             entries * prefill_slot_o_bytes(D));
     }
     return D == 64 ? launch_prefill_d<64>(p, sms, stream) : launch_prefill_d<128>(p, sms, stream);
 }

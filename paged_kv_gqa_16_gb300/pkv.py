@@ -40,7 +40,7 @@ EXPORTS = (
     "paged_prefill_attn", "paged_kv_extend", "paged_decode_step_advance",
     "pkv_testing_set_handoff_wait_ns", "paged_decode_plan", "paged_decode_attn_planned",
     "paged_decode_step_planned", "decode_attn_contig_planned", "paged_prefill_attn_ws",
-    "pkv_prefill_workspace_bytes",
+    "pkv_prefill_workspace_bytes", "pkv_prefill_plan",
 )
 
 
@@ -103,6 +103,7 @@ def lib():
             "paged_prefill_attn": (I, [DP, P, P, I, I, P, P, P, P, P, P, P, P]),
             "paged_prefill_attn_ws": (I, [DP, P, P, I, I, P, P, P, P, P, P, Z, P, P, P]),
             "pkv_prefill_workspace_bytes": (Z, [I, I]),
+            "pkv_prefill_plan": (I, [DP, I, I, Z, P]),
             "paged_kv_extend": (I, [DP, P, P, P, P, I, P, P, P, P, P, P, I, I, P, P]),
             "pkv_testing_set_handoff_wait_ns": (I, [ctypes.c_ulonglong]),
             "pkv_status_str": (ctypes.c_char_p, [I]),
@@ -313,6 +314,16 @@ def paged_prefill_attn(d: Dims, q, qo_indptr, k_pool, v_pool, kv_indices, kv_ind
         ctypes.byref(d), _ptr(q), _ptr(qo_indptr), total_q, mq, _ptr(k_pool), _ptr(v_pool),
         _ptr(kv_indices), _ptr(kv_indptr), _ptr(seq_lens), _ptr(workspace), ws_bytes,
         _ptr(out), _ptr(status), _stream(stream)))
+
+
+def prefill_plan(d: Dims, max_q_len: int, num_sms: int, ws_bytes: int = 0) -> dict:
+    """pkv_prefill_plan: the list paged_prefill_attn(_ws) would launch."""
+    out = (ctypes.c_int32 * 7)()
+    _check("pkv_prefill_plan", lib().pkv_prefill_plan(ctypes.byref(d), int(max_q_len),
+                                                       int(num_sms), int(ws_bytes),
+                                                       ctypes.cast(out, ctypes.c_void_p)))
+    keys = ("pairs", "units", "group_rows", "entries", "split", "split_base", "grid")
+    return dict(zip(keys, list(out)))
 
 
 def prefill_workspace_bytes(D: int, num_sms: int) -> int:

@@ -272,3 +272,60 @@ def test_prefill_workspace_bytes():
     assert (2 * 128 * 128 * 2) % 256 == 0 and (2 * 128 * 64 * 2) % 256 == 0
     for D, n in [(96, 152), (256, 152), (128, 0), (128, -3), (64, 1025)]:
         assert pkv.prefill_workspace_bytes(D, n) == 0
+
+
+def _pd(B, Hq, Hkv, D, max_seq_len=8192):
+    return pkv.dims(B=B, Hq=Hq, Hkv=Hkv, D=D, page_size=16, num_pages=100000,
+                    num_indices=100000, max_seq_len=max_seq_len)
+
+
+def test_prefill_plan_bench_shapes():
+    """The list paged_prefill_attn(_ws) launches on 152 SMs for the three
+    bench shapes: the extend's 512 equal units leave a last round of 56, cut
+    in two with a workspace; the causal prefills are pair-major lists of many
+    rounds and are never cut."""
+    ws128 = pkv.prefill_workspace_bytes(128, 152)
+    ext = _pd(16, 32, 8, 128)
+    assert pkv.prefill_plan(ext, 256, 152) == dict(
+        pairs=4, units=512, group_rows=38, entries=512, split=1, split_base=512, grid=152)
+    assert pkv.prefill_plan(ext, 256, 152, ws128) == dict(
+        pairs=4, units=512, group_rows=38, entries=456 + 112, split=2, split_base=456, grid=152)
+    # 4 x 4096 at n_rep 4: 128 tiles of 32 tokens, 64 pairs, 2,048 units
+    p = pkv.prefill_plan(_pd(4, 32, 8, 128), 4096, 152, ws128)
+    assert p == dict(pairs=64, units=2048, group_rows=32, entries=2048, split=1,
+                     split_base=2048, grid=152)
+    p = pkv.prefill_plan(_pd(32, 32, 8, 64), 512, 152, pkv.prefill_workspace_bytes(64, 152))
+    assert p["units"] == 2048 and p["split"] == 1 and p["group_rows"] == 256
+
+
+def test_prefill_plan_split_rules():
+    ws = lambda n: pkv.prefill_workspace_bytes(128, n)
+    # one round (38 units of one 1,200-token row): every unit cut, 152 / 38 = 4
+    p = pkv.prefill_plan(_pd(1, 8, 2, 128), 1200, 152, ws(152))
+    assert (p["units"], p["split"], p["split_base"], p["entries"], p["grid"]) == (38, 4, 0, 152, 152)
+    # at most 16 parts a unit
+    p = pkv.prefill_plan(_pd(1, 8, 2, 128), 60, 152, ws(152))
+    assert (p["units"], p["split"], p["entries"]) == (2, 16, 32)
+    # the workspace's slots bound the parts: 5 slots for 2 units -> 2 each; 3 -> none
+    assert pkv.prefill_plan(_pd(1, 8, 2, 128), 60, 152, ws(5))["split"] == 2
+    assert pkv.prefill_plan(_pd(1, 8, 2, 128), 60, 152, ws(3))["split"] == 1
+    # a last round of more than half the SMs is not cut: 229 units, 77 in the last
+    p = pkv.prefill_plan(_pd(229, 16, 1, 128), 8, 152, ws(152))
+    assert (p["units"], p["split"]) == (229, 1)
+    p = pkv.prefill_plan(_pd(228, 16, 1, 128), 8, 152, ws(152))
+    assert (p["units"], p["split"], p["split_base"], p["entries"]) == (228, 2, 152, 304)
+    # a pair-major list of several rounds (chunks of more than 4 pairs) is not cut
+    p = pkv.prefill_plan(_pd(1, 32, 8, 128), 320, 152, ws(152))      # 5 pairs, 40 units
+    assert (p["pairs"], p["units"], p["split"]) == (5, 40, 3)        # one round: cut
+    p = pkv.prefill_plan(_pd(4, 32, 8, 128), 320, 152, ws(152))      # 160 units, 2 rounds
+    assert (p["pairs"], p["units"], p["split"]) == (5, 160, 1)
+    # nothing to run
+    assert pkv.prefill_plan(_pd(2, 8, 2, 128), 0, 152, ws(152))["units"] == 0
+
+
+def test_prefill_plan_rejects():
+    d = _pd(2, 8, 2, 128)
+    for args in [(-1, 152), (16, 0), (16, 1025)]:
+        with pytest.raises(pkv.PkvError) as e:
+            pkv.prefill_plan(d, *args)
+        assert e.value.code == pkv.PKV_ERR_INVALID_ARG
