@@ -359,6 +359,23 @@ struct PrefillUnit {
     bool table_ok;
 };
 
+// Wait for phase `parity` of `bar`; false if the time limit ran out or
+// another role aborted.  The abort flag is read only once the phase is not
+// already complete: a role that fails stops producing, so every role's next
+// wait that blocks sees the flag.
+__device__ __forceinline__ bool mbar_wait_or_abort(uint64_t *bar, uint32_t parity,
+                                                   volatile int *abort_flag)
+{
+    if (mbar_try_wait(bar, parity))
+        return true;
+    const unsigned long long t0 = global_timer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (*abort_flag || global_timer_ns() - t0 > kWaitLimitNs)
+            return false;
+    }
+    return true;
+}
+
 // 32 outputs of a row, v x inv rounded to bf16, as four 16-byte stores.
 __device__ __forceinline__ void store_out_row(__nv_bfloat16 *dst, const float (&v)[32], float inv)
 {
@@ -702,7 +719,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
             if (lane == 0) {
                 bool ok = true;
                 auto wait_only = [&](uint64_t *bar, uint32_t parity) {
-                    ok = ok && mbar_wait_bounded(bar, parity) && !*abort_flag;
+                    ok = ok && mbar_wait_or_abort(bar, parity, abort_flag);
                     return ok;
                 };
                 const bool k_generic = !p.use_tma;
@@ -730,7 +747,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
                 // tile's run has been issued, then passes the turn back
                 uint32_t turns = 0u;
                 auto take_turn = [&]() {
-                    ok = ok && mbar_wait_bounded(&turn[x], turns & 1u) && !*abort_flag;
+                    ok = ok && mbar_wait_or_abort(&turn[x], turns & 1u, abort_flag);
                     ++turns;
                     if (ok)
                         tc_fence_after();
@@ -846,7 +863,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(&xch_bar[x]);
-            const bool got = mbar_wait_bounded(&xch_bar[x], xc & 1u) && !*abort_flag;
+            const bool got = mbar_wait_or_abort(&xch_bar[x], xc & 1u, abort_flag);
             tc_fence_after();
             ++xc;
             other = buf[(h ^ 1) * C::kRows + m];
@@ -869,7 +886,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
                 (t >= 0 && m < rows_used && tok_m < ntok) ? pos_first + tok_m : kNoQuery;
             float m_run = -INFINITY, l_run = 0.f;
             for (int j = 0; j < w.n_kb; ++j) {
-                ok = mbar_wait_bounded(&s_full[x], sc & 1u) && !*abort_flag;
+                ok = mbar_wait_or_abort(&s_full[x], sc & 1u, abort_flag);
                 ++sc;
                 if (!__all_sync(kAllTc, ok)) {
                     timed_out();
@@ -958,7 +975,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
             // ---- normalise and store this tile's rows; then O is free ------
             float lo;
             ok = exchange(l_run, lo);
-            ok = ok && mbar_wait_bounded(&o_full[x], (uint32_t)(it & 1)) && !*abort_flag;
+            ok = ok && mbar_wait_or_abort(&o_full[x], (uint32_t)(it & 1), abort_flag);
             if (!__all_sync(kAllTc, ok)) {
                 timed_out();
                 break;
