@@ -45,6 +45,27 @@ constexpr long long kCombineMinItems = 128;
 constexpr int kSmemLimit = 232448;        // opt-in shared memory per block, sm_100 family
 constexpr unsigned kFull = 0xffffffffu;
 
+// Wait for phase `parity` of `bar` (limit_ns as mbar_wait_bounded: zero is one
+// non-blocking probe); false if the limit ran out or another warp aborted
+// (*abort set).  The abort word is read only once the phase is not already
+// complete: a warp that fails stops its part of the pipeline, so every other
+// warp's next wait that blocks sees the word.
+__device__ __forceinline__ bool mbar_wait_or_abort(uint64_t *bar, uint32_t parity,
+                                                   unsigned long long limit_ns,
+                                                   volatile int *abort)
+{
+    if (limit_ns == 0)
+        return mbar_test_wait(bar, parity) && !*abort;
+    if (mbar_try_wait(bar, parity))
+        return true;
+    const unsigned long long t0 = global_timer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (*abort || global_timer_ns() - t0 > limit_ns)
+            return false;
+    }
+    return true;
+}
+
 template <int D, int HPC>
 struct FusedCfg {
     static constexpr int kTok = 16;
@@ -539,9 +560,8 @@ __global__ void __launch_bounds__(FusedCfg<D, HPC>::kThreads, 1)
             // stage the row's q block (and RoPE row) for the consumers
             if (q_staged && !first_early) {
                 if (pc > 0) {
-                    const bool ok = mbar_wait_bounded(&qbar[1], (uint32_t)((pc - 1) & 1),
-                                                      p.handoff_wait_ns);
-                    if (!__all_sync(kFull, ok) || scratch[0]) {
+                    const bool ok = mbar_wait_or_abort(&qbar[1], (uint32_t)((pc - 1) & 1), p.handoff_wait_ns, scratch);
+                    if (!__all_sync(kFull, ok)) {
                         aborted = true;
                         if (lane == 0) {
                             scratch[0] = 1;
@@ -558,9 +578,8 @@ __global__ void __launch_bounds__(FusedCfg<D, HPC>::kThreads, 1)
             for (int tok = t0 + (first_early ? C::kTok : 0); tok < t1; tok += C::kTok, ++it) {
                 const int st = it % NST;
                 if (it >= NST) {
-                    const bool ok = mbar_wait_bounded(&empty[st], (uint32_t)(((it / NST) - 1) & 1),
-                                                      p.handoff_wait_ns);
-                    if (!__all_sync(kFull, ok) || scratch[0]) {
+                    const bool ok = mbar_wait_or_abort(&empty[st], (uint32_t)(((it / NST) - 1) & 1), p.handoff_wait_ns, scratch);
+                    if (!__all_sync(kFull, ok)) {
                         aborted = true;
                         if (lane == 0) {
                             scratch[0] = 1;
@@ -630,9 +649,8 @@ __global__ void __launch_bounds__(FusedCfg<D, HPC>::kThreads, 1)
             if (q_staged) {
                 // staged by the producer when it started this row
                 if (!aborted) {
-                    const bool ok = mbar_wait_bounded(&qbar[0], (uint32_t)(pc & 1),
-                                                      p.handoff_wait_ns);
-                    if (!__all_sync(kFull, ok) || scratch[0]) {
+                    const bool ok = mbar_wait_or_abort(&qbar[0], (uint32_t)(pc & 1), p.handoff_wait_ns, scratch);
+                    if (!__all_sync(kFull, ok)) {
                         aborted = true;
                         if (lane == 0) {
                             scratch[0] = 1;
@@ -715,9 +733,8 @@ __global__ void __launch_bounds__(FusedCfg<D, HPC>::kThreads, 1)
         for (int tok = t0; tok < t1; tok += C::kTok, ++it) {
             const int st = it % NST;
             if (!aborted) {
-                const bool ok = mbar_wait_bounded(&full[st], (uint32_t)((it / NST) & 1),
-                                                  p.handoff_wait_ns);
-                if (!__all_sync(kFull, ok) || scratch[0]) {
+                const bool ok = mbar_wait_or_abort(&full[st], (uint32_t)((it / NST) & 1), p.handoff_wait_ns, scratch);
+                if (!__all_sync(kFull, ok)) {
                     aborted = true;
                     if (lane == 0) {
                         scratch[0] = 1;
