@@ -197,3 +197,18 @@ def test_split_rejects_misaligned_workspace():
     with pytest.raises(pkv.PkvError) as e:
         _call(c, d, t, ws[8:], out, None, 30)
     assert e.value.code == pkv.PKV_ERR_INVALID_ARG
+
+
+def test_split_flags_bad_chunk():
+    """A chunk longer than its row is refused (PKV_FLAG_BAD_LEN) in a split
+    list too: its parts do nothing, the merge skips it, and the other rows'
+    parts (8 and 6 of them) are still right."""
+    lens, qls = [2000, 20, 1500], [50, 20, 30]
+    c = wl.prefill("psb", B=3, Hq=8, Hkv=2, D=128, page_size=16, seq_lens=lens, q_lens=qls,
+                   seed=131)
+    want = _want(c)
+    c.w.seq_lens[1] = 10                    # row 1's chunk of 20 now exceeds it
+    out, st, _ = _run_ws(c)
+    assert st & pkv.FLAG_BAD_LEN
+    compare_out(out[:50], want[:50])
+    compare_out(out[70:], want[70:])
