@@ -212,3 +212,15 @@ def test_split_flags_bad_chunk():
     assert st & pkv.FLAG_BAD_LEN
     compare_out(out[:50], want[:50])
     compare_out(out[70:], want[70:])
+
+
+@pytest.mark.parametrize("ps,D", [(5, 64), (1, 128)])
+def test_split_gathered_pages(ps, D):
+    """Page sizes the TMA path does not take (5, 1): the cp.async gather loads
+    each part's blocks from its own first key, and the last part's partial V
+    block is zero-filled."""
+    c = wl.prefill("psp", B=2, Hq=8, Hkv=2, D=D, page_size=ps, seq_lens=[1700, 1333],
+                   q_lens=[100, 77], seed=140 + ps + D)
+    out, st, _ = _run_ws(c)
+    assert st == 0
+    compare_out(out, _want(c))
