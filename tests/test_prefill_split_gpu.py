@@ -224,3 +224,14 @@ def test_split_gathered_pages(ps, D):
     out, st, _ = _run_ws(c)
     assert st == 0
     compare_out(out, _want(c))
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(8, 8), (12, 4), (48, 3)])
+def test_split_gqa_ratios(Hq, Hkv):
+    """GQA ratios 1, 3 and 16 in a split list: tiles of 128, 42 (126 rows used)
+    and 8 tokens, 8 to 39 units cut 3 to 16 ways."""
+    c = wl.prefill("psq", B=1, Hq=Hq, Hkv=Hkv, D=128, page_size=16, seq_lens=[2000],
+                   q_lens=[200], seed=150 + Hq + Hkv)
+    out, st, _ = _run_ws(c)
+    assert st == 0
+    compare_out(out, _want(c))
