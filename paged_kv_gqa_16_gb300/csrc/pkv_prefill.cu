@@ -259,8 +259,9 @@ struct PrefillCfg {
     static constexpr int kVOff = kKOff + kKStages * kKVBytes;
     static constexpr int kBarOff = kVOff + kVStages * kKVBytes;
     // k_full[KS], k_empty[KS], v_full[VS], v_empty[VS], s_full[2], p_full[2],
-    // o_full[2], o_empty[2], q_full[2], q_empty[2], drain, xch_bar[2], turn[2]
-    static constexpr int kNumBars = 2 * kKStages + 2 * kVStages + 17;
+    // o_full[2], o_empty[2], q_full[2], q_empty[2], drain, xch_bar[2], turn[2],
+    // rec_full[4], rec_empty[4]
+    static constexpr int kNumBars = 2 * kKStages + 2 * kVStages + 25;
     // a row's two halves exchange their max (and at the end their l) here:
     // [tile][block parity][half][row] floats
     static constexpr int kXchOff = kBarOff + kNumBars * 8;
@@ -270,7 +271,11 @@ struct PrefillCfg {
     // a split list's entry of each tile, by unit parity: its slot when it is
     // a part of a split unit, else -1
     static constexpr int kPartSlotOff = kAbortOff + 4;
-    static constexpr int kSmemBytes = kPartSlotOff + 16;
+    // the unit of each round, published by the K warp for the other roles:
+    // a ring of kRecs records of 16 ints
+    static constexpr int kRecs = 4;
+    static constexpr int kRecOff = kPartSlotOff + 16;
+    static constexpr int kSmemBytes = kRecOff + kRecs * 16 * 4;
     static_assert(kSmemBytes <= 232448, "shared memory per block");
     // the block holds all of tensor memory: its shared memory keeps a second
     // block off the SM (whose allocation would wait for this one's release)
@@ -468,6 +473,43 @@ __device__ __forceinline__ bool prefill_unit(const PrefillParams &p, int u, Pref
     return prefill_whole_unit(p, u, w, flag);
 }
 
+// A unit as a ring record: [0] has work, then its fields.
+__device__ __forceinline__ void unit_to_rec(int *rec, bool have, const PrefillUnit &w)
+{
+    rec[0] = have ? 1 : 0;
+    rec[1] = w.b;
+    rec[2] = w.g;
+    rec[3] = w.q0;
+    rec[4] = w.q_len;
+    rec[5] = w.L;
+    rec[6] = w.tA;
+    rec[7] = w.tB;
+    rec[8] = w.kv_end;
+    rec[9] = w.pg0;
+    rec[10] = w.kb0;
+    rec[11] = w.n_kb;
+    rec[12] = w.part_id;
+    rec[13] = w.table_ok ? 1 : 0;
+}
+
+__device__ __forceinline__ bool rec_to_unit(const int *rec, PrefillUnit &w)
+{
+    w.b = rec[1];
+    w.g = rec[2];
+    w.q0 = rec[3];
+    w.q_len = rec[4];
+    w.L = rec[5];
+    w.tA = rec[6];
+    w.tB = rec[7];
+    w.kv_end = rec[8];
+    w.pg0 = rec[9];
+    w.kb0 = rec[10];
+    w.n_kb = rec[11];
+    w.part_id = rec[12];
+    w.table_ok = rec[13] != 0;
+    return rec[0] != 0;
+}
+
 // A persistent block (one per SM) takes one unit per round of gridDim.x
 // units; every role walks the same list and keeps its ring and phase
 // counters across units, so one unit's epilogue overlaps the next unit's
@@ -488,6 +530,8 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
     uint64_t *s_full = v_empty + VS, *p_full = s_full + 2, *o_full = p_full + 2;
     uint64_t *o_empty = o_full + 2, *q_full = o_empty + 2, *q_empty = q_full + 2;
     uint64_t *drain = q_empty + 2, *xch_bar = drain + 1, *turn = xch_bar + 2;
+    uint64_t *rec_full = turn + 2, *rec_empty = rec_full + C::kRecs;
+    int *recs = reinterpret_cast<int *>(smem + C::kRecOff);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kTmemSlot);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kAbortOff);
     volatile int *part_slot = reinterpret_cast<volatile int *>(smem + C::kPartSlotOff);
@@ -502,6 +546,14 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
     auto unit_index = [&](int r) {
         const int G = (int)gridDim.x, c = (int)blockIdx.x;
         return r * G + ((r & 1) ? G - 1 - c : c);
+    };
+    // round r's unit as the K warp published it (false: the wait gave up)
+    auto take_unit = [&](int r, PrefillUnit &w, bool &have) {
+        if (!mbar_wait_or_abort(&rec_full[r % C::kRecs], (uint32_t)((r / C::kRecs) & 1),
+                                abort_flag))
+            return false;
+        have = rec_to_unit(recs + (r % C::kRecs) * 16, w);
+        return true;
     };
 
     if (tid == 0) {
@@ -526,6 +578,11 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
         mbar_init(&turn[0], 1);
         mbar_init(&turn[1], 1);
         mbar_arrive(&turn[0]);                         // tile A's run goes first
+        for (int i = 0; i < C::kRecs; ++i) {
+            mbar_init(&rec_full[i], 1);                // the K warp wrote the record
+            // every reader: the V warp, both issuing threads, 16 softmax warps
+            mbar_init(&rec_empty[i], 1 + 2 + C::kSoftmaxWarps);
+        }
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -567,9 +624,38 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
             int kb = 0;                                    // blocks issued, over all units
             int qit = 0;                                   // units whose Q the V warp loaded
             for (int r = 0; r * (int)gridDim.x < n_units && !*abort_flag; ++r) {
-                const int u = unit_index(r);
                 PrefillUnit w;
-                if (u >= n_units || !prefill_unit<kSplit>(p, u, w, is_v && lane == 0))
+                bool have = false;
+                if (!is_v) {
+                    // the K warp looks the unit up (reporting refusals once)
+                    // and publishes it for the other roles
+                    const int u = unit_index(r);
+                    have = u < n_units && prefill_unit<kSplit>(p, u, w, lane == 0);
+                    if (lane == 0) {
+                        const bool free_slot =
+                            r < C::kRecs ||
+                            mbar_wait_or_abort(&rec_empty[r % C::kRecs],
+                                               (uint32_t)((r / C::kRecs - 1) & 1), abort_flag);
+                        if (free_slot) {
+                            unit_to_rec(recs + (r % C::kRecs) * 16, have, w);
+                            mbar_arrive(&rec_full[r % C::kRecs]);
+                        } else {
+                            fail();
+                        }
+                    }
+                    __syncwarp();
+                } else {
+                    const bool got = __all_sync(kAllTc, take_unit(r, w, have));
+                    __syncwarp();
+                    if (lane == 0 && got)
+                        mbar_arrive(&rec_empty[r % C::kRecs]);
+                    if (!got) {
+                        if (lane == 0)
+                            fail();
+                        break;
+                    }
+                }
+                if (!have)
                     continue;
                 // the V warp also loads the unit's Q (row m = token m / n_rep,
                 // head m % n_rep, swizzled like K), each tile's once the previous
@@ -757,9 +843,18 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
                 int kb = 0, it = 0;                        // blocks and units consumed
                 uint32_t pc = 0u;                          // P hand-offs consumed
                 for (int r = 0; r * (int)gridDim.x < n_units && ok; ++r) {
-                    const int u = unit_index(r);
+                    // round r's unit from the K warp's record
+                    const int rs = r % C::kRecs;
+                    const int *rec = recs + rs * 16;
+                    if (!wait_only(&rec_full[rs], (uint32_t)((r / C::kRecs) & 1)))
+                        break;
+                    const bool have = rec[0] != 0;
                     PrefillUnit w;
-                    if (u >= n_units || !prefill_unit<kSplit>(p, u, w, false))
+                    w.kv_end = rec[8];
+                    w.kb0 = rec[10];
+                    w.n_kb = rec[11];
+                    mbar_arrive(&rec_empty[rs]);
+                    if (!have)
                         continue;
                     const int n_kb = w.n_kb;
                     if (!wait_only(&q_full[x], (uint32_t)(it & 1)) ||
@@ -871,21 +966,37 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
         };
         int it = 0;
         for (int r = 0; r * (int)gridDim.x < n_units && ok; ++r) {
-            const int u = unit_index(r);
-            PrefillUnit w;
-            if (u >= n_units || !prefill_unit<kSplit>(p, u, w, false))
+            // round r's unit from the K warp's record, each field read where
+            // it is used (the slot is released after the epilogue)
+            const int rs = r % C::kRecs;
+            const int *rec = recs + rs * 16;
+            ok = mbar_wait_or_abort(&rec_full[rs], (uint32_t)((r / C::kRecs) & 1), abort_flag);
+            if (!__all_sync(kAllTc, ok)) {
+                timed_out();
+                break;
+            }
+            auto release = [&]() {
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&rec_empty[rs]);
+            };
+            if (rec[0] == 0) {
+                release();
                 continue;
+            }
             if (kSplit && m == 0 && h == 0)
-                part_slot[2 * x + (it & 1)] = w.part_id >= 0 ? w.part_id >> 9 : -1;
-            const int t = x == 0 ? w.tA : w.tB;
-            const int ntok = t >= 0 ? min(tq, w.q_len - t * tq) : 0;
+                part_slot[2 * x + (it & 1)] = rec[12] >= 0 ? rec[12] >> 9 : -1;
+            const int t = rec[x == 0 ? 6 : 7];
+            const int q_len = rec[4];
+            const int ntok = t >= 0 ? min(tq, q_len - t * tq) : 0;
             // positions counted from the entry's first key (a part of a split
             // unit starts at block kb0); a row with no query masks every key
-            const int pos_first = w.L - w.q_len + (t >= 0 ? t * tq : 0) - w.kb0 * C::kKeys;
+            const int pos_first = rec[5] - q_len + (t >= 0 ? t * tq : 0) - rec[10] * C::kKeys;
             const int pos =
                 (t >= 0 && m < rows_used && tok_m < ntok) ? pos_first + tok_m : kNoQuery;
             float m_run = -INFINITY, l_run = 0.f;
-            for (int j = 0; j < w.n_kb; ++j) {
+            const int n_kb = rec[11];
+            for (int j = 0; j < n_kb; ++j) {
                 ok = mbar_wait_or_abort(&s_full[x], sc & 1u, abort_flag);
                 ++sc;
                 if (!__all_sync(kAllTc, ok)) {
@@ -997,7 +1108,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
             } else if (pos != kNoQuery) {
                 const int hh = m - tok_m * n_rep;
                 orow = p.out +
-                       ((size_t)(w.q0 + t * tq + tok_m) * p.Hq + (size_t)w.g * n_rep + hh) * D +
+                       ((size_t)(rec[3] + t * tq + tok_m) * p.Hq + (size_t)rec[2] * n_rep + hh) * D +
                        (D / 2) * h;
             }
 #pragma unroll 1
@@ -1011,6 +1122,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(&o_empty[x]);
+            release();
             ++it;
         }
     }
