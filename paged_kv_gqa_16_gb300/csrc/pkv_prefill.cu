@@ -151,6 +151,25 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32])
         v[i] = __uint_as_float(r[i]);
 }
 
+// One fp32 column of this thread's TMEM lane: load (and wait), store.
+__device__ __forceinline__ float tmem_ld1(uint32_t taddr)
+{
+    uint32_t r;
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];\n\t"
+                 "tcgen05.wait::ld.sync.aligned;"
+                 : "=r"(r)
+                 : "r"(taddr)
+                 : "memory");
+    return __uint_as_float(r);
+}
+
+__device__ __forceinline__ void tmem_st1(uint32_t taddr, float v)
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr),
+                 "r"(__float_as_uint(v))
+                 : "memory");
+}
+
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32])
 {
     asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {"
@@ -257,7 +276,7 @@ struct PrefillCfg {
     static constexpr int kKVBytes = D / 64 * kRegionBytes; // one K or V block
     static constexpr int kKOff = 2 * kQBytes;
     static constexpr int kVOff = kKOff + kKStages * kKVBytes;
-    static constexpr int kBarOff = kVOff + kVStages * kKVBytes;
+    static constexpr int kBarOff = kVOff + kVStages * kKVBytes + (D <= 64 ? kRegionBytes : 0);
     // k_full[KS], k_empty[KS], v_full[VS], v_empty[VS], s_full[2], p_full[2],
     // o_full[2], o_empty[2], q_full[2], q_empty[2], drain, xch_bar[2], turn[2],
     // rec_full[4], rec_empty[4]
@@ -281,7 +300,15 @@ struct PrefillCfg {
     // block off the SM (whose allocation would wait for this one's release)
     static_assert(2 * (kSmemBytes + 1024) > 233472, "one block per SM");
     static constexpr uint32_t kTmemCols = 512;
-    static constexpr uint32_t kOCol = 256;
+    // At D = 64 the row sums l come from the tensor cores: V gets 16 more
+    // columns, all ones (one shared 128-key region of ones after the V ring,
+    // the descriptor's LBO reaching it from each slot), so P V writes
+    // l = sum of the row's bf16 P into O's column D (kOnesL).  At D = 128
+    // tensor memory has no room for them.
+    static constexpr bool kOnesL = D <= 64;
+    static constexpr int kON = kOnesL ? D + 16 : D;        // columns of a tile's O
+    static constexpr int kOnesOff = kVOff + kVStages * kKVBytes;  // the ones region (16 KB at D = 64)
+    static constexpr uint32_t kOCol = 256;                 // O of tile x at kOCol + kON x
 };
 
 // Shared-memory descriptor of a 128-byte-swizzled operand (layout type 2).
@@ -593,6 +620,14 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
+    if constexpr (C::kOnesL) {
+        // bf16 1.0 in every column of the ones region (whatever the swizzle,
+        // each of the 16 columns the products read is 1), for the tensor cores
+        uint4 *ones = reinterpret_cast<uint4 *>(smem + C::kOnesOff);
+        for (int i = tid; i < C::kRegionBytes / 16; i += C::kThreads)
+            ones[i] = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+        fence_proxy_async_smem();
+    }
     grid_dependency_wait();
     tc_fence_before();
     __syncthreads();
@@ -791,7 +826,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
             // cores always have a run queued.
             const int x = warp == C::kMmaWarpB ? 1 : 0;
             constexpr uint32_t kIdescS = instr_desc(128, C::kKeys, 0);
-            constexpr uint32_t kIdescO = instr_desc(128, D, 1);
+            constexpr uint32_t kIdescO = instr_desc(128, C::kON, 1);
             // Q and K: 128-byte swizzle, K-major: 8-row groups 1 KB apart (SBO),
             // a 16-dim step 32 bytes into the row, the next 64 dims in the next
             // region.  V: 128-byte swizzle, MN-major: 64-dim atoms one region
@@ -822,10 +857,16 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
                     }
                 };
                 auto issue_pv = [&](int vslot, bool first) {
-                    const uint64_t dv_s = dv + (uint64_t)((vslot * C::kKVBytes) >> 4);
+                    // at D = 64 the second 64-column atom of V (its columns 64..79:
+                    // ones) is the ones region, LBO bytes on from the slot
+                    const uint64_t dv_s =
+                        C::kOnesL ? smem_desc_sw128(sbase + C::kVOff + vslot * C::kKVBytes,
+                                                    C::kOnesOff - C::kVOff - vslot * C::kKVBytes,
+                                                    1024)
+                                  : dv + (uint64_t)((vslot * C::kKVBytes) >> 4);
 #pragma unroll
                     for (int s = 0; s < C::kKeys / 16; ++s)
-                        umma_ta(tmem + C::kOCol + D * x, tmem + 128 * x + 8 * s,
+                        umma_ta(tmem + C::kOCol + C::kON * x, tmem + 128 * x + 8 * s,
                                 dv_s + (uint64_t)((s * 16 * 128) >> 4), kIdescO,
                                 (!first || s > 0) ? 1u : 0u);
                 };
@@ -937,7 +978,8 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
         const int tok_m = m / n_rep;
         const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
         const uint32_t t_s = tmem + 128 * x + lane_off;
-        const uint32_t t_o = tmem + C::kOCol + D * x + (D / 2) * h + lane_off;
+        const uint32_t t_o = tmem + C::kOCol + C::kON * x + (D / 2) * h + lane_off;
+        const uint32_t t_l = tmem + C::kOCol + C::kON * x + D + lane_off;  // kOnesL: l
         float *xch = reinterpret_cast<float *>(smem + C::kXchOff) + x * 2 * 2 * C::kRows;
         const float sl2 = p.scale_log2;
         bool ok = true;
@@ -1039,7 +1081,8 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
                 if (rebase) {
                     alpha = ex2_fast(m_run - mx);      // 0 while m_run is -inf
                     m_run = mx;
-                    l_run *= alpha;
+                    if constexpr (!C::kOnesL)
+                        l_run *= alpha;
                 }
                 const float nbase = m_run == -INFINITY ? 0.f : -m_run;
                 const uint64_t scale2 = f32x2(sl2, sl2), base2 = f32x2(nbase, nbase);
@@ -1058,10 +1101,13 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
                     ffma2(y0, y1, sv[2 * i], sv[2 * i + 1], scale2, base2);
                     const float e0 = ex2_fast(y0), e1 = ex2_fast(y1);
                     pw[i] = pack_bf16x2(e0, e1);
-                    fadd2(ls[2 * (i & 3)], ls[2 * (i & 3) + 1], e0, e1);
+                    if constexpr (!C::kOnesL)       // at D = 64 P V sums l
+                        fadd2(ls[2 * (i & 3)], ls[2 * (i & 3) + 1], e0, e1);
                 }
                 tmem_st32w(t_s + 32 * h, pw);
-                l_run += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+                if constexpr (!C::kOnesL)
+                    l_run += ((ls[0] + ls[1]) + (ls[2] + ls[3])) +
+                             ((ls[4] + ls[5]) + (ls[6] + ls[7]));
                 // O is quiescent here: the commit behind this S covered the
                 // last P V, and the next one waits for this P
                 if (__any_sync(kAllTc, rebase && j > 0)) {
@@ -1074,6 +1120,8 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
                             v[i] *= alpha;
                         tmem_st32(t_o + c0, v);
                     }
+                    if (C::kOnesL && h == 1)          // l, O's column D, once
+                        tmem_st1(t_l, tmem_ld1(t_l) * alpha);
                 }
                 tmem_st_wait();
                 tc_fence_before();
@@ -1084,15 +1132,17 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
             if (!ok)
                 break;
             // ---- normalise and store this tile's rows; then O is free ------
-            float lo;
-            ok = exchange(l_run, lo);
+            float lo = 0.f;
+            if constexpr (!C::kOnesL)
+                ok = exchange(l_run, lo);
             ok = ok && mbar_wait_or_abort(&o_full[x], (uint32_t)(it & 1), abort_flag);
             if (!__all_sync(kAllTc, ok)) {
                 timed_out();
                 break;
             }
             tc_fence_after();
-            const float l_row = l_run + lo;
+            // the row's l: both halves' sums, or at D = 64 O's column D
+            const float l_row = C::kOnesL ? tmem_ld1(t_l) : l_run + lo;
             const float inv = l_row > 0.f ? 1.f / l_row : 0.f;
             // a part of a split unit stores its rows like any entry, into its
             // workspace slot, with the row's (base, l) beside them for the
