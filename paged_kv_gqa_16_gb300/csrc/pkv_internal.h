@@ -135,6 +135,9 @@ struct PrefillParams {
     int split_base;
     __nv_bfloat16 *ws_o;
     float2 *ws_ml;
+    // out is 32-byte aligned: rows are stored with 32-byte stores (set by
+    // launch_prefill; otherwise 16-byte stores, each lane its own row)
+    int out_align32;
 };
 
 // The prefill's key split.  When the unit list's last round would leave at

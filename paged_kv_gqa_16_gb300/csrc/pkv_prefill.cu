@@ -408,6 +408,60 @@ __device__ __forceinline__ bool mbar_wait_or_abort(uint64_t *bar, uint32_t parit
     return true;
 }
 
+__device__ __forceinline__ void st_global_v8(void *dst, const uint32_t (&w)[8])
+{
+    asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(dst), "r"(w[0]),
+                 "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                 : "memory");
+}
+
+// Each lane's N consecutive outputs of its row (dst, 32-byte aligned;
+// nullptr: none), v x inv rounded to bf16, stored by the whole warp.  A
+// lane's outputs are G = N / 16 pieces of 32 bytes; the G lanes of each
+// group first trade pieces (a G x G transpose by XOR shuffles), so that
+// lane j holds piece j of the group's G rows and each store instruction
+// writes whole runs of N x 2 bytes: 32 / G runs per instruction instead of
+// 32 scattered pieces, far fewer cache-line requests for the load/store
+// unit, which the block's shared-memory traffic and barriers also use.
+template <int N>
+__device__ __forceinline__ void store_rows_warp(__nv_bfloat16 *dst, const float (&v)[N], float inv,
+                                                int lane)
+{
+    constexpr int G = N / 16;
+    uint32_t w[G][8];
+#pragma unroll
+    for (int c = 0; c < G; ++c)
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            w[c][i] = pack_bf16x2(v[16 * c + 2 * i] * inv, v[16 * c + 2 * i + 1] * inv);
+    const int j = lane & (G - 1);
+#pragma unroll
+    for (int s = 1; s < G; s <<= 1) {
+        const bool hi = (j & s) != 0;
+#pragma unroll
+        for (int c = 0; c < G; ++c) {
+            if (c & s)
+                continue;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const uint32_t got = __shfl_xor_sync(kAllTc, hi ? w[c][i] : w[c | s][i], s);
+                if (hi)
+                    w[c][i] = got;
+                else
+                    w[c | s][i] = got;
+            }
+        }
+    }
+    const unsigned long long mine = reinterpret_cast<unsigned long long>(dst);
+    const int b = lane & ~(G - 1);
+#pragma unroll
+    for (int k = 0; k < G; ++k) {
+        const unsigned long long row = __shfl_sync(kAllTc, mine, b + k);
+        if (row != 0ull)
+            st_global_v8(reinterpret_cast<uint32_t *>(row) + 8 * j, w[k]);
+    }
+}
+
 // 32 outputs of a row, v x inv rounded to bf16, as four 16-byte stores.
 __device__ __forceinline__ void store_out_row(__nv_bfloat16 *dst, const float (&v)[32], float inv)
 {
@@ -1161,12 +1215,22 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
                        ((size_t)(rec[3] + t * tq + tok_m) * p.Hq + (size_t)rec[2] * n_rep + hh) * D +
                        (D / 2) * h;
             }
+            if (slot >= 0 || p.out_align32) {
+                // the warp's rows in whole runs of 32-byte stores
+                float ov[D / 2];
+                if constexpr (D / 2 == 64)
+                    tmem_ld64(t_o, ov);
+                else
+                    tmem_ld32(t_o, ov);
+                store_rows_warp<D / 2>(orow, ov, inv, lane);
+            } else {
 #pragma unroll 1
-            for (int c0 = 0; c0 < D / 2; c0 += 32) {
-                float v[32];
-                tmem_ld32(t_o + c0, v);
-                if (orow != nullptr)
-                    store_out_row(orow + c0, v, inv);
+                for (int c0 = 0; c0 < D / 2; c0 += 32) {
+                    float v[32];
+                    tmem_ld32(t_o + c0, v);
+                    if (orow != nullptr)
+                        store_out_row(orow + c0, v, inv);
+                }
             }
             tc_fence_before();
             __syncwarp();
@@ -1422,6 +1486,7 @@ cudaError_t launch_prefill(const PrefillParams &p_in, int D, int max_q_len, void
     // swizzle atoms; a 128-key block is whole pages or a part of one) and
     // every row index fits the copy's 32-bit coordinate
     PrefillParams p = p_in;
+    p.out_align32 = (reinterpret_cast<uintptr_t>(p.out) & 31) == 0;
     p.use_tma = 0;
     p.tma_rows = 0;
     const long long rows = (long long)p.num_pages * p.page_size;

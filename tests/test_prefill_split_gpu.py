@@ -6,7 +6,8 @@ their fp32 (base, l) in the workspace and a merge kernel combines them.  Cases: 
 rows (the units of many key blocks split, the causal diagonal in a unit's
 last part), a list whose last round alone is split, a mix of split and
 unsplit units in one round, workspaces with room for fewer parts, a
-workspace full of garbage, and graph replay.  Tolerance as for
+workspace full of garbage, graph replay, and outputs only 16-byte aligned
+(the 16-byte row stores).  Tolerance as for
 paged_prefill_attn: max-abs 2e-2, mean-abs 2e-3."""
 
 import numpy as np
@@ -234,4 +235,26 @@ def test_split_gqa_ratios(Hq, Hkv):
                    q_lens=[200], seed=150 + Hq + Hkv)
     out, st, _ = _run_ws(c)
     assert st == 0
+    compare_out(out, _want(c))
+
+
+@pytest.mark.parametrize("D,ws", [(64, False), (128, False), (128, True)])
+def test_out_16_byte_aligned(D, ws):
+    """An output 16 but not 32 bytes aligned takes the 16-byte row stores
+    (the 32-byte stores need 32): the same values.  With a workspace the
+    split parts still store theirs with 32-byte stores, into the workspace."""
+    c = wl.prefill("pso", B=2, Hq=12, Hkv=4, D=D, page_size=16, seq_lens=[1500, 700],
+                   q_lens=[90, 33], seed=160 + D + ws)
+    w = c.w
+    d, t = _setup(c)
+    n = c.total_q * w.Hq * w.D
+    buf = torch.full((n + 64,), float("nan"), dtype=torch.bfloat16, device="cuda")
+    off = next(i for i in range(0, 64, 8) if (buf.data_ptr() + 2 * i) % 32 == 16)
+    out = buf[off:off + n].view(c.total_q, w.Hq, w.D)
+    wsb = (torch.empty(pkv.prefill_workspace_bytes(D, _sms()), dtype=torch.uint8, device="cuda")
+           if ws else None)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    _call(c, d, t, wsb, out, st, 90)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
     compare_out(out, _want(c))
