@@ -415,17 +415,19 @@ __device__ __forceinline__ void st_global_v8(void *dst, const uint32_t (&w)[8])
                  : "memory");
 }
 
-// Each lane's N consecutive outputs of its row (dst, 32-byte aligned;
+// Each lane's N consecutive outputs of its row (dst, 16-byte aligned;
 // nullptr: none), v x inv rounded to bf16, stored by the whole warp.  A
 // lane's outputs are G = N / 16 pieces of 32 bytes; the G lanes of each
 // group first trade pieces (a G x G transpose by XOR shuffles), so that
 // lane j holds piece j of the group's G rows and each store instruction
 // writes whole runs of N x 2 bytes: 32 / G runs per instruction instead of
 // 32 scattered pieces, far fewer cache-line requests for the load/store
-// unit, which the block's shared-memory traffic and barriers also use.
+// unit, which the block's shared-memory traffic and barriers also use.  A
+// piece is one 32-byte store when every dst is 32-byte aligned (wide), else
+// two 16-byte stores.
 template <int N>
 __device__ __forceinline__ void store_rows_warp(__nv_bfloat16 *dst, const float (&v)[N], float inv,
-                                                int lane)
+                                                int lane, bool wide)
 {
     constexpr int G = N / 16;
     uint32_t w[G][8];
@@ -457,21 +459,17 @@ __device__ __forceinline__ void store_rows_warp(__nv_bfloat16 *dst, const float 
 #pragma unroll
     for (int k = 0; k < G; ++k) {
         const unsigned long long row = __shfl_sync(kAllTc, mine, b + k);
-        if (row != 0ull)
-            st_global_v8(reinterpret_cast<uint32_t *>(row) + 8 * j, w[k]);
+        uint32_t *piece = reinterpret_cast<uint32_t *>(row) + 8 * j;
+        if (row != 0ull) {
+            if (wide) {
+                st_global_v8(piece, w[k]);
+            } else {
+                *reinterpret_cast<uint4 *>(piece) = make_uint4(w[k][0], w[k][1], w[k][2], w[k][3]);
+                *reinterpret_cast<uint4 *>(piece + 4) =
+                    make_uint4(w[k][4], w[k][5], w[k][6], w[k][7]);
+            }
+        }
     }
-}
-
-// 32 outputs of a row, v x inv rounded to bf16, as four 16-byte stores.
-__device__ __forceinline__ void store_out_row(__nv_bfloat16 *dst, const float (&v)[32], float inv)
-{
-#pragma unroll
-    for (int q = 0; q < 4; ++q)
-        *reinterpret_cast<uint4 *>(dst + 8 * q) =
-            make_uint4(pack_bf16x2(v[8 * q] * inv, v[8 * q + 1] * inv),
-                       pack_bf16x2(v[8 * q + 2] * inv, v[8 * q + 3] * inv),
-                       pack_bf16x2(v[8 * q + 4] * inv, v[8 * q + 5] * inv),
-                       pack_bf16x2(v[8 * q + 6] * inv, v[8 * q + 7] * inv));
 }
 
 // Unit u of the list: rows (b x Hkv + g) in groups of p.group_rows, the
@@ -1195,48 +1193,46 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
                 break;
             }
             tc_fence_after();
-            // the row's l: both halves' sums, or at D = 64 O's column D
+            // this thread's D / 2 columns of O and the row's l (both halves'
+            // sums, or at D = 64 O's column D) into registers: O is then
+            // free.  Its hand-off and the record's release go before the
+            // row's stores, since an arrival orders the thread's earlier
+            // global stores and would wait for them to complete.
             const float l_row = C::kOnesL ? tmem_ld1(t_l) : l_run + lo;
-            const float inv = l_row > 0.f ? 1.f / l_row : 0.f;
+            float ov[D / 2];
+            if constexpr (D / 2 == 64)
+                tmem_ld64(t_o, ov);
+            else
+                tmem_ld32(t_o, ov);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&o_empty[x]);
             // a part of a split unit stores its rows like any entry, into its
             // workspace slot, with the row's (base, l) beside them for the
             // merge kernel (its slot was published at the unit's start, two
             // exchanges ago)
             __nv_bfloat16 *orow = nullptr;
+            float2 *mlrow = nullptr;
             const int slot = kSplit ? part_slot[2 * x + (it & 1)] : -1;
             if (slot >= 0) {
                 const size_t tile = (size_t)slot * 2 + x;
                 orow = p.ws_o + (tile * C::kRows + m) * D + (D / 2) * h;
                 if (h == 0)
-                    p.ws_ml[tile * C::kRows + m] = make_float2(m_run, l_row);
+                    mlrow = p.ws_ml + tile * C::kRows + m;
             } else if (pos != kNoQuery) {
                 const int hh = m - tok_m * n_rep;
                 orow = p.out +
                        ((size_t)(rec[3] + t * tq + tok_m) * p.Hq + (size_t)rec[2] * n_rep + hh) * D +
                        (D / 2) * h;
             }
-            if (slot >= 0 || p.out_align32) {
-                // the warp's rows in whole runs of 32-byte stores
-                float ov[D / 2];
-                if constexpr (D / 2 == 64)
-                    tmem_ld64(t_o, ov);
-                else
-                    tmem_ld32(t_o, ov);
-                store_rows_warp<D / 2>(orow, ov, inv, lane);
-            } else {
-#pragma unroll 1
-                for (int c0 = 0; c0 < D / 2; c0 += 32) {
-                    float v[32];
-                    tmem_ld32(t_o + c0, v);
-                    if (orow != nullptr)
-                        store_out_row(orow + c0, v, inv);
-                }
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(&o_empty[x]);
             release();
+            const float inv = l_row > 0.f ? 1.f / l_row : 0.f;
+            if (mlrow != nullptr)
+                *mlrow = make_float2(m_run, l_row);
+            // whole runs, by 32-byte stores where the output allows them
+            // (the workspace always does)
+            store_rows_warp<D / 2>(orow, ov, inv, lane, slot >= 0 || p.out_align32);
             ++it;
         }
     }
