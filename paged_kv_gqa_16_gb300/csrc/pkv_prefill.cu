@@ -1210,8 +1210,9 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
                 mbar_arrive(&o_empty[x]);
             // a part of a split unit stores its rows like any entry, into its
             // workspace slot, with the row's (base, l) beside them for the
-            // merge kernel (its slot was published at the unit's start, two
-            // exchanges ago)
+            // merge kernel (its slot was published at the unit's start; the
+            // max exchange of every block since orders that write before
+            // this read)
             __nv_bfloat16 *orow = nullptr;
             float2 *mlrow = nullptr;
             const int slot = kSplit ? part_slot[2 * x + (it & 1)] : -1;
