@@ -258,7 +258,7 @@ struct PrefillCfg {
     static constexpr int kRows = 128;                      // query rows of one tile
     static constexpr int kKeys = 128;                      // keys of one K/V block
     static constexpr int kKStages = D <= 64 ? 4 : 2;
-    static constexpr int kVStages = D <= 64 ? 4 : 2;
+    static constexpr int kVStages = D <= 64 ? 4 : 3;
     // warps 0-7: softmax of tile A, 8-15: tile B (a row's two threads, in
     // warpgroups 2x and 2x + 1, take 64 of a block's 128 keys each); warp
     // 16: tensor-memory owner and tile A's products; warp 17: K loads; warp
@@ -282,9 +282,15 @@ struct PrefillCfg {
     // rec_full[4], rec_empty[4]
     static constexpr int kNumBars = 2 * kKStages + 2 * kVStages + 25;
     // a row's two halves exchange their max (and at the end their l) here:
-    // [tile][block parity][half][row] floats
+    // [tile][half][row] floats, one buffer (which leaves room for the third V
+    // stage at D = 128).  A half's next write is ordered after its partner's
+    // read of the last value: within a unit by P -> next S (the issuing
+    // thread waits for every warp's P before the S behind the next write);
+    // the l after the last max by the wait for the unit's last P V; a new
+    // unit's first max after the l by a wait for o_empty (every warp of the
+    // tile has read its l and O)
     static constexpr int kXchOff = kBarOff + kNumBars * 8;
-    static constexpr int kXchBytes = 2 * 2 * 2 * kRows * 4;
+    static constexpr int kXchBytes = 2 * 2 * kRows * 4;
     static constexpr int kTmemSlot = kXchOff + kXchBytes;
     static constexpr int kAbortOff = kTmemSlot + 4;
     // a split list's entry of each tile, by unit parity: its slot when it is
@@ -1032,7 +1038,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
         const uint32_t t_s = tmem + 128 * x + lane_off;
         const uint32_t t_o = tmem + C::kOCol + C::kON * x + (D / 2) * h + lane_off;
         const uint32_t t_l = tmem + C::kOCol + C::kON * x + D + lane_off;  // kOnesL: l
-        float *xch = reinterpret_cast<float *>(smem + C::kXchOff) + x * 2 * 2 * C::kRows;
+        float *xch = reinterpret_cast<float *>(smem + C::kXchOff) + x * 2 * C::kRows;
         const float sl2 = p.scale_log2;
         bool ok = true;
         auto timed_out = [&]() {
@@ -1046,7 +1052,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
         // half's (false: the wait timed out).  The tensor-memory fences order
         // each half's reads of S before the other half's P overwrites them.
         auto exchange = [&](float v, float &other) {
-            float *buf = xch + (xc & 1u) * 2 * C::kRows;
+            float *buf = xch;
             buf[h * C::kRows + m] = v;
             tc_fence_before();
             __syncwarp();
@@ -1090,6 +1096,15 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
                 (t >= 0 && m < rows_used && tok_m < ntok) ? pos_first + tok_m : kNoQuery;
             float m_run = -INFINITY, l_run = 0.f;
             const int n_kb = rec[11];
+            // the partner half has read the previous unit's l (it loaded O
+            // after it) before this unit's first max overwrites it
+            if (!C::kOnesL && it > 0) {
+                ok = mbar_wait_or_abort(&o_empty[x], (uint32_t)((it - 1) & 1), abort_flag);
+                if (!__all_sync(kAllTc, ok)) {
+                    timed_out();
+                    break;
+                }
+            }
             for (int j = 0; j < n_kb; ++j) {
                 ok = mbar_wait_or_abort(&s_full[x], sc & 1u, abort_flag);
                 ++sc;
@@ -1184,10 +1199,12 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
             if (!ok)
                 break;
             // ---- normalise and store this tile's rows; then O is free ------
+            // the last P V done (every warp's last P, so the partner's read of
+            // the last max, came before it), then the halves' l
+            ok = mbar_wait_or_abort(&o_full[x], (uint32_t)(it & 1), abort_flag);
             float lo = 0.f;
             if constexpr (!C::kOnesL)
-                ok = exchange(l_run, lo);
-            ok = ok && mbar_wait_or_abort(&o_full[x], (uint32_t)(it & 1), abort_flag);
+                ok = ok && exchange(l_run, lo);
             if (!__all_sync(kAllTc, ok)) {
                 timed_out();
                 break;
