@@ -22,12 +22,15 @@
 //   - S = Q K^T (M 128, N 128, K = D in steps of 16) goes to tensor memory;
 //   - a row's two threads each read half of its S (64 keys), mask keys past
 //     its position, exchange their halves' max, update the fp32 online
-//     softmax (log2 domain, the scale folded into one FFMA per exponent, l
-//     from the fp32 terms), rescale their halves of O in tensor memory only
-//     when the max has grown by more than 2^8, and write P (bf16) back over
-//     S;
+//     softmax (log2 domain, the scale folded into one FFMA per exponent; l
+//     from the fp32 terms at D = 128), rescale their halves of O in tensor
+//     memory only when the max has grown by more than 2^8, and write P
+//     (bf16) back over S;
 //   - O += P V (M 128, N = D, K = 128) takes P from tensor memory and V
-//     (MN-major) from shared memory;
+//     (MN-major) from shared memory; at D = 64 V has 16 more columns of
+//     ones (N = 80), so the product also sums l;
+//   - at a unit's end each thread loads its half row of O, hands O back,
+//     and its lane group stores the rows in whole runs;
 //   - tile A's products are issued by one thread and tile B's by another,
 //     taking turns one run at a time, so each makes its waits and commits
 //     while the other's run goes out.
@@ -1026,11 +1029,10 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
         // warps 0-7 run tile A, 8-15 tile B; warpgroup h of a tile takes keys
         // [64 h, 64 h + 64) of each 128-key block, so a row's two threads
         // (one tensor-memory lane) each handle half of its keys.  Per block
-        // they exchange their halves' max through shared memory (buffers
-        // alternating with the block, one mbarrier phase per block and tile),
-        // keep their own part of l, and each rescales and stores its D / 2
-        // columns of O.  The hand-offs to the MMA thread take one arrival per
-        // warp.
+        // they exchange their halves' max through shared memory (one buffer,
+        // one mbarrier phase per block and tile), keep their own part of l
+        // (at D = 128), and each rescales and stores its D / 2 columns of O.
+        // The hand-offs to the MMA thread take one arrival per warp.
         const int x = warp >> 3, h = (warp >> 2) & 1;
         const int m = tid & (C::kRows - 1);
         const int tok_m = m / n_rep;
