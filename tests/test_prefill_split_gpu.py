@@ -238,7 +238,7 @@ def test_split_gqa_ratios(Hq, Hkv):
     compare_out(out, _want(c))
 
 
-@pytest.mark.parametrize("D,ws", [(64, False), (128, False), (128, True)])
+@pytest.mark.parametrize("D,ws", [(64, False), (64, True), (128, False), (128, True)])
 def test_out_16_byte_aligned(D, ws):
     """An output 16 but not 32 bytes aligned takes the 16-byte row stores
     (the 32-byte stores need 32): the same values.  With a workspace the
